@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA recurrent-state hot path on one GB300 per rank.
+
+Main line: speculative-decode verify + ReplaySSM commit, 16 sequences x 32
+heads x d=128, bf16 inputs, fp32 state in 64 shuffled slots, T = 8 drafts,
+accepted_len ~ U{0..8}, ring depth 8.  One step = one decode step of the
+model's KDA layers: for each of NL layers, kda_verify (which also applies the
+previous step's commit) then kda_commit.  NL layers have their own state
+pools, so the state touched per step is NL x 32 MiB, at least 4x the L2.  The
+value is drafted tokens verified through one KDA layer per second,
+B * T * NL * steps / time.  Each step is one CUDA graph captured from the
+public API calls, with timing events around every verify launch.
+
+Extra keys: `roofline` (verify kernel vs HBM), `cpu_baseline` (the fp64
+oracle on the host cores, bounded sample), `e2e` (same metric with the
+step's inputs copied from pinned host memory and outputs copied back inside
+the timed region), `prefill` (chunked prefill with in-pass checkpoints,
+1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region),
+`clocks` (nvidia-smi samples during the timed region).
+
+`--impl reference` times the oracle itself on the host cores on the same
+workload (rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import kda_inputs as ki  # noqa: E402
+
+METRIC = "KDA verify+commit tokens/s, % of HBM roofline; chunked-prefill tokens/s"
+B, H, D, P, T, DEPTH = 16, 32, 128, 64, 8, 8
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle CPU-baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def unit_bytes(a_prev, d=D, t=T):
+    """Algorithmic HBM bytes of one (sequence, head) unit of one verify launch:
+    state read, state write when the pending commit is non-empty, the T drafted
+    tokens' inputs (q, k, v, alpha bf16 + beta), their fp32 outputs, ring write
+    of (k, v, alpha, beta) for T tokens, ring read of a_prev entries, slot and
+    ctrl words."""
+    ring_tok = 3 * d * 2 + 2
+    return (d * d * 4 + d * d * 4 * (a_prev > 0) + t * (4 * d * 2 + 2)
+            + t * d * 4 + t * ring_tok + a_prev * ring_tok + 8)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                pk = json.load(f)
+            if pk.get("hbm_gbs"):
+                return float(pk["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def verify_source_hash():
+    src = os.path.join(ROOT, "recurrent_kda_state_gb300", "csrc", "kda_verify.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "verify_spec_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_sha256_16") == verify_source_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1] or \
+               [s for (_, s) in self.samples]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_spec_rate(seconds, heads_sampled=2, seed=ki.SEED_SPEC):
+    """Oracle verify+commit on the spec workload, restricted to a sample of
+    heads, until `seconds` of CPU work are spent.  Returns (tokens/s scaled to
+    all heads, cores, sample description, steps)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    slots = ki.slot_table(rng, B, P)
+    sess = oracle.OracleSession(P, heads_sampled, D, D)
+    toks = [ki.round_to(ki.gen_tokens(rng, [T] * B, heads_sampled, D), "bf16")
+            for _ in range(8)]
+    accs = [ki.accepted_uniform(rng, B, T) for _ in range(8)]
+    steps, t0 = 0, time.perf_counter()
+    while steps < 1 or time.perf_counter() - t0 < seconds:
+        sess.verify(toks[steps % 8], slots)
+        sess.commit(accs[steps % 8], slots)
+        steps += 1
+    el = time.perf_counter() - t0
+    rate = B * T * steps * heads_sampled / H / el
+    desc = ("%d spec steps (16 seqs x T=8, commit a~U{0..8}) on %d of 32 heads, "
+            "d=128, fp64; scaled to 32 heads" % (steps, heads_sampled))
+    return rate, oracle.num_threads(), desc, steps
+
+
+# ----------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    rng = np.random.default_rng(ki.SEED_SPEC)
+    hs = 1  # each step: one layer x 16 seqs x 1 head (bounded sample)
+    slots = ki.slot_table(rng, B, P)
+    sess = oracle.OracleSession(P, hs, D, D)
+    toks = [ki.round_to(ki.gen_tokens(rng, [T] * B, hs, D), "bf16")
+            for _ in range(8)]
+    accs = [ki.accepted_uniform(rng, B, T) for _ in range(8)]
+
+    def step(s):
+        sess.verify(toks[s % 8], slots)
+        sess.commit(accs[s % 8], slots)
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(s)
+    el = time.perf_counter() - t0
+    value = B * T * args.steps * hs / H / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": ki.SPEC.name, "sample": "1 of 32 heads per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s",
+                         "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "each step: verify T=8 + commit for 16 seqs "
+                                   "on 1 of 32 heads (fp64), scaled to 32 heads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ kda arm
+def build_inputs(torch, rng, NL, dev):
+    """One input set: NL layers of packed tokens in one contiguous arena."""
+    N = B * T
+    per = N * H * D * 4 + N * H          # q, k, v, alpha + beta (bf16 elems)
+    arena = torch.empty(NL * per, dtype=torch.bfloat16, device=dev)
+    views = []
+    for l in range(NL):
+        tok = ki.gen_tokens(rng, [T] * B, H, D)
+        base = l * per
+        vs = {}
+        off = base
+        for n in ("q", "k", "v", "alpha"):
+            vs[n] = arena[off:off + N * H * D].view(N, H, D)
+            vs[n].copy_(torch.from_numpy(tok[n]).to(torch.bfloat16))
+            off += N * H * D
+        vs["beta"] = arena[off:off + N * H].view(N, H)
+        vs["beta"].copy_(torch.from_numpy(tok["beta"]).to(torch.bfloat16))
+        views.append(vs)
+    return arena, views
+
+
+def run_prefill(torch, K, dev):
+    w = ki.PREFILL
+    rng = np.random.default_rng(w.seed)
+    L, C, E = 8192, 64, 1024
+    tok = ki.gen_tokens(rng, [L], H, D)
+    t = {n: torch.from_numpy(tok[n]).to(device=dev, dtype=torch.bfloat16)
+         for n in ("q", "k", "v", "alpha", "beta")}
+    cu = torch.tensor([0, L], dtype=torch.int32, device=dev)
+    tb = K.TokenBatch(t["q"], t["k"], t["v"], t["alpha"], t["beta"], cu)
+    init = ki.initial_states(rng, 1, H, D, D, 0.02)
+    pool = K.StatePool.zeros(1 + L // E, H, D, device=dev)
+    pool.data[0].copy_(torch.from_numpy(np.swapaxes(init[0], -1, -2).copy()))
+    slots = torch.tensor([0], dtype=torch.int32, device=dev)
+    ck = torch.arange(1, 1 + L // E, dtype=torch.int32, device=dev).view(1, -1)
+    ws_bytes = K.kda_prefill_workspace_size(L, 1, H, D, D, C)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        K.kda_prefill_chunked(tb, pool, slots, C, E, ck, workspace=ws)
+    reps = 10
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        e0.record(stream)
+        K.kda_prefill_chunked(tb, pool, slots, C, E, ck, workspace=ws)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    alg_bytes = (L * H * (4 * D * 2 + 2) + L * H * D * 4
+                 + (2 + L // E) * H * D * D * 4)
+    flops = 11.6e6 * (L // C) * H
+    return {
+        "workload": w.name, "tokens_per_s": L / (ms * 1e-3), "ms": ms,
+        "launches_per_call": 3, "reps": reps, "algorithmic_bytes": alg_bytes,
+        "achieved_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+        "chunk_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
+        "workspace_bytes": ws_bytes,
+        "note": "CUDA-core fp32 chunk form (intra-chunk kernel + sequential "
+                "state kernel); tensor-pipe utilisation 0",
+    }
+
+
+def run_kda(args, rank, world, local_rank):
+    import torch
+    from recurrent_kda_state_gb300 import kda as K
+    from recurrent_kda_state_gb300._build import build_library
+    build_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    touched = B * H * D * D * 4
+    NL = max(1, math.ceil(4 * l2 / touched))
+    rng = np.random.default_rng(ki.SEED_SPEC + 7919 * rank)
+    slots_np = ki.slot_table(rng, B, P)
+    slots = torch.as_tensor(slots_np, device=dev)
+    pools = [K.StatePool.zeros(P, H, D, device=dev) for _ in range(NL)]
+    rings = [K.ReplayRing(P, H, D, DEPTH, torch.bfloat16, device=dev)
+             for _ in range(NL)]
+    G = 4
+    sets = [build_inputs(torch, rng, NL, dev) for _ in range(G)]
+    N = B * T
+    cu = torch.arange(0, (B + 1) * T, T, dtype=torch.int32, device=dev)
+    outs = torch.empty(G, NL, N, H, D, dtype=torch.float32, device=dev)
+    batches = [[K.TokenBatch(v["q"], v["k"], v["v"], v["alpha"], v["beta"], cu,
+                             o=outs[g, l]) for l, v in enumerate(sets[g][1])]
+               for g in range(G)]
+    A = 256
+    acc_np = ki.accepted_uniform(rng, A * B, T).reshape(A, B)
+    acc = torch.as_tensor(acc_np, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    total_steps = args.warmup + args.steps
+    graphs, events = [], []
+    K.kda_get_device_error()
+    with torch.cuda.stream(stream):
+        for s in range(total_steps):
+            g = torch.cuda.CUDAGraph()
+            evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True))
+                   for _ in range(NL)] if s >= args.warmup else None
+            g.capture_begin()
+            for l in range(NL):
+                if evs:
+                    evs[l][0].record(stream)
+                K.kda_verify(batches[s % G][l], T, pools[l], slots, rings[l],
+                             stream=stream)
+                if evs:
+                    evs[l][1].record(stream)
+                K.kda_commit(acc[s % A], slots, pools[l], rings[l], stream=stream)
+            g.capture_end()
+            graphs.append(g)
+            events.append(evs)
+    torch.cuda.synchronize()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            graphs[s].replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(args.warmup, total_steps):
+            graphs[s].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier()
+    clocks.stop()
+    ms = e0.elapsed_time(e1)
+    bits = K.kda_get_device_error()
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # per-launch verify durations over the timed region
+    durs, abytes = [], []
+    for s in range(args.warmup, total_steps):
+        a_prev = acc_np[(s - 1) % A]
+        b = float(sum(unit_bytes(int(x)) for x in a_prev) * H)
+        for l in range(NL):
+            ev0, ev1 = events[s][l]
+            durs.append(ev0.elapsed_time(ev1))
+            abytes.append(b)
+    mean_dur_s = float(np.mean(durs)) * 1e-3
+    achieved = float(np.mean(abytes)) / mean_dur_s / 1e9
+    peak, peak_kind = load_peaks()
+    tokens = B * T * args.steps * NL * world
+    value = tokens / (ms * 1e-3)
+
+    # end to end: inputs from pinned host memory, outputs back, same graphs
+    host_in = [sets[g][0].cpu().pin_memory() for g in range(G)]
+    host_acc = acc.cpu().pin_memory()
+    host_out = torch.empty(outs.shape[1:], dtype=torch.float32).pin_memory()
+    h2d = sets[0][0].numel() * 2 + B * 4
+    d2h = host_out.numel() * 4
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for s in range(args.warmup, total_steps):
+            sets[s % G][0].copy_(host_in[s % G], non_blocking=True)
+            acc[s % A].copy_(host_acc[s % A], non_blocking=True)
+            graphs[s].replay()
+            host_out.copy_(outs[s % G], non_blocking=True)
+        f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = f0.elapsed_time(f1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    prefill = run_prefill(torch, K, dev)
+    cpu = None
+    if rank == 0:
+        rate, cores, desc, _ = oracle_spec_rate(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores,
+               "kind": "oracle", "sample": desc}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": ki.SPEC.name, "num_seqs": B, "heads": H, "d": D,
+            "T": T, "ring_depth": DEPTH, "slots": P, "kda_layers": NL,
+            "inputs": "bf16 q/k/v/alpha/beta, fp32 state and outputs",
+            "value_def": "verified draft tokens per second per KDA layer "
+                         "(B*T*layers*steps/time)",
+            "l2": "inputs larger than L2: %d layer state pools touched per "
+                  "step = %.0f MiB vs L2 %.0f MiB" % (
+                      NL, NL * touched / 2 ** 20, l2 / 2 ** 20),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(), "kernel": "verify_kernel<128, bf16>",
+                     "peak_source": peak_kind,
+                     "mean_launch_us": mean_dur_s * 1e6,
+                     "alg_bytes_per_launch": float(np.mean(abytes))},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * NL * args.steps,
+        "clocks": clocks.summary(w0, w1),
+        "device_error_bits": bits,
+        "prefill": prefill,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_kda(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

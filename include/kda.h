@@ -1,0 +1,236 @@
+/*
+ * kda.h -- C ABI of the KDA recurrent-state hot path (libkda.so).
+ *
+ * What it computes.  Kimi Delta Attention keeps a fixed-size recurrent state
+ * per (sequence, head) instead of a growing KV cache ("Confirmed" on the vLLM
+ * Kimi K3 news page).  The pages name KDA but print no equation; this library
+ * fixes it as a gated delta rule with per-key-channel decay:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t                                  (post-update state)
+ *
+ * S is d_k x d_v, alpha_t in R^{d_k} scales key rows, beta_t is a scalar.
+ * No scaling of q and no normalisation of k happen inside the library.
+ *
+ * Three parts ("vLLM lifts Kimi K3 throughput by up to 2.8x"):
+ *   - chunked prefill that exports state checkpoints at cache-block
+ *     boundaries inside the same pass ("KDA checkpoints stay inside the
+ *     prefill");
+ *   - T-token draft verification over the committed state;
+ *   - ReplaySSM commit: the drafted tokens' inputs are kept in a replay ring
+ *     and the accepted state is rebuilt by replay, so a rejection only moves
+ *     a pointer and no state is written per draft position ("ReplaySSM
+ *     shrinks rollback state").
+ * Mixed batches of speculative and ordinary requests use contiguous segments
+ * of one packed token tensor and write outputs in place ("Small tensor copies
+ * leave the hot path").
+ *
+ * Conventions for every entry point.
+ *   - All pointers inside the structs and all int32 index arrays are DEVICE
+ *     pointers unless stated; the caller owns every buffer.  The library
+ *     allocates no device memory and keeps no per-call host state.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  Argument errors are detected on the host
+ *     before anything is enqueued and returned synchronously as a negative
+ *     status; nothing is launched then.
+ *   - Errors that depend on device data (a slot id out of range, an accepted
+ *     length above the pending count, a segment longer than the ring) are
+ *     never trapped: the affected (sequence, head) unit is skipped, its state
+ *     and ring are left untouched, and a KDA_DERR_* bit is ORed into a
+ *     library-wide device error word read by kda_get_device_error().
+ *   - Packed token tensors are [N][H][d] row-major (beta is [N][H]);
+ *     sequence i owns rows [cu_seqlens[i], cu_seqlens[i+1]).
+ *   - A state pool is fp32 [num_slots][H][d_v][d_k]: the state S of one
+ *     (slot, head) is stored transposed, so each column of S (one value
+ *     channel, all key channels) is contiguous.
+ *   - Supported head dims: d_k == d_v in {16, 32, 64, 128}.  Input dtypes:
+ *     fp32 or bf16 (q, k, v, alpha and beta all the same dtype); state and
+ *     outputs are fp32.  Every pointer must be 16-byte aligned.
+ *   - Calls that touch disjoint buffers may run concurrently on different
+ *     streams; the device error word is shared.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *kda_stream_t;
+
+/* Status codes (return values). */
+enum {
+  KDA_OK = 0,
+  KDA_EINVAL = -1,  /* bad scalar argument or NULL pointer                */
+  KDA_EDTYPE = -2,  /* unsupported or mismatched dtype                     */
+  KDA_ESHAPE = -3,  /* unsupported or mismatched dimension                 */
+  KDA_EALIGN = -4,  /* a pointer is not 16-byte aligned                    */
+  KDA_EPROTO = -5,  /* ring / commit protocol misuse detectable on host    */
+  KDA_ECUDA = -6,   /* a CUDA runtime call failed (launch, copy, sync)     */
+  KDA_EDEVICE = -7, /* kda_get_device_error found bits set                 */
+  KDA_ENOSPC = -8   /* workspace smaller than kda_prefill_workspace_size() */
+};
+
+/* Bits of the device error word. */
+enum {
+  KDA_DERR_SLOT = 1,     /* a state / checkpoint slot id outside the pool  */
+  KDA_DERR_ACCEPT = 2,   /* accepted_len < 0 or above the pending count     */
+  KDA_DERR_DEPTH = 4,    /* a speculative segment longer than ring depth    */
+  KDA_DERR_SEGMENT = 8,  /* cu_seqlens not non-decreasing / beyond N        */
+  KDA_DERR_RING = 16,    /* ring control word corrupt (pending > depth)     */
+  KDA_DERR_RANGE = 32    /* prefill: cumulative log-decay across half a
+                            chunk below -80 in some channel (fp32 factor
+                            range); outputs of that chunk are unreliable   */
+};
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* One packed batch of tokens and its output buffer. */
+typedef struct {
+  kda_dtype dtype;          /* dtype of q, k, v, alpha, beta                */
+  const void *q;            /* [N][H][d_k]                                  */
+  const void *k;            /* [N][H][d_k]                                  */
+  const void *v;            /* [N][H][d_v]                                  */
+  const void *alpha;        /* [N][H][d_k]  per-channel decay in (0, 1]     */
+  const void *beta;         /* [N][H]                                       */
+  float *o;                 /* [N][H][d_v]  fp32 outputs, written in place  */
+  const int32_t *cu_seqlens; /* [B + 1] device, cu[0] = 0, cu[B] = N        */
+  int32_t num_seqs;         /* B                                            */
+  int32_t num_tokens;       /* N (host copy of cu_seqlens[B])               */
+  int32_t num_heads;        /* H                                            */
+  int32_t d_k, d_v;
+} kda_tokens;
+
+/* Paged per-sequence states: fp32 [num_slots][H][d_v][d_k]. */
+typedef struct {
+  float *base;
+  int32_t num_slots, num_heads, d_k, d_v;
+} kda_state_pool;
+
+/* ReplaySSM ring, one per state pool (per layer).  For every (slot, head)
+ * it holds the inputs of the last verify's drafted tokens, entry e = the
+ * e-th drafted position, plus a control pair {pending, accepted}:
+ *   k, alpha : [num_slots][H][depth][d_k]   (token dtype)
+ *   v        : [num_slots][H][depth][d_v]   (token dtype)
+ *   beta     : [num_slots][H][depth]        (token dtype)
+ *   ctrl     : [num_slots][H][2] int32      {pending, accepted}
+ * A slot's ctrl must be zero (kda_ring_reset) before its first verify. */
+typedef struct {
+  void *k, *v, *alpha, *beta;
+  int32_t *ctrl;
+  int32_t depth;
+  kda_dtype dtype;
+} kda_replay_ring;
+
+/*
+ * kda_prefill_chunked -- chunked prefill with in-pass checkpoints.
+ * ("KDA checkpoints stay inside the prefill", vLLM Kimi K3 optimisation page.)
+ *
+ * For each sequence i the state starts at pool[state_slots[i]], runs every
+ * token of segment i through the recurrence (chunk-wise WY/UT form, chunks
+ * of `chunk` tokens aligned to absolute positions), writes o for every
+ * token, and writes the final state back to pool[state_slots[i]].
+ * Checkpoints: let p0 = start_pos[i] (tokens already folded into the state;
+ * start_pos may be NULL = all zero).  After the token at absolute position
+ * P = (floor(p0 / ckpt_every) + m + 1) * ckpt_every (1-based count of tokens
+ * in the sequence) the state is copied into pool[ckpt_slots[i * max_ckpt + m]]
+ * for m < max_ckpt; entries < 0 are skipped; boundaries past max_ckpt are
+ * dropped.  ckpt_every == 0 disables checkpoints (ckpt_slots may be NULL).
+ * Requirements: chunk in {16, 32, 64}; ckpt_every % chunk == 0; workspace of
+ * at least kda_prefill_workspace_size(...) bytes, 256-byte aligned, owned by
+ * the caller and not used by another call until this one completes.
+ * The target slots must have no pending commit (see kda_materialize).
+ */
+int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
+                        const int32_t *state_slots, const int32_t *ckpt_slots,
+                        int32_t max_ckpt, int32_t ckpt_every, int32_t chunk,
+                        const int32_t *start_pos, void *workspace,
+                        size_t workspace_bytes, kda_stream_t stream);
+
+/* Bytes of workspace kda_prefill_chunked needs for these sizes (0 on bad
+ * arguments). */
+size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
+                                  int32_t num_heads, int32_t d_k, int32_t d_v,
+                                  int32_t chunk);
+
+/*
+ * kda_verify -- one verify launch over a mixed packed batch.
+ * ("ReplaySSM shrinks rollback state"; "Small tensor copies leave the hot
+ * path".)
+ *
+ * For every sequence i and head h, with slot s = state_slots[i]:
+ *   1. the pending commit of (s, h) is applied first: the `accepted` leading
+ *      ring entries recorded by the last kda_commit are replayed onto the
+ *      state, token by token, and the state is written back once;
+ *   2. speculative rows (is_spec[i] != 0, or is_spec == NULL): the segment's
+ *      T_i <= max_T <= depth drafted tokens are evaluated from the committed
+ *      state, o receives their outputs, their inputs are copied into ring
+ *      entries 0..T_i-1, and ctrl becomes {T_i, 0}; no draft state is stored;
+ *   3. ordinary rows (is_spec[i] == 0): the segment's tokens are applied and
+ *      committed at once (ordinary decode), o receives their outputs, and
+ *      ctrl becomes {0, 0}.
+ * A verify that follows another verify with no kda_commit between them
+ * treats the earlier drafts as all rejected.
+ */
+int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
+               const int32_t *state_slots, kda_replay_ring *ring,
+               const int32_t *is_spec, kda_stream_t stream);
+
+/*
+ * kda_commit -- record how many drafted tokens each sequence accepted.
+ * ("Rejecting a draft only moves the buffer pointer.")
+ *
+ * accepted_len[i] (device, 0 <= a <= pending) is recorded in ctrl of every
+ * head of slot state_slots[i]; the replay itself is folded into the next
+ * kda_verify or kda_materialize of that slot, so the state is read and
+ * written once per step.  a == 0 leaves the state untouched.  No host sync.
+ */
+int kda_commit(const int32_t *accepted_len, const int32_t *state_slots,
+               int32_t num_seqs, kda_state_pool *pool, kda_replay_ring *ring,
+               kda_stream_t stream);
+
+/*
+ * kda_materialize -- apply every recorded commit now: replay the accepted
+ * ring entries of each listed slot onto its state, write the state, and
+ * clear ctrl to {0, 0}.  Call before reading a state any other way (gather,
+ * copy, prefill from it) after a commit.
+ */
+int kda_materialize(const int32_t *state_slots, int32_t num_seqs,
+                    kda_state_pool *pool, kda_replay_ring *ring,
+                    kda_stream_t stream);
+
+/* kda_ring_reset -- set ctrl of every head of the listed slots to {0, 0}
+ * (a fresh slot, or drafts to discard). */
+int kda_ring_reset(const int32_t *slots, int32_t n, const kda_state_pool *pool,
+                   kda_replay_ring *ring, kda_stream_t stream);
+
+/* kda_gather_states -- out[i] = pool[slots[i]] for i < n; out is fp32
+ * [n][H][d_v][d_k] on the device.  Reads committed-and-materialized state. */
+int kda_gather_states(const kda_state_pool *pool, const int32_t *slots,
+                      int32_t n, float *out, kda_stream_t stream);
+
+/* kda_copy_slots -- pool[dst[i]] = pool[src[i]] for i < n (prefix-cache
+ * fork of a checkpoint into a live slot).  The src and dst sets must be
+ * disjoint. */
+int kda_copy_slots(kda_state_pool *pool, const int32_t *src,
+                   const int32_t *dst, int32_t n, kda_stream_t stream);
+
+/* kda_get_device_error -- synchronize `stream`, read the device error word
+ * of the current device into *host_bits (host pointer), clear it, and return
+ * KDA_EDEVICE if any bit was set, else KDA_OK. */
+int kda_get_device_error(int32_t *host_bits, kda_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *kda_status_string(int status);
+
+/* Library ABI version: 1. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H */

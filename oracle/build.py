@@ -1,15 +1,16 @@
 """Compile the fp64 CPU oracle (test infrastructure only).
 
-Builds ``oracle/_build/libkda_oracle.so`` from ``kda_oracle.c`` with gcc:
+Builds ``oracle/_build/<machine>/libkda_oracle.so`` from ``kda_oracle.c`` with gcc:
 no fast-math, floating-point contraction off (identical bits on x86 and
 Arm), OpenMP when the compiler supports it.
 """
 import os
+import platform
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "kda_oracle.c")
-OUT_DIR = os.path.join(HERE, "_build")
+OUT_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB = os.path.join(OUT_DIR, "libkda_oracle.so")
 
 

@@ -1,0 +1,312 @@
+// Public C ABI of libkda.so: argument validation on the host, then launches on
+// the caller's stream.  Nothing is allocated here; every buffer belongs to the
+// caller.  The only library-owned device object is one error word per device.
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+// Library-wide device error word (one per device that loads the library).
+__device__ unsigned int g_kda_device_error = 0;
+
+namespace {
+
+// Device address of g_kda_device_error for the current device.
+unsigned int *device_error_word() {
+  static std::mutex mu;
+  static unsigned int *cache[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned int *>(p);
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ECUDA; }
+
+constexpr int kMaxGridY = 65535;
+constexpr size_t kMaxSmem = 227 * 1024;
+
+int check_pool(const kda_state_pool *pool) {
+  if (!pool || !pool->base) return KDA_EINVAL;
+  if (!aligned16(pool->base)) return KDA_EALIGN;
+  if (pool->num_slots < 1 || pool->num_heads < 1) return KDA_ESHAPE;
+  if (pool->d_k != pool->d_v || !dim_ok(pool->d_k)) return KDA_ESHAPE;
+  return KDA_OK;
+}
+
+int check_tokens(const kda_tokens *t, const kda_state_pool *pool) {
+  if (!t) return KDA_EINVAL;
+  if (t->dtype != KDA_F32 && t->dtype != KDA_BF16) return KDA_EDTYPE;
+  if (t->num_seqs < 0 || t->num_tokens < 0) return KDA_EINVAL;
+  if (t->num_heads != pool->num_heads || t->d_k != pool->d_k || t->d_v != pool->d_v)
+    return KDA_ESHAPE;
+  if (t->num_seqs > kMaxGridY) return KDA_ESHAPE;
+  if (t->num_seqs == 0) return KDA_OK;
+  if (!t->cu_seqlens) return KDA_EINVAL;
+  if (t->num_tokens > 0) {
+    const void *ptrs[] = {t->q, t->k, t->v, t->alpha, t->beta, t->o};
+    for (const void *p : ptrs) {
+      if (!p) return KDA_EINVAL;
+      if (!aligned16(p)) return KDA_EALIGN;
+    }
+  }
+  if (!aligned16(t->cu_seqlens)) return KDA_EALIGN;
+  return KDA_OK;
+}
+
+int check_ring(const kda_replay_ring *r, kda_dtype dt, bool payload) {
+  if (!r || !r->ctrl) return KDA_EINVAL;
+  if (!aligned16(r->ctrl)) return KDA_EALIGN;
+  if (r->depth < 1 || r->depth > 64) return KDA_EINVAL;
+  if (!payload) return KDA_OK;
+  if (r->dtype != dt) return KDA_EDTYPE;
+  const void *ptrs[] = {r->k, r->v, r->alpha, r->beta};
+  for (const void *p : ptrs) {
+    if (!p) return KDA_EINVAL;
+    if (!aligned16(p)) return KDA_EALIGN;
+  }
+  return KDA_OK;
+}
+
+kda::VerifyParams verify_params(const kda_state_pool *pool,
+                                const kda_replay_ring *ring,
+                                const int32_t *slots, int B, unsigned *err) {
+  kda::VerifyParams p = {};
+  p.state_slots = slots;
+  p.pool = pool->base;
+  p.rk = ring->k;
+  p.rv = ring->v;
+  p.ra = ring->alpha;
+  p.rb = ring->beta;
+  p.ctrl = ring->ctrl;
+  p.err = err;
+  p.B = B;
+  p.H = pool->num_heads;
+  p.P = pool->num_slots;
+  p.depth = ring->depth;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 1; }
+
+const char *kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_EINVAL: return "KDA_EINVAL: bad scalar argument or NULL pointer";
+    case KDA_EDTYPE: return "KDA_EDTYPE: unsupported or mismatched dtype";
+    case KDA_ESHAPE: return "KDA_ESHAPE: unsupported or mismatched dimension";
+    case KDA_EALIGN: return "KDA_EALIGN: pointer not 16-byte aligned";
+    case KDA_EPROTO: return "KDA_EPROTO: ring/commit protocol misuse";
+    case KDA_ECUDA: return "KDA_ECUDA: CUDA runtime error";
+    case KDA_EDEVICE: return "KDA_EDEVICE: device error bits set";
+    case KDA_ENOSPC: return "KDA_ENOSPC: workspace too small";
+    default: return "KDA_UNKNOWN";
+  }
+}
+
+size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
+                                  int32_t num_heads, int32_t d_k, int32_t d_v,
+                                  int32_t chunk) {
+  if (num_tokens < 0 || num_seqs < 0 || num_heads < 1 || d_k != d_v ||
+      !dim_ok(d_k) || (chunk != 16 && chunk != 32 && chunk != 64))
+    return 0;
+  return kda::prefill_workspace_bytes(num_tokens, num_seqs, num_heads, d_k, chunk);
+}
+
+int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
+                        const int32_t *state_slots, const int32_t *ckpt_slots,
+                        int32_t max_ckpt, int32_t ckpt_every, int32_t chunk,
+                        const int32_t *start_pos, void *workspace,
+                        size_t workspace_bytes, kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if ((st = check_tokens(tok, pool))) return st;
+  if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_EINVAL;
+  if (ckpt_every < 0 || max_ckpt < 0) return KDA_EINVAL;
+  if (ckpt_every > 0 && ckpt_every % chunk != 0) return KDA_EINVAL;
+  if (ckpt_every > 0 && max_ckpt > 0 && !ckpt_slots) return KDA_EINVAL;
+  if (tok->num_seqs == 0) return KDA_OK;
+  if (!state_slots || !workspace) return KDA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return KDA_EALIGN;
+  const size_t need = kda::prefill_workspace_bytes(
+      tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, chunk);
+  if (workspace_bytes < need) return KDA_ENOSPC;
+  if ((long long)tok->num_tokens / chunk + 2LL * tok->num_seqs > 0x7fffffffLL)
+    return KDA_ESHAPE;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::PrefillParams p = {};
+  p.q = tok->q;
+  p.k = tok->k;
+  p.v = tok->v;
+  p.alpha = tok->alpha;
+  p.beta = tok->beta;
+  p.o = tok->o;
+  p.cu_seqlens = tok->cu_seqlens;
+  p.state_slots = state_slots;
+  p.ckpt_slots = ckpt_every > 0 && max_ckpt > 0 ? ckpt_slots : nullptr;
+  p.start_pos = start_pos;
+  p.pool = pool->base;
+  p.ws = static_cast<unsigned char *>(workspace);
+  p.err = err;
+  p.B = tok->num_seqs;
+  p.N = tok->num_tokens;
+  p.H = tok->num_heads;
+  p.P = pool->num_slots;
+  p.max_ckpt = max_ckpt;
+  p.ckpt_every = ckpt_every;
+  p.max_chunks = kda::prefill_max_chunks(tok->num_tokens, tok->num_seqs, chunk);
+  return cuda_status(kda::launch_prefill(p, tok->dtype, tok->d_k, chunk,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
+               const int32_t *state_slots, kda_replay_ring *ring,
+               const int32_t *is_spec, kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if ((st = check_tokens(tok, pool))) return st;
+  if ((st = check_ring(ring, tok->dtype, true))) return st;
+  if (max_T < 0) return KDA_EINVAL;
+  if (!is_spec && max_T > ring->depth) return KDA_EPROTO;
+  const size_t smem = (size_t)(ring->depth + max_T) * (4 * tok->d_k + 4) * sizeof(float);
+  if (smem > kMaxSmem) return KDA_EINVAL;
+  if (tok->num_seqs == 0) return KDA_OK;
+  if (!state_slots) return KDA_EINVAL;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::VerifyParams p = verify_params(pool, ring, state_slots, tok->num_seqs, err);
+  p.q = tok->q;
+  p.k = tok->k;
+  p.v = tok->v;
+  p.alpha = tok->alpha;
+  p.beta = tok->beta;
+  p.o = tok->o;
+  p.cu_seqlens = tok->cu_seqlens;
+  p.is_spec = is_spec;
+  p.N = tok->num_tokens;
+  p.max_T = max_T;
+  p.mode = 0;
+  return cuda_status(kda::launch_verify(p, tok->dtype, tok->d_k,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_commit(const int32_t *accepted_len, const int32_t *state_slots,
+               int32_t num_seqs, kda_state_pool *pool, kda_replay_ring *ring,
+               kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if ((st = check_ring(ring, KDA_F32, false))) return st;
+  if (num_seqs < 0) return KDA_EINVAL;
+  if (num_seqs == 0) return KDA_OK;
+  if (!accepted_len || !state_slots) return KDA_EINVAL;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::CommitParams p = {accepted_len, state_slots, ring->ctrl, err, num_seqs,
+                         pool->num_heads, pool->num_slots};
+  return cuda_status(kda::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_materialize(const int32_t *state_slots, int32_t num_seqs,
+                    kda_state_pool *pool, kda_replay_ring *ring,
+                    kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if (!ring) return KDA_EINVAL;
+  if ((st = check_ring(ring, ring->dtype, true))) return st;
+  if (ring->dtype != KDA_F32 && ring->dtype != KDA_BF16) return KDA_EDTYPE;
+  if (num_seqs < 0 || num_seqs > kMaxGridY) return KDA_EINVAL;
+  if (num_seqs == 0) return KDA_OK;
+  if (!state_slots) return KDA_EINVAL;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::VerifyParams p = verify_params(pool, ring, state_slots, num_seqs, err);
+  p.max_T = 0;
+  p.mode = 1;
+  return cuda_status(kda::launch_verify(p, ring->dtype, pool->d_k,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_ring_reset(const int32_t *slots, int32_t n, const kda_state_pool *pool,
+                   kda_replay_ring *ring, kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if ((st = check_ring(ring, KDA_F32, false))) return st;
+  if (n < 0) return KDA_EINVAL;
+  if (n == 0) return KDA_OK;
+  if (!slots) return KDA_EINVAL;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::CommitParams p = {nullptr, slots, ring->ctrl, err, n, pool->num_heads,
+                         pool->num_slots};
+  return cuda_status(kda::launch_ring_reset(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_gather_states(const kda_state_pool *pool, const int32_t *slots,
+                      int32_t n, float *out, kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if (n < 0 || n > kMaxGridY) return KDA_EINVAL;
+  if (n == 0) return KDA_OK;
+  if (!slots || !out) return KDA_EINVAL;
+  if (!aligned16(out)) return KDA_EALIGN;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::SlotCopyParams p = {};
+  p.src_base = pool->base;
+  p.dst_base = out;
+  p.src_slots = slots;
+  p.dst_slots = nullptr;
+  p.err = err;
+  p.n = n;
+  p.P = pool->num_slots;
+  p.state_floats = (long long)pool->num_heads * pool->d_v * pool->d_k;
+  return cuda_status(kda::launch_slot_copy(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_copy_slots(kda_state_pool *pool, const int32_t *src, const int32_t *dst,
+                   int32_t n, kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if (n < 0 || n > kMaxGridY) return KDA_EINVAL;
+  if (n == 0) return KDA_OK;
+  if (!src || !dst) return KDA_EINVAL;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::SlotCopyParams p = {};
+  p.src_base = pool->base;
+  p.dst_base = pool->base;
+  p.src_slots = src;
+  p.dst_slots = dst;
+  p.err = err;
+  p.n = n;
+  p.P = pool->num_slots;
+  p.state_floats = (long long)pool->num_heads * pool->d_v * pool->d_k;
+  return cuda_status(kda::launch_slot_copy(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_get_device_error(int32_t *host_bits, kda_stream_t stream) {
+  if (!host_bits) return KDA_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ECUDA;
+  unsigned int bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, g_kda_device_error, sizeof(bits)) != cudaSuccess)
+    return KDA_ECUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(zero)) != cudaSuccess)
+    return KDA_ECUDA;
+  *host_bits = (int32_t)bits;
+  return bits ? KDA_EDEVICE : KDA_OK;
+}
+
+}  // extern "C"

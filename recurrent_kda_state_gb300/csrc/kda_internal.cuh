@@ -1,0 +1,148 @@
+// Internal declarations shared by the CUDA translation units of libkda.so.
+// Launch parameter blocks, device-side dtype helpers and the launchers that
+// kda_api.cu calls after validating the public arguments.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// ----------------------------------------------------------------- dtypes
+template <typename Tin>
+struct InVec;  // 16-byte vector of inputs, converted to fp32
+
+template <>
+struct InVec<float> {
+  static constexpr int kElems = 4;
+  __device__ __forceinline__ static void load(const float *p, float *dst) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
+  }
+  __device__ __forceinline__ static void store(float *p, const float *src) {
+    *reinterpret_cast<float4 *>(p) = make_float4(src[0], src[1], src[2], src[3]);
+  }
+};
+
+template <>
+struct InVec<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *dst) {
+    const uint4 a = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dst[2 * i] = __uint_as_float(w[i] << 16);
+      dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  // Exact for values that came from bf16 (the ring stores copies of inputs).
+  __device__ __forceinline__ static void store(__nv_bfloat16 *p, const float *src) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = (__float_as_uint(src[2 * i]) >> 16) |
+             (__float_as_uint(src[2 * i + 1]) & 0xffff0000u);
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <typename Tin>
+__device__ __forceinline__ float in_scalar(const Tin *p);
+template <>
+__device__ __forceinline__ float in_scalar<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float in_scalar<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  return __bfloat162float(*p);
+}
+template <typename Tin>
+__device__ __forceinline__ void out_scalar(Tin *p, float x);
+template <>
+__device__ __forceinline__ void out_scalar<float>(float *p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void out_scalar<__nv_bfloat16>(__nv_bfloat16 *p, float x) {
+  *reinterpret_cast<uint16_t *>(p) = (uint16_t)(__float_as_uint(x) >> 16);
+}
+
+__device__ __forceinline__ void set_error(unsigned int *err, unsigned int bit) {
+  atomicOr(err, bit);
+}
+
+// ------------------------------------------------------- launch parameters
+struct VerifyParams {
+  const void *q, *k, *v, *alpha, *beta;  // packed inputs (NULL when mode==1)
+  float *o;
+  const int32_t *cu_seqlens;
+  const int32_t *state_slots;
+  const int32_t *is_spec;  // may be NULL (all speculative)
+  float *pool;
+  void *rk, *rv, *ra, *rb;  // ring payload
+  int32_t *ctrl;            // ring control [P][H][2]
+  unsigned int *err;
+  int B, N, H, P, depth, max_T;
+  int mode;  // 0 = verify, 1 = materialize (no tokens)
+};
+
+struct CommitParams {
+  const int32_t *accepted_len;  // NULL for ring reset
+  const int32_t *slots;
+  int32_t *ctrl;
+  unsigned int *err;
+  int B, H, P;
+};
+
+struct SlotCopyParams {
+  const float *src_base;
+  float *dst_base;
+  const int32_t *src_slots;  // indices into src_base's pool
+  const int32_t *dst_slots;  // NULL: dst is dense [n][state]
+  unsigned int *err;
+  int n, P;
+  long long state_floats;  // H * d_v * d_k
+};
+
+struct PrefillParams {
+  const void *q, *k, *v, *alpha, *beta;
+  float *o;
+  const int32_t *cu_seqlens;
+  const int32_t *state_slots;
+  const int32_t *ckpt_slots;  // [B][max_ckpt] or NULL
+  const int32_t *start_pos;   // [B] or NULL
+  float *pool;
+  unsigned char *ws;          // workspace (chunk table + per-chunk operands)
+  unsigned int *err;
+  int B, N, H, P, max_ckpt, ckpt_every, max_chunks;
+};
+
+// Workspace geometry of the chunked prefill (shared with the size query):
+// [chunk table: (B + 1) int32, padded to 256 B][entries: (chunk, head) ->
+// prefill_entry_floats(D, C) fp32 each, 256-byte aligned].
+__host__ __device__ inline size_t prefill_table_bytes(int B) {
+  return ((size_t)(B + 1) * sizeof(int) + 255) & ~(size_t)255;
+}
+__host__ __device__ inline size_t prefill_entry_floats(int D, int C) {
+  const size_t f = (size_t)4 * C * D + (size_t)C * C + D;
+  return (f + 63) & ~(size_t)63;
+}
+__host__ __device__ inline int prefill_max_chunks(int N, int B, int C) {
+  return N / C + 2 * B;
+}
+__host__ __device__ inline size_t prefill_workspace_bytes(int N, int B, int H,
+                                                          int D, int C) {
+  return prefill_table_bytes(B) + (size_t)prefill_max_chunks(N, B, C) * H *
+                                      prefill_entry_floats(D, C) * sizeof(float);
+}
+
+// Launchers: return cudaError_t of the launch.
+cudaError_t launch_verify(const VerifyParams &p, kda_dtype dt, int D,
+                          cudaStream_t s);
+cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
+cudaError_t launch_ring_reset(const CommitParams &p, cudaStream_t s);
+cudaError_t launch_slot_copy(const SlotCopyParams &p, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,
+                           cudaStream_t s);
+
+}  // namespace kda
