@@ -4,8 +4,9 @@
 Main line: speculative-decode verify + ReplaySSM commit, 16 sequences x 32
 heads x d=128, bf16 inputs, fp32 state in 64 shuffled slots, T = 8 drafts,
 accepted_len ~ U{0..8}, ring depth 8.  One step = one decode step of the
-model's KDA layers: for each of NL layers, kda_verify (which also applies the
-previous step's commit) then kda_commit.  NL layers have their own state
+model's KDA layers: kda_verify on each of NL layers (each also applies that
+layer's pending commit from the previous step), then one kda_commit_layers
+recording the step's accepted lengths in every layer's ring.  NL layers have their own state
 pools, so the state touched per step is NL x 32 MiB, at least 4x the L2.  The
 value is drafted tokens verified through one KDA layer per second,
 B * T * NL * steps / time.  Each step is one CUDA graph captured from the
@@ -342,7 +343,8 @@ def run_kda(args, rank, world, local_rank):
                              stream=stream)
                 if evs:
                     evs[l][1].record(stream)
-                K.kda_commit(acc[s % A], slots, pools[l], rings[l], stream=stream)
+            # the sampler's accepted lengths, recorded in every layer's ring
+            K.kda_commit_layers(acc[s % A], slots, pools[0], rings, stream=stream)
             g.capture_end()
             graphs.append(g)
             events.append(evs)
@@ -457,7 +459,7 @@ def run_kda(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * NL * args.steps,
+        "gpu_launches": (NL + 1) * args.steps,
         "clocks": clocks.summary(w0, w1),
         "device_error_bits": bits,
         "prefill": prefill,

@@ -118,7 +118,8 @@ typedef struct {
  *   v        : [num_slots][H][depth][d_v]   (token dtype)
  *   beta     : [num_slots][H][depth]        (token dtype)
  *   ctrl     : [num_slots][H][2] int32      {pending, accepted}
- * A slot's ctrl must be zero (kda_ring_reset) before its first verify. */
+ * A slot's ctrl must be zero (kda_ring_reset) before its first verify.
+ * depth must be in [1, 16]. */
 typedef struct {
   void *k, *v, *alpha, *beta;
   int32_t *ctrl;
@@ -192,6 +193,18 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
 int kda_commit(const int32_t *accepted_len, const int32_t *state_slots,
                int32_t num_seqs, kda_state_pool *pool, kda_replay_ring *ring,
                kda_stream_t stream);
+
+/*
+ * kda_commit_layers -- kda_commit for the rings of several layers in one
+ * launch: a speculative step verifies every KDA layer, samples once, and
+ * records the same accepted_len[i] in each layer's ring.  rings is a HOST
+ * array of num_layers <= 64 ring descriptors whose pools all have the
+ * geometry of `pool` (the pool's base pointer is not used).
+ */
+int kda_commit_layers(const int32_t *accepted_len, const int32_t *state_slots,
+                      int32_t num_seqs, const kda_state_pool *pool,
+                      const kda_replay_ring *rings, int32_t num_layers,
+                      kda_stream_t stream);
 
 /*
  * kda_materialize -- apply every recorded commit now: replay the accepted

@@ -7,6 +7,7 @@ from .kda import (  # noqa: F401
     StatePool,
     TokenBatch,
     kda_commit,
+    kda_commit_layers,
     kda_copy_slots,
     kda_gather_states,
     kda_get_device_error,

@@ -63,7 +63,7 @@ int check_tokens(const kda_tokens *t, const kda_state_pool *pool) {
 int check_ring(const kda_replay_ring *r, kda_dtype dt, bool payload) {
   if (!r || !r->ctrl) return KDA_EINVAL;
   if (!aligned16(r->ctrl)) return KDA_EALIGN;
-  if (r->depth < 1 || r->depth > 64) return KDA_EINVAL;
+  if (r->depth < 1 || r->depth > kda::verify_max_spec_tokens()) return KDA_EINVAL;
   if (!payload) return KDA_OK;
   if (r->dtype != dt) return KDA_EDTYPE;
   const void *ptrs[] = {r->k, r->v, r->alpha, r->beta};
@@ -179,8 +179,7 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
   if ((st = check_ring(ring, tok->dtype, true))) return st;
   if (max_T < 0) return KDA_EINVAL;
   if (!is_spec && max_T > ring->depth) return KDA_EPROTO;
-  const size_t smem = (size_t)(ring->depth + max_T) * (4 * tok->d_k + 4) * sizeof(float);
-  if (smem > kMaxSmem) return KDA_EINVAL;
+  if (kda::verify_smem_bytes(tok->d_k, ring->depth, max_T) > kMaxSmem) return KDA_EINVAL;
   if (tok->num_seqs == 0) return KDA_OK;
   if (!state_slots) return KDA_EINVAL;
   unsigned *err = device_error_word();
@@ -215,6 +214,34 @@ int kda_commit(const int32_t *accepted_len, const int32_t *state_slots,
   kda::CommitParams p = {accepted_len, state_slots, ring->ctrl, err, num_seqs,
                          pool->num_heads, pool->num_slots};
   return cuda_status(kda::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_commit_layers(const int32_t *accepted_len, const int32_t *state_slots,
+                      int32_t num_seqs, const kda_state_pool *pool,
+                      const kda_replay_ring *rings, int32_t num_layers,
+                      kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if (num_seqs < 0 || num_layers < 0 || num_layers > kda::kMaxCommitLayers)
+    return KDA_EINVAL;
+  if (num_seqs == 0 || num_layers == 0) return KDA_OK;
+  if (!accepted_len || !state_slots || !rings) return KDA_EINVAL;
+  kda::CommitLayersParams p = {};
+  for (int l = 0; l < num_layers; ++l) {
+    if ((st = check_ring(&rings[l], KDA_F32, false))) return st;
+    p.ctrl[l] = rings[l].ctrl;
+  }
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  p.accepted_len = accepted_len;
+  p.slots = state_slots;
+  p.err = err;
+  p.B = num_seqs;
+  p.H = pool->num_heads;
+  p.P = pool->num_slots;
+  p.L = num_layers;
+  return cuda_status(
+      kda::launch_commit_layers(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int kda_materialize(const int32_t *state_slots, int32_t num_seqs,

@@ -83,7 +83,8 @@ struct VerifyParams {
   int32_t *ctrl;            // ring control [P][H][2]
   unsigned int *err;
   int B, N, H, P, depth, max_T;
-  int mode;  // 0 = verify, 1 = materialize (no tokens)
+  int mode;             // 0 = verify, 1 = materialize (no tokens)
+  int prefetch_stride;  // CTAs of the first wave (0: no L2 prefetch)
 };
 
 struct CommitParams {
@@ -92,6 +93,15 @@ struct CommitParams {
   int32_t *ctrl;
   unsigned int *err;
   int B, H, P;
+};
+
+constexpr int kMaxCommitLayers = 64;
+struct CommitLayersParams {
+  const int32_t *accepted_len;
+  const int32_t *slots;
+  int32_t *ctrl[kMaxCommitLayers];
+  unsigned int *err;
+  int B, H, P, L;
 };
 
 struct SlotCopyParams {
@@ -136,10 +146,16 @@ __host__ __device__ inline size_t prefill_workspace_bytes(int N, int B, int H,
                                       prefill_entry_floats(D, C) * sizeof(float);
 }
 
+// Verify launch geometry: dynamic shared memory for (D, ring depth, max_T),
+// and the longest speculative segment the kernel supports (ring depth limit).
+size_t verify_smem_bytes(int D, int depth, int max_T);
+int verify_max_spec_tokens();
+
 // Launchers: return cudaError_t of the launch.
 cudaError_t launch_verify(const VerifyParams &p, kda_dtype dt, int D,
                           cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
+cudaError_t launch_commit_layers(const CommitLayersParams &p, cudaStream_t s);
 cudaError_t launch_ring_reset(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_slot_copy(const SlotCopyParams &p, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,

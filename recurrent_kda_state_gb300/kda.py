@@ -41,7 +41,7 @@ class kda_replay_ring(ctypes.Structure):
 
 
 EXPORTS = ("kda_prefill_chunked", "kda_prefill_workspace_size", "kda_verify",
-           "kda_commit", "kda_materialize", "kda_ring_reset",
+           "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
            "kda_gather_states", "kda_copy_slots", "kda_get_device_error",
            "kda_status_string", "kda_version")
 
@@ -64,6 +64,7 @@ def lib():
         L.kda_prefill_workspace_size.restype = ctypes.c_size_t
         L.kda_verify.argtypes = [tp, _I32, pp, _P, rp, _P, _P]
         L.kda_commit.argtypes = [_P, _P, _I32, pp, rp, _P]
+        L.kda_commit_layers.argtypes = [_P, _P, _I32, pp, rp, _I32, _P]
         L.kda_materialize.argtypes = [_P, _I32, pp, rp, _P]
         L.kda_ring_reset.argtypes = [_P, _I32, pp, rp, _P]
         L.kda_gather_states.argtypes = [pp, _P, _I32, _P, _P]
@@ -192,6 +193,15 @@ def kda_commit(accepted_len, state_slots, pool, ring, stream=None):
     _check(lib().kda_commit(_ptr(accepted_len), _ptr(state_slots),
                             state_slots.numel(), ctypes.byref(pool.c),
                             ctypes.byref(ring.c), _stream(stream)), "kda_commit")
+
+
+def kda_commit_layers(accepted_len, state_slots, pool, rings, stream=None):
+    """kda_commit on several layers' rings (same pool geometry), one launch."""
+    arr = (kda_replay_ring * len(rings))(*[r.c for r in rings])
+    _check(lib().kda_commit_layers(_ptr(accepted_len), _ptr(state_slots),
+                                   state_slots.numel(), ctypes.byref(pool.c),
+                                   arr, len(rings), _stream(stream)),
+           "kda_commit_layers")
 
 
 def kda_materialize(state_slots, pool, ring, stream=None):

@@ -119,4 +119,8 @@ def test_commit_and_slot_validation(L):
                                None) == kda.KDA_EALIGN
     assert L.kda_copy_slots(by(pool), None, s, 1, None) == kda.KDA_EINVAL
     assert L.kda_ring_reset(s, 1, by(pool), None, None) == kda.KDA_EINVAL
+    rings = (kda.kda_replay_ring * 2)(_ring(), _ring())
+    assert L.kda_commit_layers(s, s, 1, by(pool), rings, 65, None) == kda.KDA_EINVAL
+    assert L.kda_commit_layers(s, s, 1, by(pool), None, 2, None) == kda.KDA_EINVAL
+    assert L.kda_commit_layers(s, s, 0, by(pool), rings, 2, None) == kda.KDA_OK
     assert L.kda_get_device_error(None, None) == kda.KDA_EINVAL

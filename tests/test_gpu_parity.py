@@ -164,6 +164,37 @@ def test_verify1_commit1_equals_decode_state():
     assert torch.equal(poolA.data, poolB.data)
 
 
+def test_commit_layers_equals_per_layer_commit():
+    """One kda_commit_layers launch == kda_commit on each layer, bit for bit."""
+    rng = np.random.default_rng(23)
+    B, H, d, P, T, NL = 5, 4, 128, 9, 8, 3
+    slots = i32(ki.slot_table(rng, B, P))
+    pools = [_random_pool(rng, P, H, d) for _ in range(NL)]
+    pools2 = [K.StatePool(p.data.clone()) for p in pools]
+    rings = [K.ReplayRing(P, H, d, T, torch.bfloat16) for _ in range(NL)]
+    rings2 = [K.ReplayRing(P, H, d, T, torch.bfloat16) for _ in range(NL)]
+    for step in range(3):
+        toks = [device_batch(_spec_tokens(rng, B, H, d, T, "bf16"), "bf16")
+                for _ in range(NL)]
+        a = i32(ki.accepted_uniform(rng, B, T))
+        for l in range(NL):
+            K.kda_verify(toks[l], T, pools[l], slots, rings[l])
+        K.kda_commit_layers(a, slots, pools[0], rings)
+        for l in range(NL):
+            t2 = K.TokenBatch(toks[l].q, toks[l].k, toks[l].v, toks[l].alpha,
+                              toks[l].beta, toks[l].cu_seqlens)
+            K.kda_verify(t2, T, pools2[l], slots, rings2[l])
+            K.kda_commit(a, slots, pools2[l], rings2[l])
+            assert torch.equal(t2.o, toks[l].o)
+    for l in range(NL):
+        assert torch.equal(rings[l].ctrl, rings2[l].ctrl)
+        K.kda_materialize(slots, pools[l], rings[l])
+        K.kda_materialize(slots, pools2[l], rings2[l])
+        torch.cuda.synchronize()
+        assert torch.equal(pools[l].data, pools2[l].data)
+    assert K.kda_get_device_error() == 0
+
+
 def test_commit_zero_leaves_state_bytes():
     rng = np.random.default_rng(22)
     B, H, d, P, T = 3, 4, 128, 5, 8
