@@ -82,9 +82,11 @@ enum {
   KDA_DERR_DEPTH = 4,    /* a speculative segment longer than ring depth    */
   KDA_DERR_SEGMENT = 8,  /* cu_seqlens not non-decreasing / beyond N        */
   KDA_DERR_RING = 16,    /* ring control word corrupt (pending > depth)     */
-  KDA_DERR_RANGE = 32    /* prefill: cumulative log-decay across half a
+  KDA_DERR_RANGE = 32,   /* prefill: cumulative log-decay across half a
                             chunk below -80 in some channel (fp32 factor
                             range); outputs of that chunk are unreliable   */
+  KDA_DERR_TIMEOUT = 64  /* a bounded wait on the tensor cores gave up; the
+                            affected outputs were not written             */
 };
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;

@@ -1,0 +1,134 @@
+// Blackwell (sm_100-family) tensor-core helpers written against the public
+// PTX ISA: tcgen05 MMA with operands in shared memory, accumulators in tensor
+// memory (TMEM), completion through an mbarrier.
+//
+// Operand layout used everywhere in this library: "K-major, 128-byte swizzle".
+// A tile of R rows (R a multiple of 8) and K fp32/tf32 columns is stored as
+// K/32 blocks of R x 128 bytes; inside a block, row r occupies 128 bytes at
+// (r / 8) * 1024 + (r % 8) * 128 and its 16-byte chunk c sits at chunk
+// position c ^ (r % 8).  Tiles must start on a 1024-byte boundary.
+#pragma once
+
+#include <stdint.h>
+
+namespace kda {
+namespace umma {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of element (row, k) of a K-major SW128 tile with `rows` rows.
+__host__ __device__ __forceinline__ uint32_t sw128_off(int row, int k, int rows) {
+  const int kb = k >> 5, kin = k & 31;
+  const int chunk = kin >> 2, within = kin & 3;
+  const int r8 = row & 7;
+  return (uint32_t)(kb * rows * 128 + (row >> 3) * 1024 + r8 * 128 +
+                    ((chunk ^ r8) << 4) + within * 4);
+}
+
+// Shared-memory matrix descriptor: start address, leading byte offset (unused
+// for swizzled K-major tiles), stride byte offset between 8-row groups
+// (1024), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor: kind::tf32, fp32 accumulator, A and B K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) (+)= A * B^T for one K = 8 step; A is M x 8, B is N x 8 (tf32).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t da,
+                                         uint64_t db, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+// Arrive on `mbar` once every tcgen05 op issued so far by this thread is done.
+__device__ __forceinline__ void commit(uint64_t *mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      :: "r"(smem_u32(mbar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+               :: "r"(smem_u32(mbar)), "r"(count));
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Wait for phase `parity` of `mbar` to complete; gives up after `limit`
+// polls and returns false (the caller reports a device error).
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity,
+                                          int limit) {
+  uint32_t done = 0;
+  for (int it = 0; it < limit; ++it) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Warp-collective TMEM allocation of `ncols` columns (power of two >= 32);
+// the TMEM address is written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_u32(slot)), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols));
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the
+// tensor core (async proxy).
+__device__ __forceinline__ void fence_smem_to_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 consecutive TMEM columns of this thread's lane -> registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tf32 part of an fp32 value (low 13 mantissa bits cleared), exact.
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+}  // namespace umma
+}  // namespace kda

@@ -25,6 +25,7 @@
 //   o_tj    = (S^T qt_t)_j + sum_{s<=t} B_ts delta_s
 // which is the recurrence unrolled over the drafted tokens.
 #include "kda_internal.cuh"
+#include "kda_umma.cuh"
 
 namespace kda {
 namespace {
@@ -206,48 +207,84 @@ __device__ __forceinline__ void load_all_records(
   if (bdst) *bdst = bval;
 }
 
-// Shared-memory carve-up (floats) for a launch with ring depth `depth` and at
-// most `maxT` tokens per row: replay records, token records, kt, qt, kh, the
-// reduced dots xs / ys, and the kTMax x kTMax matrices A and B.
+// Shared-memory carve-up (bytes from a 1024-byte aligned base) for ring depth
+// `depth` and at most `maxT` tokens per row; TP = padded draft count (8 or
+// 16).  `a` is the tcgen05 A tile: the committed state, K-major 128B-swizzled
+// (128 rows = value columns j, K = key rows c); before that it holds the
+// token records.  `b` is the B tile [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows).
 template <int D>
 struct Smem {
-  int rep, drf, kt, qt, kh, xs, ys, am, bm, total;
+  int tp, a, b, rep, kh, vb, am, bm, total;
   __host__ __device__ Smem(int depth, int maxT) {
-    rep = 0;
-    drf = rep + depth * Rec<D>::kStride;
-    kt = drf + maxT * Rec<D>::kStride;
-    qt = kt + maxT * D;
-    kh = qt + maxT * D;
-    xs = kh + maxT * D;
-    ys = xs + maxT * D;
-    am = ys + maxT * D;
-    bm = am + kTMax * kTMax;
-    total = bm + kTMax * kTMax;
+    tp = maxT <= 8 ? 8 : 16;
+    const int kblk = (D + 31) / 32;
+    a = 0;
+    b = a + kblk * 128 * 128;
+    rep = b + kblk * 4 * tp * 128;
+    kh = rep + depth * Rec<D>::kStride * 4;
+    vb = kh + tp * D * 4;
+    am = vb + (tp * D + tp) * 4;
+    bm = am + kTMax * kTMax * 4;
+    total = bm + kTMax * kTMax * 4 + 1024;  // + alignment slack
   }
 };
 
-// Per-launch shared quantities of the chunk form (independent of S):
-// kt, qt (gamma-scaled), A (without beta) and B.
-template <int D>
-__device__ void draft_prep(float *sm, const Smem<D> &L, int T, int tid) {
+// Per-launch quantities of the chunk form that do not depend on S, built from
+// the token records at `drf`: the B tile (gamma-scaled keys and queries split
+// into tf32 hi + lo parts, zero rows past T), k / gamma (kh), v and beta
+// (vb), and the T x T matrices A (without beta) and B of the triangular
+// solve.  Also copies the drafted inputs into the ring.
+template <int D, typename Tin>
+__device__ void draft_prep(unsigned char *smb, const Smem<D> &L,
+                           const float *drf, int T, int tid, Tin *wk, Tin *wa,
+                           Tin *wv, Tin *wb) {
   constexpr int NT = 2 * D;
-  const float *rec = sm + L.drf;
-  float *kt = sm + L.kt, *qt = sm + L.qt, *kh = sm + L.kh;
+  const int TP = L.tp, N1 = 4 * TP;
+  float *kh = reinterpret_cast<float *>(smb + L.kh);
+  float *vb = reinterpret_cast<float *>(smb + L.vb);
+  float *am = reinterpret_cast<float *>(smb + L.am);
+  float *bmat = reinterpret_cast<float *>(smb + L.bm);
+  unsigned char *sb = smb + L.b;
   int unsafe = 0;
   for (int c = tid; c < D; c += NT) {
     float g = 1.f;
-    for (int t = 0; t < T; ++t) {
-      const float *r = rec + t * Rec<D>::kStride;
-      g = g * r[Rec<D>::kA + c];
-      kt[t * D + c] = g * r[Rec<D>::kK + c];
-      qt[t * D + c] = g * r[Rec<D>::kQ + c];
-      unsafe |= !(g >= 0x1p-60f && g <= 0x1p60f);
-      kh[t * D + c] = r[Rec<D>::kK + c] * __frcp_rn(g);
+    for (int t = 0; t < TP; ++t) {
+      float kt = 0.f, qt = 0.f;
+      if (t < T) {
+        const float *r = drf + t * Rec<D>::kStride;
+        g = g * r[Rec<D>::kA + c];
+        kt = g * r[Rec<D>::kK + c];
+        qt = g * r[Rec<D>::kQ + c];
+        unsafe |= !(g >= 0x1p-60f && g <= 0x1p60f);
+        kh[t * D + c] = r[Rec<D>::kK + c] * __frcp_rn(g);
+        vb[t * D + c] = r[Rec<D>::kV + c];
+      }
+      const float kth = umma::tf32_hi(kt), qth = umma::tf32_hi(qt);
+      *reinterpret_cast<float *>(sb + umma::sw128_off(t, c, N1)) = kth;
+      *reinterpret_cast<float *>(sb + umma::sw128_off(TP + t, c, N1)) = qth;
+      *reinterpret_cast<float *>(sb + umma::sw128_off(2 * TP + t, c, N1)) = kt - kth;
+      *reinterpret_cast<float *>(sb + umma::sw128_off(3 * TP + t, c, N1)) = qt - qth;
     }
+  }
+  for (int t = tid; t < T; t += NT) vb[TP * D + t] = drf[t * Rec<D>::kStride + Rec<D>::kB];
+  // ring <- drafted inputs (exact: the records hold the inputs' values)
+  {
+    constexpr int E = InVec<Tin>::kElems;
+    constexpr int CH = D / E;
+    for (int idx = tid; idx < T * 3 * CH; idx += NT) {
+      const int t = idx / (3 * CH);
+      const int r = idx - t * 3 * CH;
+      const int which = r / CH, ch = r - (r / CH) * CH;
+      const int off = which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV;
+      Tin *dst = (which == 0 ? wk : which == 1 ? wa : wv) + (size_t)t * D + ch * E;
+      InVec<Tin>::store(dst, drf + t * Rec<D>::kStride + off + ch * E);
+    }
+    for (int t = tid; t < T; t += NT)
+      out_scalar<Tin>(wb + t, drf[t * Rec<D>::kStride + Rec<D>::kB]);
   }
   unsafe = __syncthreads_or(unsafe);
   // T^2 pair dots (B: s <= t, then A: s < t), 4 lanes per pair, each lane a
-  // quarter of the key channels (interleaved float4 groups).
+  // quarter of the key channels.  kt / qt are re-formed as hi + lo (exact).
   const int nb = T * (T + 1) / 2, npairs = T * T;
   const int rg = tid & 3;
   for (int base = 0; base < npairs * 4; base += NT) {
@@ -268,27 +305,99 @@ __device__ void draft_prep(float *sm, const Smem<D> &L, int T, int tid) {
         s = r;
       }
       if (!unsafe) {
-        const float4 *x4 = reinterpret_cast<const float4 *>((isB ? qt : kt) + t * D);
-        const float4 *h4 = reinterpret_cast<const float4 *>(kh + s * D);
+        const int rh = isB ? TP + t : t;
         for (int m = rg; m < D / 4; m += 4) {
-          const float4 x = x4[m], y = h4[m];
-          acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+          const float4 xh = *reinterpret_cast<const float4 *>(sb + umma::sw128_off(rh, 4 * m, N1));
+          const float4 xl = *reinterpret_cast<const float4 *>(sb + umma::sw128_off(rh + 2 * TP, 4 * m, N1));
+          const float4 y = *reinterpret_cast<const float4 *>(kh + s * D + 4 * m);
+          acc = fmaf(xh.x + xl.x, y.x, acc);
+          acc = fmaf(xh.y + xl.y, y.y, acc);
+          acc = fmaf(xh.z + xl.z, y.z, acc);
+          acc = fmaf(xh.w + xl.w, y.w, acc);
         }
       } else {
         // decay products taken explicitly when gamma leaves the safe range
         for (int c = rg; c < D; c += 4) {
           float pr = 1.f;
-          for (int u = s + 1; u <= t; ++u) pr *= rec[u * Rec<D>::kStride + Rec<D>::kA + c];
-          const float x = rec[t * Rec<D>::kStride + (isB ? Rec<D>::kQ : Rec<D>::kK) + c];
-          acc = fmaf(x * rec[s * Rec<D>::kStride + Rec<D>::kK + c], pr, acc);
+          for (int u = s + 1; u <= t; ++u) pr *= drf[u * Rec<D>::kStride + Rec<D>::kA + c];
+          const float x = drf[t * Rec<D>::kStride + (isB ? Rec<D>::kQ : Rec<D>::kK) + c];
+          acc = fmaf(x * drf[s * Rec<D>::kStride + Rec<D>::kK + c], pr, acc);
         }
       }
     }
     acc += __shfl_xor_sync(kFull, acc, 1);
     acc += __shfl_xor_sync(kFull, acc, 2);
     if (valid && rg == 0) {
-      if (isB) sm[L.bm + t * kTMax + s] = acc;
-      else sm[L.am + t * kTMax + s] = acc;
+      if (isB) bmat[t * kTMax + s] = acc;
+      else am[t * kTMax + s] = acc;
+    }
+  }
+}
+
+// Thread's state slice -> A tile (row j, K = c), either the tf32 hi part or
+// the remainder S - hi.
+template <int D>
+__device__ __forceinline__ void write_state_tile(unsigned char *sa,
+                                                 const f2 (&S)[2][D / 8], int rg,
+                                                 int j0, bool lo_part) {
+  constexpr int F = D / 16;
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+      float x[4];
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(x[0]), "=f"(x[1]) : "l"(S[e][2 * f]));
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(x[2]), "=f"(x[3]) : "l"(S[e][2 * f + 1]));
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float hi = umma::tf32_hi(x[m]);
+        x[m] = lo_part ? x[m] - hi : hi;
+      }
+      *reinterpret_cast<float4 *>(sa + umma::sw128_off(j0 + e, 4 * (rg + 4 * f), 128)) =
+          make_float4(x[0], x[1], x[2], x[3]);
+    }
+}
+
+// Column j's drafted outputs from the accumulator lane (TMEM address ta):
+// x_t = D[t] + D[2TP + t], y_t = D[TP + t] + D[3TP + t];
+// delta_t = beta_t (v_tj - x_t - sum_{s<t} A_ts delta_s),
+// o_tj = y_t + sum_{s<=t} B_ts delta_s.  grp < 0: write every t, else only
+// t with t % 2 == grp.  Every lane of the warp must call this (TMEM load).
+template <int D, int TP>
+__device__ __forceinline__ void draft_outputs(const VerifyParams &p,
+                                              const unsigned char *smb,
+                                              const Smem<D> &L, uint32_t ta,
+                                              int j, int grp, int T, int tok0,
+                                              int h) {
+  float v[4 * TP];
+#pragma unroll
+  for (int cb = 0; cb < 4 * TP; cb += 16) {
+    float w16[16];
+    umma::tmem_ld16(ta + cb, w16);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) v[cb + m] = w16[m];
+  }
+  if (j >= D) return;
+  const float *vb = reinterpret_cast<const float *>(smb + L.vb);
+  const float *am = reinterpret_cast<const float *>(smb + L.am);
+  const float *bmat = reinterpret_cast<const float *>(smb + L.bm);
+  float del[TP];
+#pragma unroll
+  for (int t = 0; t < TP; ++t) {
+    if (t < T) {
+      float a = v[t] + v[2 * TP + t];
+#pragma unroll
+      for (int s = 0; s < t; ++s) a = fmaf(am[t * kTMax + s], del[s], a);
+      del[t] = vb[TP * D + t] * (vb[t * D + j] - a);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TP; ++t) {
+    if (t < T && (grp < 0 || (t & 1) == grp)) {
+      float o = v[TP + t] + v[3 * TP + t];
+#pragma unroll
+      for (int s = 0; s <= t; ++s) o = fmaf(bmat[t * kTMax + s], del[s], o);
+      p.o[((size_t)(tok0 + t) * p.H + h) * D + j] = o;
     }
   }
 }
@@ -296,11 +405,13 @@ __device__ void draft_prep(float *sm, const Smem<D> &L, int T, int tid) {
 template <int D, typename Tin>
 __global__ void __launch_bounds__(2 * D, 2)
     verify_kernel(const VerifyParams p) {
-  constexpr int NT = 2 * D;
   constexpr int F = D / 16;
   extern __shared__ float4 smem4[];
-  float *sm = reinterpret_cast<float *>(smem4);
+  unsigned char *smb = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
   __shared__ int s_info[6];  // skip, slot, accepted, T, tok0, spec
+  __shared__ uint64_t s_mbar;
+  __shared__ uint32_t s_tmem;
 
   const int h = blockIdx.x;
   const int i = blockIdx.y;
@@ -380,9 +491,11 @@ __global__ void __launch_bounds__(2 * D, 2)
   const int tok0 = s_info[4];
   const bool spec = s_info[5] != 0;
 
-  // 2. ring entries to replay and this launch's tokens -> shared memory
+  // 2. ring entries to replay and this launch's tokens -> shared memory (the
+  //    token records sit in the A tile's space until the drafts need it)
   const size_t unit = (size_t)slot * H + h;
-  float *tsm = sm + L.drf;
+  float *rep = reinterpret_cast<float *>(smb + L.rep);
+  float *drf = reinterpret_cast<float *>(smb + L.a);
   {
     const size_t row = (size_t)tok0 * H + h;
     const Tin *tq = reinterpret_cast<const Tin *>(p.q);
@@ -391,7 +504,7 @@ __global__ void __launch_bounds__(2 * D, 2)
     const Tin *ta = reinterpret_cast<const Tin *>(p.alpha);
     const Tin *tbe = reinterpret_cast<const Tin *>(p.beta);
     load_all_records<D, Tin>(
-        sm + L.rep, tsm, acc, T,
+        rep, drf, acc, T,
         reinterpret_cast<const Tin *>(p.rk) + unit * p.depth * D,
         reinterpret_cast<const Tin *>(p.ra) + unit * p.depth * D,
         reinterpret_cast<const Tin *>(p.rv) + unit * p.depth * D,
@@ -401,16 +514,19 @@ __global__ void __launch_bounds__(2 * D, 2)
         tbe ? tbe + row : nullptr, (size_t)H * D, (size_t)H, tid);
   }
   __syncthreads();
-  // chunk-form quantities of the drafts (do not depend on S; overlap the loads)
   if (spec && T > 0) {
-    draft_prep<D>(sm, L, T, tid);
+    draft_prep<D, Tin>(smb, L, drf, T, tid,
+                       reinterpret_cast<Tin *>(p.rk) + unit * p.depth * D,
+                       reinterpret_cast<Tin *>(p.ra) + unit * p.depth * D,
+                       reinterpret_cast<Tin *>(p.rv) + unit * p.depth * D,
+                       reinterpret_cast<Tin *>(p.rb) + unit * p.depth);
     __syncthreads();
   }
 
   // 3. lazy commit: replay the accepted entries
   float o0 = 0.f, o1 = 0.f;
   for (int t = 0; t < acc; ++t)
-    kda_step<D, false>(S, sm + L.rep + t * Rec<D>::kStride, rg, j0, o0, o1);
+    kda_step<D, false>(S, rep + t * Rec<D>::kStride, rg, j0, o0, o1);
 
   auto store_state = [&]() {
     ulonglong2 *c0 = reinterpret_cast<ulonglong2 *>(st + (size_t)j0 * D);
@@ -425,7 +541,7 @@ __global__ void __launch_bounds__(2 * D, 2)
   if (!spec) {
     // ordinary decode (or materialize): apply and commit
     for (int t = 0; t < T; ++t) {
-      kda_step<D, true>(S, tsm + t * Rec<D>::kStride, rg, j0, o0, o1);
+      kda_step<D, true>(S, drf + t * Rec<D>::kStride, rg, j0, o0, o1);
       if (rg == 0)
         *reinterpret_cast<float2 *>(p.o + ((size_t)(tok0 + t) * H + h) * D + j0) =
             make_float2(o0, o1);
@@ -440,123 +556,83 @@ __global__ void __launch_bounds__(2 * D, 2)
   }
 
   if (acc > 0) store_state();
-  // ring <- this launch's drafted inputs (the replayed entries are in smem)
-  {
-    constexpr int E = InVec<Tin>::kElems;
-    constexpr int CH = D / E;
-    Tin *wk = reinterpret_cast<Tin *>(p.rk) + unit * p.depth * D;
-    Tin *wa = reinterpret_cast<Tin *>(p.ra) + unit * p.depth * D;
-    Tin *wv = reinterpret_cast<Tin *>(p.rv) + unit * p.depth * D;
-    Tin *wb = reinterpret_cast<Tin *>(p.rb) + unit * p.depth;
-    for (int idx = tid; idx < T * 3 * CH; idx += NT) {
-      const int t = idx / (3 * CH);
-      const int r = idx - t * 3 * CH;
-      const int which = r / CH, ch = r - (r / CH) * CH;
-      const int off = which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV;
-      Tin *dst = (which == 0 ? wk : which == 1 ? wa : wv) + (size_t)t * D + ch * E;
-      InVec<Tin>::store(dst, tsm + t * Rec<D>::kStride + off + ch * E);
-    }
-    for (int t = tid; t < T; t += NT)
-      out_scalar<Tin>(wb + t, tsm[t * Rec<D>::kStride + Rec<D>::kB]);
-  }
   if (tid == 0) {
     int32_t *c = p.ctrl + unit * 2;
     c[0] = T;
     c[1] = 0;
   }
+  if (T == 0) return;
 
-  // 4. drafts: (S^T kt_t, S^T qt_t) for the thread's two columns, four
-  //    drafted tokens per pass, then a column-wise triangular solve.
-  const float *kt = sm + L.kt;
-  const float *qt = sm + L.qt;
-  float *xs = sm + L.xs;
-  float *ys = sm + L.ys;
-  for (int t0 = 0; t0 < T; t0 += 4) {
-    f2 ak[4][2], aq[4][2];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      ak[u][0] = ak[u][1] = aq[u][0] = aq[u][1] = 0;
-#pragma unroll
-    for (int f = 0; f < F; ++f) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (t0 + u < T) {
-          const ulonglong2 kk =
-              reinterpret_cast<const ulonglong2 *>(kt + (t0 + u) * D)[rg + 4 * f];
-          const ulonglong2 qq =
-              reinterpret_cast<const ulonglong2 *>(qt + (t0 + u) * D)[rg + 4 * f];
-          ak[u][0] = fma2(kk.x, S[0][2 * f], ak[u][0]);
-          ak[u][0] = fma2(kk.y, S[0][2 * f + 1], ak[u][0]);
-          ak[u][1] = fma2(kk.x, S[1][2 * f], ak[u][1]);
-          ak[u][1] = fma2(kk.y, S[1][2 * f + 1], ak[u][1]);
-          aq[u][0] = fma2(qq.x, S[0][2 * f], aq[u][0]);
-          aq[u][0] = fma2(qq.y, S[0][2 * f + 1], aq[u][0]);
-          aq[u][1] = fma2(qq.x, S[1][2 * f], aq[u][1]);
-          aq[u][1] = fma2(qq.y, S[1][2 * f + 1], aq[u][1]);
-        }
-      }
-    }
-    // reduce the 16 partial dots (4 tokens x {x0, x1, y0, y1}) over the four
-    // row groups of the column pair; lane rg ends with token t0 + rg.
-    {
-      float v[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        v[u][0] = sum2(ak[u][0]);
-        v[u][1] = sum2(ak[u][1]);
-        v[u][2] = sum2(aq[u][0]);
-        v[u][3] = sum2(aq[u][1]);
-      }
-      const bool hi2 = (rg & 2) != 0, hi1 = (rg & 1) != 0;
-      float r[2][4];
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float keep = hi2 ? v[u + 2][w] : v[u][w];
-          const float give = hi2 ? v[u][w] : v[u + 2][w];
-          r[u][w] = keep + __shfl_xor_sync(kFull, give, 2);
-        }
-      float fin[4];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float keep = hi1 ? r[1][w] : r[0][w];
-        const float give = hi1 ? r[0][w] : r[1][w];
-        fin[w] = keep + __shfl_xor_sync(kFull, give, 1);
-      }
-      const int t = t0 + rg;
-      if (t < T) {
-        *reinterpret_cast<float2 *>(xs + t * D + j0) = make_float2(fin[0], fin[1]);
-        *reinterpret_cast<float2 *>(ys + t * D + j0) = make_float2(fin[2], fin[3]);
-      }
-    }
-  }
+  // 4. drafts: X = S^T [K~ | Q~] on the tensor cores, 3xTF32:
+  //    pass 1  D  = S_hi [K~_hi Q~_hi K~_lo Q~_lo]^T   (N = 4 TP)
+  //    pass 2  D += S_lo [K~_hi Q~_hi]^T               (N = 2 TP, first columns)
+  //    x_t = D[t] + D[2TP + t],  y_t = D[TP + t] + D[3TP + t]
+  const int TP = L.tp, N1 = 4 * TP, N2 = 2 * TP;
+  unsigned char *sa = smb + L.a;
+  if (tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)N1);
+  if (tid == 0) umma::mbar_init(&s_mbar, 1);
+  write_state_tile<D>(sa, S, rg, j0, false);
+  umma::fence_smem_to_async();
+  umma::fence_before_sync();
   __syncthreads();
-  // column-wise forward substitution: thread -> (column, parity of t)
-  {
-    const int j = tid >> 1, par = tid & 1;
-    const float *am = sm + L.am, *bm = sm + L.bm;
-    float del[kTMax];
-#pragma unroll
-    for (int t = 0; t < kTMax; ++t) {
-      if (t < T) {
-        const float *r = tsm + t * Rec<D>::kStride;
-        float a = xs[t * D + j];
-#pragma unroll
-        for (int s = 0; s < t; ++s) a = fmaf(am[t * kTMax + s], del[s], a);
-        del[t] = r[Rec<D>::kB] * (r[Rec<D>::kV + j] - a);
-      }
+  umma::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  const uint32_t a_base = umma::smem_u32(sa), b_base = umma::smem_u32(smb + L.b);
+  constexpr int NK = D / 8;
+  if (tid == 0) {
+    const uint32_t id1 = umma::idesc_tf32(128, N1);
+    for (int s = 0; s < NK; ++s)
+      umma::mma_tf32(tmem, umma::sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32),
+                     umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
+                     id1, s > 0 ? 1u : 0u);
+    umma::commit(&s_mbar);
+  }
+  bool ok = umma::mbar_wait(&s_mbar, 0, 1 << 22);
+  int waiting = ok ? -1 : 0;  // phase still owed by the tensor cores
+  if (ok) {
+    write_state_tile<D>(sa, S, rg, j0, true);
+    umma::fence_smem_to_async();
+  }
+  umma::fence_before_sync();
+  ok = __syncthreads_and(ok);
+  umma::fence_after_sync();
+  if (ok) {
+    if (tid == 0) {
+      const uint32_t id2 = umma::idesc_tf32(128, N2);
+      for (int s = 0; s < NK; ++s)
+        umma::mma_tf32(tmem, umma::sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32),
+                       umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
+                       id2, 1u);
+      umma::commit(&s_mbar);
     }
-#pragma unroll
-    for (int t = 0; t < kTMax; ++t) {
-      if (t < T && (t & 1) == par) {
-        float o = ys[t * D + j];
-#pragma unroll
-        for (int s = 0; s <= t; ++s) o = fmaf(bm[t * kTMax + s], del[s], o);
-        p.o[((size_t)(tok0 + t) * H + h) * D + j] = o;
-      }
+    ok = umma::mbar_wait(&s_mbar, 1, 1 << 22);
+    if (!ok) waiting = 1;
+  }
+  umma::fence_after_sync();
+  ok = __syncthreads_and(ok);
+  if (!ok) {
+    if (tid == 0) set_error(p.err, KDA_DERR_TIMEOUT);
+    // give the tensor cores one more bounded chance before TMEM is freed
+    if (waiting >= 0) umma::mbar_wait(&s_mbar, (uint32_t)waiting, 1 << 26);
+  } else {
+    // 5. one thread per value column j: triangular solve and outputs.  Warp w
+    //    reads TMEM lanes 32 (w % 4) ..; with D = 128 the upper four warps
+    //    repeat the solve and write the odd drafted positions.
+    const bool warp_on = (tid >> 5) < (D < 128 ? (D + 31) / 32 : 8);
+    if (warp_on) {
+      const int q = (tid >> 5) & 3;
+      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16);
+      const int j = (q << 5) + (tid & 31);
+      const int grp = D < 128 ? -1 : (tid >> 7);
+      if (TP == 8)
+        draft_outputs<D, 8>(p, smb, L, ta, j, grp, T, tok0, h);
+      else
+        draft_outputs<D, 16>(p, smb, L, ta, j, grp, T, tok0, h);
     }
   }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) umma::tmem_dealloc(tmem, (uint32_t)N1);
 }
 
 __global__ void commit_kernel(const CommitParams p) {
@@ -638,10 +714,10 @@ cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
 
 size_t verify_smem_bytes(int D, int depth, int max_T) {
   switch (D) {
-    case 16: return sizeof(float) * Smem<16>(depth, max_T).total;
-    case 32: return sizeof(float) * Smem<32>(depth, max_T).total;
-    case 64: return sizeof(float) * Smem<64>(depth, max_T).total;
-    case 128: return sizeof(float) * Smem<128>(depth, max_T).total;
+    case 16: return Smem<16>(depth, max_T).total;
+    case 32: return Smem<32>(depth, max_T).total;
+    case 64: return Smem<64>(depth, max_T).total;
+    case 128: return Smem<128>(depth, max_T).total;
     default: return 0;
   }
 }

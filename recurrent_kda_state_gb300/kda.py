@@ -17,6 +17,7 @@ KDA_OK, KDA_EINVAL, KDA_EDTYPE, KDA_ESHAPE, KDA_EALIGN = 0, -1, -2, -3, -4
 KDA_EPROTO, KDA_ECUDA, KDA_EDEVICE, KDA_ENOSPC = -5, -6, -7, -8
 KDA_DERR_SLOT, KDA_DERR_ACCEPT, KDA_DERR_DEPTH = 1, 2, 4
 KDA_DERR_SEGMENT, KDA_DERR_RING, KDA_DERR_RANGE = 8, 16, 32
+KDA_DERR_TIMEOUT = 64
 KDA_F32, KDA_BF16 = 0, 1
 
 _P = ctypes.c_void_p
