@@ -245,26 +245,43 @@ __device__ void draft_prep(unsigned char *smb, const Smem<D> &L,
   float *am = reinterpret_cast<float *>(smb + L.am);
   float *bmat = reinterpret_cast<float *>(smb + L.bm);
   unsigned char *sb = smb + L.b;
+  // one thread per (4 key channels, drafted row t): gamma_t = prod_{r<=t}
+  // alpha_r, then the B tile rows t, TP+t, 2TP+t, 3TP+t as 16-byte stores.
   int unsafe = 0;
-  for (int c = tid; c < D; c += NT) {
-    float g = 1.f;
-    for (int t = 0; t < TP; ++t) {
-      float kt = 0.f, qt = 0.f;
-      if (t < T) {
-        const float *r = drf + t * Rec<D>::kStride;
-        g = g * r[Rec<D>::kA + c];
-        kt = g * r[Rec<D>::kK + c];
-        qt = g * r[Rec<D>::kQ + c];
-        unsafe |= !(g >= 0x1p-60f && g <= 0x1p60f);
-        kh[t * D + c] = r[Rec<D>::kK + c] * __frcp_rn(g);
-        vb[t * D + c] = r[Rec<D>::kV + c];
+  for (int item = tid; item < (D / 4) * TP; item += NT) {
+    const int c4 = item % (D / 4), t = item / (D / 4);
+    float4 kt = make_float4(0.f, 0.f, 0.f, 0.f), qt = kt;
+    if (t < T) {
+      float4 g = *reinterpret_cast<const float4 *>(drf + Rec<D>::kA + 4 * c4);
+      for (int r = 1; r <= t; ++r) {
+        const float4 a = *reinterpret_cast<const float4 *>(
+            drf + r * Rec<D>::kStride + Rec<D>::kA + 4 * c4);
+        g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
       }
-      const float kth = umma::tf32_hi(kt), qth = umma::tf32_hi(qt);
-      *reinterpret_cast<float *>(sb + umma::sw128_off(t, c, N1)) = kth;
-      *reinterpret_cast<float *>(sb + umma::sw128_off(TP + t, c, N1)) = qth;
-      *reinterpret_cast<float *>(sb + umma::sw128_off(2 * TP + t, c, N1)) = kt - kth;
-      *reinterpret_cast<float *>(sb + umma::sw128_off(3 * TP + t, c, N1)) = qt - qth;
+      const float *rr = drf + t * Rec<D>::kStride;
+      const float4 k = *reinterpret_cast<const float4 *>(rr + Rec<D>::kK + 4 * c4);
+      const float4 q = *reinterpret_cast<const float4 *>(rr + Rec<D>::kQ + 4 * c4);
+      kt = make_float4(g.x * k.x, g.y * k.y, g.z * k.z, g.w * k.w);
+      qt = make_float4(g.x * q.x, g.y * q.y, g.z * q.z, g.w * q.w);
+      const float gm = fminf(fminf(g.x, g.y), fminf(g.z, g.w));
+      const float gx = fmaxf(fmaxf(g.x, g.y), fmaxf(g.z, g.w));
+      unsafe |= !(gm >= 0x1p-60f && gx <= 0x1p60f);
+      *reinterpret_cast<float4 *>(kh + t * D + 4 * c4) =
+          make_float4(k.x * __frcp_rn(g.x), k.y * __frcp_rn(g.y),
+                      k.z * __frcp_rn(g.z), k.w * __frcp_rn(g.w));
+      *reinterpret_cast<float4 *>(vb + t * D + 4 * c4) =
+          *reinterpret_cast<const float4 *>(rr + Rec<D>::kV + 4 * c4);
     }
+    const float4 kh4 = make_float4(umma::tf32_hi(kt.x), umma::tf32_hi(kt.y),
+                                   umma::tf32_hi(kt.z), umma::tf32_hi(kt.w));
+    const float4 qh4 = make_float4(umma::tf32_hi(qt.x), umma::tf32_hi(qt.y),
+                                   umma::tf32_hi(qt.z), umma::tf32_hi(qt.w));
+    *reinterpret_cast<float4 *>(sb + umma::sw128_off(t, 4 * c4, N1)) = kh4;
+    *reinterpret_cast<float4 *>(sb + umma::sw128_off(TP + t, 4 * c4, N1)) = qh4;
+    *reinterpret_cast<float4 *>(sb + umma::sw128_off(2 * TP + t, 4 * c4, N1)) =
+        make_float4(kt.x - kh4.x, kt.y - kh4.y, kt.z - kh4.z, kt.w - kh4.w);
+    *reinterpret_cast<float4 *>(sb + umma::sw128_off(3 * TP + t, 4 * c4, N1)) =
+        make_float4(qt.x - qh4.x, qt.y - qh4.y, qt.z - qh4.z, qt.w - qh4.w);
   }
   for (int t = tid; t < T; t += NT) vb[TP * D + t] = drf[t * Rec<D>::kStride + Rec<D>::kB];
   // ring <- drafted inputs (exact: the records hold the inputs' values)
@@ -342,7 +359,12 @@ __device__ __forceinline__ void write_state_tile(unsigned char *sa,
                                                  int j0, bool lo_part) {
   constexpr int F = D / 16;
 #pragma unroll
-  for (int e = 0; e < 2; ++e)
+  for (int e = 0; e < 2; ++e) {
+    // row j = j0 + e of the tile; key chunk (rg + 4 f) lies in 32-wide block
+    // f / 2 at chunk position rg + 4 (f % 2), swizzled by j % 8.
+    const int j = j0 + e;
+    unsigned char *row = sa + (j >> 3) * 1024 + (j & 7) * 128;
+    const int x0 = (rg ^ (j & 7)) << 4, x1 = ((rg + 4) ^ (j & 7)) << 4;
 #pragma unroll
     for (int f = 0; f < F; ++f) {
       float x[4];
@@ -353,9 +375,10 @@ __device__ __forceinline__ void write_state_tile(unsigned char *sa,
         const float hi = umma::tf32_hi(x[m]);
         x[m] = lo_part ? x[m] - hi : hi;
       }
-      *reinterpret_cast<float4 *>(sa + umma::sw128_off(j0 + e, 4 * (rg + 4 * f), 128)) =
+      *reinterpret_cast<float4 *>(row + (f >> 1) * 16384 + ((f & 1) ? x1 : x0)) =
           make_float4(x[0], x[1], x[2], x[3]);
     }
+  }
 }
 
 // Column j's drafted outputs from the accumulator lane (TMEM address ta):
@@ -402,7 +425,7 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
   }
 }
 
-template <int D, typename Tin>
+template <int D, typename Tin, int TPC>
 __global__ void __launch_bounds__(2 * D, 2)
     verify_kernel(const VerifyParams p) {
   constexpr int F = D / 16;
@@ -567,7 +590,7 @@ __global__ void __launch_bounds__(2 * D, 2)
   //    pass 1  D  = S_hi [K~_hi Q~_hi K~_lo Q~_lo]^T   (N = 4 TP)
   //    pass 2  D += S_lo [K~_hi Q~_hi]^T               (N = 2 TP, first columns)
   //    x_t = D[t] + D[2TP + t],  y_t = D[TP + t] + D[3TP + t]
-  const int TP = L.tp, N1 = 4 * TP, N2 = 2 * TP;
+  constexpr int TP = TPC, N1 = 4 * TP, N2 = 2 * TP;
   unsigned char *sa = smb + L.a;
   if (tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)N1);
   if (tid == 0) umma::mbar_init(&s_mbar, 1);
@@ -624,10 +647,7 @@ __global__ void __launch_bounds__(2 * D, 2)
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16);
       const int j = (q << 5) + (tid & 31);
       const int grp = D < 128 ? -1 : (tid >> 7);
-      if (TP == 8)
-        draft_outputs<D, 8>(p, smb, L, ta, j, grp, T, tok0, h);
-      else
-        draft_outputs<D, 16>(p, smb, L, ta, j, grp, T, tok0, h);
+      draft_outputs<D, TPC>(p, smb, L, ta, j, grp, T, tok0, h);
     }
   }
   umma::fence_before_sync();
@@ -690,7 +710,7 @@ __global__ void ring_reset_kernel(const CommitParams p) {
 template <int D, typename Tin>
 cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
   const size_t smem = verify_smem_bytes(D, p.depth, p.max_T);
-  auto kern = verify_kernel<D, Tin>;
+  auto kern = p.max_T <= 8 ? verify_kernel<D, Tin, 8> : verify_kernel<D, Tin, 16>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
