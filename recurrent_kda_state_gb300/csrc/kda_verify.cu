@@ -24,6 +24,10 @@
 //   delta_t = beta_t (v_tj - (S^T kt_t)_j - sum_{s<t} A_ts delta_s)
 //   o_tj    = (S^T qt_t)_j + sum_{s<=t} B_ts delta_s
 // which is the recurrence unrolled over the drafted tokens.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_umma.cuh"
 
@@ -149,8 +153,10 @@ __device__ __forceinline__ void cvt16<__nv_bfloat16>(const uint4 &raw, float *ds
 
 // Ring entries to replay (k, alpha, v, beta of `acc` entries) and this
 // launch's tokens (k, alpha, v, q, beta of T rows) -> fp32 records in shared
-// memory.  Loads are issued in batches of four 16-byte vectors per thread
-// before any of them is converted, so their latencies overlap.
+// memory.  Vector rows are numbered ring-first (3 per entry) then token rows
+// (4 per token); thread tid always copies 16-byte chunk tid % CH of rows
+// tid / CH, + NT / CH, ...  All of a thread's loads are issued before any of
+// them is converted.
 template <int D, typename Tin>
 __device__ __forceinline__ void load_all_records(
     float *rep, float *drf, int acc, int T, const Tin *rk, const Tin *ra,
@@ -159,10 +165,11 @@ __device__ __forceinline__ void load_all_records(
     int tid) {
   constexpr int NT = 2 * D;
   constexpr int E = InVec<Tin>::kElems;
-  constexpr int CH = D / E;
-  constexpr int R = 4;
-  const int nring = acc * 3 * CH;
-  const int ntot = nring + T * 4 * CH;
+  constexpr int CH = D / E;         // power of two
+  constexpr int RSTEP = NT / CH;    // vector rows per pass
+  constexpr int R = 4;              // loads in flight per thread
+  const int ch = tid % CH;
+  const int nring = acc * 3, nrows = nring + T * 4;
   float bval = 0.f;
   float *bdst = nullptr;
   if (tid < acc) {
@@ -172,27 +179,25 @@ __device__ __forceinline__ void load_all_records(
     bval = in_scalar<Tin>(tb + (size_t)(tid - acc) * beta_stride);
     bdst = drf + (tid - acc) * Rec<D>::kStride + Rec<D>::kB;
   }
-  for (int base = 0; base < ntot; base += R * NT) {
+  for (int base = tid / CH; base < nrows; base += R * RSTEP) {
     uint4 buf[R];
     float *dst[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int idx = base + r * NT + tid;
+      const int row = base + r * RSTEP;
       dst[r] = nullptr;
-      if (idx < ntot) {
+      if (row < nrows) {
         const Tin *src;
-        if (idx < nring) {
-          const int t = idx / (3 * CH), rem = idx - t * 3 * CH;
-          const int which = rem / CH, ch = rem - which * CH;
+        if (row < nring) {
+          const int t = row / 3, which = row - 3 * (row / 3);
           src = (which == 0 ? rk : which == 1 ? ra : rv) + t * D + ch * E;
           dst[r] = rep + t * Rec<D>::kStride +
                    (which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV) + ch * E;
         } else {
-          const int j = idx - nring;
-          const int t = j / (4 * CH), rem = j - t * 4 * CH;
-          const int which = rem / CH, ch = rem - which * CH;
-          src = (which == 0 ? tk : which == 1 ? ta : which == 2 ? tv : tq) +
-                (size_t)t * tok_stride + ch * E;
+          const int rr = row - nring;
+          const int t = rr >> 2, which = rr & 3;
+          const Tin *base_ptr = which == 0 ? tk : which == 1 ? ta : which == 2 ? tv : tq;
+          src = base_ptr + (size_t)t * tok_stride + ch * E;
           dst[r] = drf + t * Rec<D>::kStride +
                    (which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA
                     : which == 2 ? Rec<D>::kV : Rec<D>::kQ) + ch * E;
@@ -209,19 +214,25 @@ __device__ __forceinline__ void load_all_records(
 
 // Shared-memory carve-up (bytes from a 1024-byte aligned base) for ring depth
 // `depth` and at most `maxT` tokens per row; TP = padded draft count (8 or
-// 16).  `a` is the tcgen05 A tile: the committed state, K-major 128B-swizzled
-// (128 rows = value columns j, K = key rows c); before that it holds the
-// token records.  `b` is the B tile [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows).
+// 16).
+//   a    tcgen05 A tile: the committed state, K-major 128B-swizzled (128 rows
+//        = value columns j, K = key rows c);
+//   rb   the replay records, later (once replayed) the B tile
+//        [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows, K-major 128B-swizzled);
+//   drf  this launch's token records;  kh = k / gamma;  vb = v and beta of the
+//        drafted tokens;  am, bm = the T x T matrices of the triangular solve.
 template <int D>
 struct Smem {
-  int tp, a, b, rep, kh, vb, am, bm, total;
+  int tp, a, rb, drf, kh, vb, am, bm, total;
   __host__ __device__ Smem(int depth, int maxT) {
     tp = maxT <= 8 ? 8 : 16;
     const int kblk = (D + 31) / 32;
+    const int rep_bytes = depth * Rec<D>::kStride * 4;
+    const int b_bytes = kblk * 4 * tp * 128;
     a = 0;
-    b = a + kblk * 128 * 128;
-    rep = b + kblk * 4 * tp * 128;
-    kh = rep + depth * Rec<D>::kStride * 4;
+    rb = kblk * 128 * 128;
+    drf = rb + (((rep_bytes > b_bytes ? rep_bytes : b_bytes) + 1023) & ~1023);
+    kh = drf + maxT * Rec<D>::kStride * 4;
     vb = kh + tp * D * 4;
     am = vb + (tp * D + tp) * 4;
     bm = am + kTMax * kTMax * 4;
@@ -229,34 +240,32 @@ struct Smem {
   }
 };
 
-// Per-launch quantities of the chunk form that do not depend on S, built from
-// the token records at `drf`: the B tile (gamma-scaled keys and queries split
-// into tf32 hi + lo parts, zero rows past T), k / gamma (kh), v and beta
-// (vb), and the T x T matrices A (without beta) and B of the triangular
-// solve.  Also copies the drafted inputs into the ring.
-template <int D, typename Tin>
-__device__ void draft_prep(unsigned char *smb, const Smem<D> &L,
-                           const float *drf, int T, int tid, Tin *wk, Tin *wa,
-                           Tin *wv, Tin *wb) {
-  constexpr int NT = 2 * D;
-  const int TP = L.tp, N1 = 4 * TP;
+// Chunk-form quantities of the drafts that do not depend on S, part 1: one
+// thread per (4 key channels, drafted row t): gamma_t = prod_{r<=t} alpha_r,
+// the B tile rows t, TP+t (gamma k, gamma q as fp32: the tensor cores read
+// their tf32 part) and 2TP+t, 3TP+t (the remainders past tf32), zero rows
+// past T, kh = k / gamma, and v, beta.  Returns whether
+// gamma left [2^-60, 2^60] anywhere (then A and B use explicit products).
+template <int D, int TP>
+__device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
+                                          const float *drf, int T, int tid) {
+  constexpr int NT = 2 * D, N1 = 4 * TP;
   float *kh = reinterpret_cast<float *>(smb + L.kh);
   float *vb = reinterpret_cast<float *>(smb + L.vb);
-  float *am = reinterpret_cast<float *>(smb + L.am);
-  float *bmat = reinterpret_cast<float *>(smb + L.bm);
-  unsigned char *sb = smb + L.b;
-  // one thread per (4 key channels, drafted row t): gamma_t = prod_{r<=t}
-  // alpha_r, then the B tile rows t, TP+t, 2TP+t, 3TP+t as 16-byte stores.
+  unsigned char *sb = smb + L.rb;
   int unsafe = 0;
   for (int item = tid; item < (D / 4) * TP; item += NT) {
     const int c4 = item % (D / 4), t = item / (D / 4);
     float4 kt = make_float4(0.f, 0.f, 0.f, 0.f), qt = kt;
     if (t < T) {
       float4 g = *reinterpret_cast<const float4 *>(drf + Rec<D>::kA + 4 * c4);
-      for (int r = 1; r <= t; ++r) {
-        const float4 a = *reinterpret_cast<const float4 *>(
-            drf + r * Rec<D>::kStride + Rec<D>::kA + 4 * c4);
-        g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
+#pragma unroll
+      for (int r = 1; r < TP; ++r) {
+        if (r <= t) {
+          const float4 a = *reinterpret_cast<const float4 *>(
+              drf + r * Rec<D>::kStride + Rec<D>::kA + 4 * c4);
+          g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
+        }
       }
       const float *rr = drf + t * Rec<D>::kStride;
       const float4 k = *reinterpret_cast<const float4 *>(rr + Rec<D>::kK + 4 * c4);
@@ -267,41 +276,39 @@ __device__ void draft_prep(unsigned char *smb, const Smem<D> &L,
       const float gx = fmaxf(fmaxf(g.x, g.y), fmaxf(g.z, g.w));
       unsafe |= !(gm >= 0x1p-60f && gx <= 0x1p60f);
       *reinterpret_cast<float4 *>(kh + t * D + 4 * c4) =
-          make_float4(k.x * __frcp_rn(g.x), k.y * __frcp_rn(g.y),
-                      k.z * __frcp_rn(g.z), k.w * __frcp_rn(g.w));
+          make_float4(__fdividef(k.x, g.x), __fdividef(k.y, g.y),
+                      __fdividef(k.z, g.z), __fdividef(k.w, g.w));
       *reinterpret_cast<float4 *>(vb + t * D + 4 * c4) =
           *reinterpret_cast<const float4 *>(rr + Rec<D>::kV + 4 * c4);
+      if (c4 == 0) vb[TP * D + t] = rr[Rec<D>::kB];
     }
+    // the tensor cores read fp32 operands as tf32 by dropping the low 13
+    // mantissa bits, so the hi rows take the values as they are
     const float4 kh4 = make_float4(umma::tf32_hi(kt.x), umma::tf32_hi(kt.y),
                                    umma::tf32_hi(kt.z), umma::tf32_hi(kt.w));
     const float4 qh4 = make_float4(umma::tf32_hi(qt.x), umma::tf32_hi(qt.y),
                                    umma::tf32_hi(qt.z), umma::tf32_hi(qt.w));
-    *reinterpret_cast<float4 *>(sb + umma::sw128_off(t, 4 * c4, N1)) = kh4;
-    *reinterpret_cast<float4 *>(sb + umma::sw128_off(TP + t, 4 * c4, N1)) = qh4;
+    *reinterpret_cast<float4 *>(sb + umma::sw128_off(t, 4 * c4, N1)) = kt;
+    *reinterpret_cast<float4 *>(sb + umma::sw128_off(TP + t, 4 * c4, N1)) = qt;
     *reinterpret_cast<float4 *>(sb + umma::sw128_off(2 * TP + t, 4 * c4, N1)) =
         make_float4(kt.x - kh4.x, kt.y - kh4.y, kt.z - kh4.z, kt.w - kh4.w);
     *reinterpret_cast<float4 *>(sb + umma::sw128_off(3 * TP + t, 4 * c4, N1)) =
         make_float4(qt.x - qh4.x, qt.y - qh4.y, qt.z - qh4.z, qt.w - qh4.w);
   }
-  for (int t = tid; t < T; t += NT) vb[TP * D + t] = drf[t * Rec<D>::kStride + Rec<D>::kB];
-  // ring <- drafted inputs (exact: the records hold the inputs' values)
-  {
-    constexpr int E = InVec<Tin>::kElems;
-    constexpr int CH = D / E;
-    for (int idx = tid; idx < T * 3 * CH; idx += NT) {
-      const int t = idx / (3 * CH);
-      const int r = idx - t * 3 * CH;
-      const int which = r / CH, ch = r - (r / CH) * CH;
-      const int off = which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV;
-      Tin *dst = (which == 0 ? wk : which == 1 ? wa : wv) + (size_t)t * D + ch * E;
-      InVec<Tin>::store(dst, drf + t * Rec<D>::kStride + off + ch * E);
-    }
-    for (int t = tid; t < T; t += NT)
-      out_scalar<Tin>(wb + t, drf[t * Rec<D>::kStride + Rec<D>::kB]);
-  }
-  unsafe = __syncthreads_or(unsafe);
-  // T^2 pair dots (B: s <= t, then A: s < t), 4 lanes per pair, each lane a
-  // quarter of the key channels.  kt / qt are re-formed as hi + lo (exact).
+  return unsafe;
+}
+
+// Part 2: the T^2 pair dots (B: s <= t, then A: s < t; A without beta),
+// 4 lanes per pair, each lane a quarter of the key channels.
+template <int D, int TP>
+__device__ __forceinline__ void prep_pairs(unsigned char *smb,
+                                           const Smem<D> &L, const float *drf,
+                                           int T, int tid, int unsafe) {
+  constexpr int NT = 2 * D, N1 = 4 * TP;
+  const float *kh = reinterpret_cast<const float *>(smb + L.kh);
+  float *am = reinterpret_cast<float *>(smb + L.am);
+  float *bmat = reinterpret_cast<float *>(smb + L.bm);
+  const unsigned char *sb = smb + L.rb;
   const int nb = T * (T + 1) / 2, npairs = T * T;
   const int rg = tid & 3;
   for (int base = 0; base < npairs * 4; base += NT) {
@@ -322,15 +329,22 @@ __device__ void draft_prep(unsigned char *smb, const Smem<D> &L,
         s = r;
       }
       if (!unsafe) {
+        // rows t (gamma k) and TP + t (gamma q) of the B tile hold the exact
+        // fp32 values; chunk m = rg + 4 u sits in 32-wide block u / 2 at
+        // position rg + 4 (u % 2)
         const int rh = isB ? TP + t : t;
-        for (int m = rg; m < D / 4; m += 4) {
-          const float4 xh = *reinterpret_cast<const float4 *>(sb + umma::sw128_off(rh, 4 * m, N1));
-          const float4 xl = *reinterpret_cast<const float4 *>(sb + umma::sw128_off(rh + 2 * TP, 4 * m, N1));
+        const unsigned char *hrow = sb + (rh >> 3) * 1024 + (rh & 7) * 128;
+        const int x0 = (rg ^ (rh & 7)) << 4, x1 = ((rg + 4) ^ (rh & 7)) << 4;
+#pragma unroll
+        for (int u = 0; u < D / 16; ++u) {
+          const int m = rg + 4 * u;
+          const float4 x = *reinterpret_cast<const float4 *>(
+              hrow + (u >> 1) * N1 * 128 + ((u & 1) ? x1 : x0));
           const float4 y = *reinterpret_cast<const float4 *>(kh + s * D + 4 * m);
-          acc = fmaf(xh.x + xl.x, y.x, acc);
-          acc = fmaf(xh.y + xl.y, y.y, acc);
-          acc = fmaf(xh.z + xl.z, y.z, acc);
-          acc = fmaf(xh.w + xl.w, y.w, acc);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+          acc = fmaf(x.z, y.z, acc);
+          acc = fmaf(x.w, y.w, acc);
         }
       } else {
         // decay products taken explicitly when gamma leaves the safe range
@@ -351,8 +365,8 @@ __device__ void draft_prep(unsigned char *smb, const Smem<D> &L,
   }
 }
 
-// Thread's state slice -> A tile (row j, K = c), either the tf32 hi part or
-// the remainder S - hi.
+// Thread's state slice -> A tile (row j, K = c): the values as they are (the
+// tensor cores use their tf32 part), or the remainder S - tf32(S).
 template <int D>
 __device__ __forceinline__ void write_state_tile(unsigned char *sa,
                                                  const f2 (&S)[2][D / 8], int rg,
@@ -360,8 +374,8 @@ __device__ __forceinline__ void write_state_tile(unsigned char *sa,
   constexpr int F = D / 16;
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    // row j = j0 + e of the tile; key chunk (rg + 4 f) lies in 32-wide block
-    // f / 2 at chunk position rg + 4 (f % 2), swizzled by j % 8.
+    // row j = j0 + e; key chunk (rg + 4 f) lies in 32-wide block f / 2 at
+    // chunk position rg + 4 (f % 2), swizzled by j % 8
     const int j = j0 + e;
     unsigned char *row = sa + (j >> 3) * 1024 + (j & 7) * 128;
     const int x0 = (rg ^ (j & 7)) << 4, x1 = ((rg + 4) ^ (j & 7)) << 4;
@@ -370,10 +384,9 @@ __device__ __forceinline__ void write_state_tile(unsigned char *sa,
       float x[4];
       asm("mov.b64 {%0, %1}, %2;" : "=f"(x[0]), "=f"(x[1]) : "l"(S[e][2 * f]));
       asm("mov.b64 {%0, %1}, %2;" : "=f"(x[2]), "=f"(x[3]) : "l"(S[e][2 * f + 1]));
+      if (lo_part) {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float hi = umma::tf32_hi(x[m]);
-        x[m] = lo_part ? x[m] - hi : hi;
+        for (int m = 0; m < 4; ++m) x[m] = x[m] - umma::tf32_hi(x[m]);
       }
       *reinterpret_cast<float4 *>(row + (f >> 1) * 16384 + ((f & 1) ? x1 : x0)) =
           make_float4(x[0], x[1], x[2], x[3]);
@@ -384,21 +397,28 @@ __device__ __forceinline__ void write_state_tile(unsigned char *sa,
 // Column j's drafted outputs from the accumulator lane (TMEM address ta):
 // x_t = D[t] + D[2TP + t], y_t = D[TP + t] + D[3TP + t];
 // delta_t = beta_t (v_tj - x_t - sum_{s<t} A_ts delta_s),
-// o_tj = y_t + sum_{s<=t} B_ts delta_s.  grp < 0: write every t, else only
-// t with t % 2 == grp.  Every lane of the warp must call this (TMEM load).
+// o_tj = y_t + sum_{s<=t} B_ts delta_s.  Only t with t % ng == grp are
+// written.  Every lane of the warp must call this (TMEM load).
 template <int D, int TP>
 __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
                                               const unsigned char *smb,
                                               const Smem<D> &L, uint32_t ta,
-                                              int j, int grp, int T, int tok0,
-                                              int h) {
-  float v[4 * TP];
+                                              int j, int grp, int ng, int T,
+                                              int tok0, int h) {
+  // x_t = D[t] + D[2TP + t] and y_t = D[TP + t] + D[3TP + t], read 8
+  // columns at a time to keep few values live
+  float x[TP], y[TP];
 #pragma unroll
-  for (int cb = 0; cb < 4 * TP; cb += 16) {
-    float w16[16];
-    umma::tmem_ld16(ta + cb, w16);
+  for (int c8 = 0; c8 < TP; c8 += 8) {
+    float a[8], b[8];
+    umma::tmem_ld8(ta + c8, a);
+    umma::tmem_ld8(ta + 2 * TP + c8, b);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) v[cb + m] = w16[m];
+    for (int m = 0; m < 8; ++m) x[c8 + m] = a[m] + b[m];
+    umma::tmem_ld8(ta + TP + c8, a);
+    umma::tmem_ld8(ta + 3 * TP + c8, b);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) y[c8 + m] = a[m] + b[m];
   }
   if (j >= D) return;
   const float *vb = reinterpret_cast<const float *>(smb + L.vb);
@@ -408,7 +428,7 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
 #pragma unroll
   for (int t = 0; t < TP; ++t) {
     if (t < T) {
-      float a = v[t] + v[2 * TP + t];
+      float a = x[t];
 #pragma unroll
       for (int s = 0; s < t; ++s) a = fmaf(am[t * kTMax + s], del[s], a);
       del[t] = vb[TP * D + t] * (vb[t * D + j] - a);
@@ -416,8 +436,8 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
   }
 #pragma unroll
   for (int t = 0; t < TP; ++t) {
-    if (t < T && (grp < 0 || (t & 1) == grp)) {
-      float o = v[TP + t] + v[3 * TP + t];
+    if (t < T && t % ng == grp) {
+      float o = y[t];
 #pragma unroll
       for (int s = 0; s <= t; ++s) o = fmaf(bmat[t * kTMax + s], del[s], o);
       p.o[((size_t)(tok0 + t) * p.H + h) * D + j] = o;
@@ -425,14 +445,14 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
   }
 }
 
-template <int D, typename Tin, int TPC>
+template <int D, typename Tin, int TP>
 __global__ void __launch_bounds__(2 * D, 2)
-    verify_kernel(const VerifyParams p) {
+    verify_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap tmap) {
   constexpr int F = D / 16;
   extern __shared__ float4 smem4[];
   unsigned char *smb = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
-  __shared__ int s_info[6];  // skip, slot, accepted, T, tok0, spec
+  __shared__ int s_acc;  // accepted count to replay, -1: ring word invalid
   __shared__ uint64_t s_mbar;
   __shared__ uint32_t s_tmem;
 
@@ -444,13 +464,35 @@ __global__ void __launch_bounds__(2 * D, 2)
   const int rg = tid & 3;
   const int j0 = 2 * (tid >> 2);
 
-  // 1. the unit's state -> registers first (its address needs only the slot
-  //    id), 16-byte loads, 4 lanes cover 64 contiguous bytes of a column.
-  const int slot0 = p.state_slots[i];
-  const bool slot_ok = slot0 >= 0 && slot0 < p.P;
-  float *st = p.pool + ((size_t)(slot_ok ? slot0 : 0) * H + h) * D * D;
+  // Round trip 1 (all threads, same addresses): slot, segment, row kind.
+  const int slot = p.state_slots[i];
+  int tok0 = 0, T = 0, spec = 0, bad = 0;
+  if (slot < 0 || slot >= p.P) bad = KDA_DERR_SLOT;
+  if (p.mode == 0) {
+    const int c0 = p.cu_seqlens[i], c1 = p.cu_seqlens[i + 1];
+    spec = p.is_spec ? (p.is_spec[i] != 0) : 1;
+    if (!bad) {
+      if (c0 < 0 || c1 < c0 || c1 > p.N) {
+        bad = KDA_DERR_SEGMENT;
+      } else {
+        tok0 = c0;
+        T = c1 - c0;
+        if (T > p.max_T || (spec && T > p.depth)) bad = KDA_DERR_DEPTH;
+      }
+    }
+  }
+  if (bad) {
+    if (tid == 0) set_error(p.err, (unsigned)bad);
+    return;
+  }
+
+  // Round trip 2, all independent: the state (16-byte loads, 4 lanes per 64
+  // contiguous bytes of a column), the ring control word, every ring entry
+  // (the accepted count is not known yet), and this launch's tokens.
+  const size_t unit = (size_t)slot * H + h;
+  float *st = p.pool + unit * D * D;
   f2 S[2][2 * F];
-  if (slot_ok) {
+  {
     const ulonglong2 *c0 = reinterpret_cast<const ulonglong2 *>(st + (size_t)j0 * D);
     const ulonglong2 *c1 = c0 + D / 4;
 #pragma unroll
@@ -461,7 +503,38 @@ __global__ void __launch_bounds__(2 * D, 2)
       S[1][2 * f] = y.x; S[1][2 * f + 1] = y.y;
     }
   }
-  // later-wave units' states -> L2 now, so HBM streams while this wave computes
+  if (tid == 0) {
+    const int32_t *c = p.ctrl + unit * 2;
+    const int pend = c[0], acc = c[1];
+    const bool okc = pend >= 0 && pend <= p.depth && acc >= 0 && acc <= pend;
+    if (!okc) set_error(p.err, KDA_DERR_RING);
+    s_acc = okc ? acc : -1;
+    if (spec && T > 0) umma::mbar_init(&s_mbar, 1);
+  }
+  float *rep = reinterpret_cast<float *>(smb + L.rb);
+  float *drf = reinterpret_cast<float *>(smb + L.drf);
+  {
+    const size_t row = (size_t)tok0 * H + h;
+    const Tin *tq = reinterpret_cast<const Tin *>(p.q);
+    const Tin *tk = reinterpret_cast<const Tin *>(p.k);
+    const Tin *tv = reinterpret_cast<const Tin *>(p.v);
+    const Tin *ta = reinterpret_cast<const Tin *>(p.alpha);
+    const Tin *tbe = reinterpret_cast<const Tin *>(p.beta);
+    load_all_records<D, Tin>(
+        rep, drf, p.depth, T,
+        reinterpret_cast<const Tin *>(p.rk) + unit * p.depth * D,
+        reinterpret_cast<const Tin *>(p.ra) + unit * p.depth * D,
+        reinterpret_cast<const Tin *>(p.rv) + unit * p.depth * D,
+        reinterpret_cast<const Tin *>(p.rb) + unit * p.depth,
+        tk ? tk + row * D : nullptr, ta ? ta + row * D : nullptr,
+        tv ? tv + row * D : nullptr, tq ? tq + row * D : nullptr,
+        tbe ? tbe + row : nullptr, (size_t)H * D, (size_t)H, tid);
+  }
+  __syncthreads();
+  const int acc = s_acc;
+  if (acc < 0) return;
+  // this unit's loads have landed: stream later waves' states into L2 while
+  // this wave computes
   if (tid == 32 && p.prefetch_stride > 0) {
     const int b = i * H + h;
     if (b < p.prefetch_stride) {
@@ -475,78 +548,8 @@ __global__ void __launch_bounds__(2 * D, 2)
       }
     }
   }
-  if (tid == 0) {
-    int skip = 0, acc = 0, T = 0, tok0 = 0, spec = 0;
-    if (!slot_ok) {
-      set_error(p.err, KDA_DERR_SLOT);
-      skip = 1;
-    }
-    if (!skip && p.mode == 0) {
-      const int c0 = p.cu_seqlens[i], c1 = p.cu_seqlens[i + 1];
-      if (c0 < 0 || c1 < c0 || c1 > p.N) {
-        set_error(p.err, KDA_DERR_SEGMENT);
-        skip = 1;
-      } else {
-        tok0 = c0;
-        T = c1 - c0;
-        spec = p.is_spec ? (p.is_spec[i] != 0) : 1;
-        if (T > p.max_T || (spec && T > p.depth)) {
-          set_error(p.err, KDA_DERR_DEPTH);
-          skip = 1;
-        }
-      }
-    }
-    if (!skip) {
-      const int32_t *c = p.ctrl + ((size_t)slot0 * H + h) * 2;
-      const int pend = c[0];
-      acc = c[1];
-      if (pend < 0 || pend > p.depth || acc < 0 || acc > pend) {
-        set_error(p.err, KDA_DERR_RING);
-        skip = 1;
-      }
-    }
-    s_info[0] = skip; s_info[1] = slot0; s_info[2] = acc;
-    s_info[3] = T; s_info[4] = tok0; s_info[5] = spec;
-  }
-  __syncthreads();
-  if (s_info[0]) return;
-  const int slot = s_info[1], acc = s_info[2], T = s_info[3];
-  const int tok0 = s_info[4];
-  const bool spec = s_info[5] != 0;
 
-  // 2. ring entries to replay and this launch's tokens -> shared memory (the
-  //    token records sit in the A tile's space until the drafts need it)
-  const size_t unit = (size_t)slot * H + h;
-  float *rep = reinterpret_cast<float *>(smb + L.rep);
-  float *drf = reinterpret_cast<float *>(smb + L.a);
-  {
-    const size_t row = (size_t)tok0 * H + h;
-    const Tin *tq = reinterpret_cast<const Tin *>(p.q);
-    const Tin *tk = reinterpret_cast<const Tin *>(p.k);
-    const Tin *tv = reinterpret_cast<const Tin *>(p.v);
-    const Tin *ta = reinterpret_cast<const Tin *>(p.alpha);
-    const Tin *tbe = reinterpret_cast<const Tin *>(p.beta);
-    load_all_records<D, Tin>(
-        rep, drf, acc, T,
-        reinterpret_cast<const Tin *>(p.rk) + unit * p.depth * D,
-        reinterpret_cast<const Tin *>(p.ra) + unit * p.depth * D,
-        reinterpret_cast<const Tin *>(p.rv) + unit * p.depth * D,
-        reinterpret_cast<const Tin *>(p.rb) + unit * p.depth,
-        tk ? tk + row * D : nullptr, ta ? ta + row * D : nullptr,
-        tv ? tv + row * D : nullptr, tq ? tq + row * D : nullptr,
-        tbe ? tbe + row : nullptr, (size_t)H * D, (size_t)H, tid);
-  }
-  __syncthreads();
-  if (spec && T > 0) {
-    draft_prep<D, Tin>(smb, L, drf, T, tid,
-                       reinterpret_cast<Tin *>(p.rk) + unit * p.depth * D,
-                       reinterpret_cast<Tin *>(p.ra) + unit * p.depth * D,
-                       reinterpret_cast<Tin *>(p.rv) + unit * p.depth * D,
-                       reinterpret_cast<Tin *>(p.rb) + unit * p.depth);
-    __syncthreads();
-  }
-
-  // 3. lazy commit: replay the accepted entries
+  // Lazy commit: replay the accepted entries onto the state.
   float o0 = 0.f, o1 = 0.f;
   for (int t = 0; t < acc; ++t)
     kda_step<D, false>(S, rep + t * Rec<D>::kStride, rg, j0, o0, o1);
@@ -577,31 +580,32 @@ __global__ void __launch_bounds__(2 * D, 2)
     }
     return;
   }
-
-  if (acc > 0) store_state();
-  if (tid == 0) {
-    int32_t *c = p.ctrl + unit * 2;
-    c[0] = T;
-    c[1] = 0;
+  if (T == 0) {
+    if (acc > 0) store_state();
+    if (tid == 0) {
+      int32_t *c = p.ctrl + unit * 2;
+      c[0] = 0;
+      c[1] = 0;
+    }
+    return;
   }
-  if (T == 0) return;
 
-  // 4. drafts: X = S^T [K~ | Q~] on the tensor cores, 3xTF32:
-  //    pass 1  D  = S_hi [K~_hi Q~_hi K~_lo Q~_lo]^T   (N = 4 TP)
-  //    pass 2  D += S_lo [K~_hi Q~_hi]^T               (N = 2 TP, first columns)
-  //    x_t = D[t] + D[2TP + t],  y_t = D[TP + t] + D[3TP + t]
-  constexpr int TP = TPC, N1 = 4 * TP, N2 = 2 * TP;
+  // Drafts: X = S^T [K~ | Q~] on the tensor cores, 3xTF32:
+  //   pass 1  D  = S_hi [K~_hi Q~_hi K~_lo Q~_lo]^T   (N = 4 TP)
+  //   pass 2  D += S_lo [K~_hi Q~_hi]^T               (N = 2 TP, first columns)
+  //   x_t = D[t] + D[2TP + t],  y_t = D[TP + t] + D[3TP + t]
+  constexpr int N1 = 4 * TP, N2 = 2 * TP, NK = D / 8;
   unsigned char *sa = smb + L.a;
+  __syncthreads();  // every replay read of the records is done (B reuses them)
   if (tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)N1);
-  if (tid == 0) umma::mbar_init(&s_mbar, 1);
   write_state_tile<D>(sa, S, rg, j0, false);
+  int unsafe = prep_tiles<D, TP>(smb, L, drf, T, tid);
   umma::fence_smem_to_async();
   umma::fence_before_sync();
-  __syncthreads();
+  unsafe = __syncthreads_or(unsafe);
   umma::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  const uint32_t a_base = umma::smem_u32(sa), b_base = umma::smem_u32(smb + L.b);
-  constexpr int NK = D / 8;
+  const uint32_t a_base = umma::smem_u32(sa), b_base = umma::smem_u32(smb + L.rb);
   if (tid == 0) {
     const uint32_t id1 = umma::idesc_tf32(128, N1);
     for (int s = 0; s < NK; ++s)
@@ -610,16 +614,60 @@ __global__ void __launch_bounds__(2 * D, 2)
                      id1, s > 0 ? 1u : 0u);
     umma::commit(&s_mbar);
   }
-  bool ok = umma::mbar_wait(&s_mbar, 0, 1 << 22);
+  // the committed state leaves from the A tile (raw fp32, K-major 128B
+  // swizzled = the tensor map's box layout) through the TMA
+  constexpr bool kTmaStore = D >= 32;
+  if (kTmaStore && acc > 0 && tid == 0) {
+    const uint32_t row = (uint32_t)(unit * D);
+#pragma unroll
+    for (int kb = 0; kb < D / 32; ++kb)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+          :: "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * kb), "r"(row),
+             "r"(a_base + kb * 16384) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+  // overlapped with pass 1: pair dots, ring append, ring word
+  prep_pairs<D, TP>(smb, L, drf, T, tid, unsafe);
+  if (!kTmaStore && acc > 0) store_state();
+  {
+    constexpr int E = InVec<Tin>::kElems;
+    constexpr int CH = D / E;
+    Tin *wk = reinterpret_cast<Tin *>(p.rk) + unit * p.depth * D;
+    Tin *wa = reinterpret_cast<Tin *>(p.ra) + unit * p.depth * D;
+    Tin *wv = reinterpret_cast<Tin *>(p.rv) + unit * p.depth * D;
+    Tin *wb = reinterpret_cast<Tin *>(p.rb) + unit * p.depth;
+    for (int idx = tid; idx < T * 3 * CH; idx += 2 * D) {
+      const int t = idx / (3 * CH);
+      const int r = idx - t * 3 * CH;
+      const int which = r / CH, ch = r - (r / CH) * CH;
+      const int off = which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV;
+      Tin *dst = (which == 0 ? wk : which == 1 ? wa : wv) + (size_t)t * D + ch * E;
+      InVec<Tin>::store(dst, drf + t * Rec<D>::kStride + off + ch * E);
+    }
+    if (tid < T) out_scalar<Tin>(wb + tid, drf[tid * Rec<D>::kStride + Rec<D>::kB]);
+  }
+  if (tid == 0) {
+    int32_t *c = p.ctrl + unit * 2;
+    c[0] = T;
+    c[1] = 0;
+  }
+  // one thread waits on the tensor cores (and for the TMA to have read the
+  // tile); the others park on the barrier
+  if (kTmaStore && acc > 0 && tid == 0)
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  bool ok = tid == 0 ? umma::mbar_wait(&s_mbar, 0, 1 << 22) : true;
+  ok = __syncthreads_and(ok);
   int waiting = ok ? -1 : 0;  // phase still owed by the tensor cores
   if (ok) {
     write_state_tile<D>(sa, S, rg, j0, true);
     umma::fence_smem_to_async();
   }
   umma::fence_before_sync();
-  ok = __syncthreads_and(ok);
+  __syncthreads();
   umma::fence_after_sync();
   if (ok) {
+    bool ok2 = true;
     if (tid == 0) {
       const uint32_t id2 = umma::idesc_tf32(128, N2);
       for (int s = 0; s < NK; ++s)
@@ -627,27 +675,29 @@ __global__ void __launch_bounds__(2 * D, 2)
                        umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
                        id2, 1u);
       umma::commit(&s_mbar);
+      ok2 = umma::mbar_wait(&s_mbar, 1, 1 << 22);
     }
-    ok = umma::mbar_wait(&s_mbar, 1, 1 << 22);
+    ok = __syncthreads_and(ok2);
     if (!ok) waiting = 1;
   }
   umma::fence_after_sync();
-  ok = __syncthreads_and(ok);
   if (!ok) {
-    if (tid == 0) set_error(p.err, KDA_DERR_TIMEOUT);
-    // give the tensor cores one more bounded chance before TMEM is freed
-    if (waiting >= 0) umma::mbar_wait(&s_mbar, (uint32_t)waiting, 1 << 26);
+    if (tid == 0) {
+      set_error(p.err, KDA_DERR_TIMEOUT);
+      // give the tensor cores one more bounded chance before TMEM is freed
+      umma::mbar_wait(&s_mbar, (uint32_t)waiting, 1 << 26);
+    }
   } else {
-    // 5. one thread per value column j: triangular solve and outputs.  Warp w
-    //    reads TMEM lanes 32 (w % 4) ..; with D = 128 the upper four warps
-    //    repeat the solve and write the odd drafted positions.
-    const bool warp_on = (tid >> 5) < (D < 128 ? (D + 31) / 32 : 8);
-    if (warp_on) {
-      const int q = (tid >> 5) & 3;
+    // One thread per value column: triangular solve and outputs.  Warp w
+    // can read only TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 (value columns);
+    // the NT / 128 groups of four warps each repeat the solve and write the
+    // drafted positions t with t % groups == group.
+    const int w = tid >> 5, q = w & 3;
+    if (32 * q < D) {
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16);
-      const int j = (q << 5) + (tid & 31);
-      const int grp = D < 128 ? -1 : (tid >> 7);
-      draft_outputs<D, TPC>(p, smb, L, ta, j, grp, T, tok0, h);
+      const int ng = D >= 64 ? D / 64 : 1;  // (2 D threads) / 128
+      draft_outputs<D, TP>(p, smb, L, ta, (q << 5) + (tid & 31), w >> 2, ng, T,
+                           tok0, h);
     }
   }
   umma::fence_before_sync();
@@ -707,6 +757,45 @@ __global__ void ring_reset_kernel(const CommitParams p) {
   c[1] = 0;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Tensor map of a state pool viewed as rows of D fp32 (row = one value column
+// of one (slot, head) state), box 32 x min(D, 128), 128-byte swizzle: one box
+// is one K-block of the verify kernel's A tile.
+cudaError_t state_tensor_map(CUtensorMap *tm, float *pool, int P, int H, int D) {
+  memset(tm, 0, sizeof(*tm));
+  if (D < 32) return cudaSuccess;  // the kernel stores small states directly
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)P * H * D};
+  const cuuint64_t gstride[1] = {(cuuint64_t)D * sizeof(float)};
+  const cuuint32_t box[2] = {32, (cuuint32_t)(D < 128 ? D : 128)};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, gdim, gstride,
+                         box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, typename Tin>
 cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
   const size_t smem = verify_smem_bytes(D, p.depth, p.max_T);
@@ -725,8 +814,11 @@ cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
     p.prefetch_stride = per_sm * sms;
   else
     p.prefetch_stride = 0;
+  CUtensorMap tm;
+  cudaError_t te = state_tensor_map(&tm, p.pool, p.P, p.H, D);
+  if (te != cudaSuccess) return te;
   dim3 grid(p.H, p.B);
-  kern<<<grid, 2 * D, smem, s>>>(p);
+  kern<<<grid, 2 * D, smem, s>>>(p, tm);
   return cudaGetLastError();
 }
 
