@@ -161,6 +161,38 @@ size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
                                   int32_t chunk);
 
 /*
+ * kda_prefill_chunked_noalloc -- kda_prefill_chunked for callers that cannot
+ * allocate device memory.  (No counterpart on the pages: this is a service of
+ * this library, not part of the method.)
+ *
+ * Some hosts own every byte of device memory through their own allocator and
+ * forbid a library from calling cudaMalloc (or make it unsafe to do so while
+ * their work is in flight), and some callers simply have no allocator handle
+ * to pass a workspace from.  This entry point needs no workspace argument:
+ * its scratch is a fixed array of KDA_NOALLOC_SCRATCH_BYTES in device memory
+ * that belongs to this library, and every GPU that loads the library holds
+ * that array until the process exits.  Nothing is allocated or freed here.
+ *
+ * Arguments, outputs and semantics are those of kda_prefill_chunked; the
+ * caller still passes inputs, outputs, pool and slot tables.
+ *   - Returns KDA_ENOSPC, before any CUDA call, when
+ *     kda_prefill_workspace_size(...) for these sizes exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents
+ *     (no part of it needs to start at zero: each call writes what it reads).
+ *     Calls whose work overlaps on the GPU (different streams, or different
+ *     host threads, without ordering between them) race on it; order them.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int kda_prefill_chunked_noalloc(const kda_tokens *tok, kda_state_pool *pool,
+                                const int32_t *state_slots,
+                                const int32_t *ckpt_slots, int32_t max_ckpt,
+                                int32_t ckpt_every, int32_t chunk,
+                                const int32_t *start_pos, kda_stream_t stream);
+
+/*
  * kda_verify -- one verify launch over a mixed packed batch.
  * ("ReplaySSM shrinks rollback state"; "Small tensor copies leave the hot
  * path".)

@@ -41,7 +41,8 @@ class kda_replay_ring(ctypes.Structure):
                 ("ctrl", _P), ("depth", _I32), ("dtype", ctypes.c_int)]
 
 
-EXPORTS = ("kda_prefill_chunked", "kda_prefill_workspace_size", "kda_verify",
+EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_noalloc",
+           "kda_prefill_workspace_size", "kda_verify",
            "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
            "kda_gather_states", "kda_copy_slots", "kda_get_device_error",
            "kda_status_string", "kda_version")
@@ -61,6 +62,8 @@ def lib():
                       ctypes.POINTER(kda_replay_ring))
         L.kda_prefill_chunked.argtypes = [tp, pp, _P, _P, _I32, _I32, _I32, _P,
                                           _P, ctypes.c_size_t, _P]
+        L.kda_prefill_chunked_noalloc.argtypes = [tp, pp, _P, _P, _I32, _I32,
+                                                  _I32, _P, _P]
         L.kda_prefill_workspace_size.argtypes = [_I32] * 6
         L.kda_prefill_workspace_size.restype = ctypes.c_size_t
         L.kda_verify.argtypes = [tp, _I32, pp, _P, rp, _P, _P]
@@ -182,6 +185,20 @@ def kda_prefill_chunked(tok, pool, state_slots, chunk, ckpt_every=0,
         _ptr(workspace), workspace.numel(), _stream(stream)),
         "kda_prefill_chunked")
     return workspace
+
+
+KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def kda_prefill_chunked_noalloc(tok, pool, state_slots, chunk, ckpt_every=0,
+                                ckpt_slots=None, start_pos=None, stream=None):
+    """kda_prefill_chunked with the library's own fixed scratch instead of a
+    workspace argument, for callers that cannot allocate device memory."""
+    max_ckpt = 0 if ckpt_slots is None else int(ckpt_slots.shape[1])
+    _check(lib().kda_prefill_chunked_noalloc(
+        ctypes.byref(tok.c), ctypes.byref(pool.c), _ptr(state_slots),
+        _ptr(ckpt_slots), max_ckpt, ckpt_every, chunk, _ptr(start_pos),
+        _stream(stream)), "kda_prefill_chunked_noalloc")
 
 
 def kda_verify(tok, max_T, pool, state_slots, ring, is_spec=None, stream=None):
