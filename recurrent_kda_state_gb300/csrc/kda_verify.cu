@@ -335,6 +335,7 @@ __device__ __forceinline__ void prep_pairs(unsigned char *smb,
         const int rh = isB ? TP + t : t;
         const unsigned char *hrow = sb + (rh >> 3) * 1024 + (rh & 7) * 128;
         const int x0 = (rg ^ (rh & 7)) << 4, x1 = ((rg + 4) ^ (rh & 7)) << 4;
+        float acc2 = 0.f;
 #pragma unroll
         for (int u = 0; u < D / 16; ++u) {
           const int m = rg + 4 * u;
@@ -342,10 +343,11 @@ __device__ __forceinline__ void prep_pairs(unsigned char *smb,
               hrow + (u >> 1) * N1 * 128 + ((u & 1) ? x1 : x0));
           const float4 y = *reinterpret_cast<const float4 *>(kh + s * D + 4 * m);
           acc = fmaf(x.x, y.x, acc);
-          acc = fmaf(x.y, y.y, acc);
+          acc2 = fmaf(x.y, y.y, acc2);
           acc = fmaf(x.z, y.z, acc);
-          acc = fmaf(x.w, y.w, acc);
+          acc2 = fmaf(x.w, y.w, acc2);
         }
+        acc += acc2;
       } else {
         // decay products taken explicitly when gamma leaves the safe range
         for (int c = rg; c < D; c += 4) {
@@ -410,15 +412,17 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
   float x[TP], y[TP];
 #pragma unroll
   for (int c8 = 0; c8 < TP; c8 += 8) {
-    float a[8], b[8];
-    umma::tmem_ld8(ta + c8, a);
-    umma::tmem_ld8(ta + 2 * TP + c8, b);
+    uint32_t a[8], b[8], c[8], d[8];
+    umma::tmem_ld8_async(ta + c8, a);
+    umma::tmem_ld8_async(ta + 2 * TP + c8, b);
+    umma::tmem_ld8_async(ta + TP + c8, c);
+    umma::tmem_ld8_async(ta + 3 * TP + c8, d);
+    umma::tmem_wait_ld();
 #pragma unroll
-    for (int m = 0; m < 8; ++m) x[c8 + m] = a[m] + b[m];
-    umma::tmem_ld8(ta + TP + c8, a);
-    umma::tmem_ld8(ta + 3 * TP + c8, b);
-#pragma unroll
-    for (int m = 0; m < 8; ++m) y[c8 + m] = a[m] + b[m];
+    for (int m = 0; m < 8; ++m) {
+      x[c8 + m] = __uint_as_float(a[m]) + __uint_as_float(b[m]);
+      y[c8 + m] = __uint_as_float(c[m]) + __uint_as_float(d[m]);
+    }
   }
   if (j >= D) return;
   const float *vb = reinterpret_cast<const float *>(smb + L.vb);
@@ -485,6 +489,10 @@ __global__ void __launch_bounds__(2 * D, 2)
     if (tid == 0) set_error(p.err, (unsigned)bad);
     return;
   }
+  // speculative rows with drafts take their tensor-memory columns now, while
+  // the loads below are in flight
+  const bool drafts = spec && T > 0;
+  if (drafts && tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)(4 * TP));
 
   // Round trip 2, all independent: the state (16-byte loads, 4 lanes per 64
   // contiguous bytes of a column), the ring control word, every ring entry
@@ -530,9 +538,14 @@ __global__ void __launch_bounds__(2 * D, 2)
         tv ? tv + row * D : nullptr, tq ? tq + row * D : nullptr,
         tbe ? tbe + row : nullptr, (size_t)H * D, (size_t)H, tid);
   }
+  umma::fence_before_sync();
   __syncthreads();
+  umma::fence_after_sync();
   const int acc = s_acc;
-  if (acc < 0) return;
+  if (acc < 0) {
+    if (drafts && tid < 32) umma::tmem_dealloc(s_tmem, (uint32_t)(4 * TP));
+    return;
+  }
   // this unit's loads have landed: stream later waves' states into L2 while
   // this wave computes
   if (tid == 32 && p.prefetch_stride > 0) {
@@ -597,7 +610,6 @@ __global__ void __launch_bounds__(2 * D, 2)
   constexpr int N1 = 4 * TP, N2 = 2 * TP, NK = D / 8;
   unsigned char *sa = smb + L.a;
   __syncthreads();  // every replay read of the records is done (B reuses them)
-  if (tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)N1);
   write_state_tile<D>(sa, S, rg, j0, false);
   int unsafe = prep_tiles<D, TP>(smb, L, drf, T, tid);
   umma::fence_smem_to_async();
@@ -617,7 +629,8 @@ __global__ void __launch_bounds__(2 * D, 2)
   // the committed state leaves from the A tile (raw fp32, K-major 128B
   // swizzled = the tensor map's box layout) through the TMA
   constexpr bool kTmaStore = D >= 32;
-  if (kTmaStore && acc > 0 && tid == 0) {
+  constexpr int kTmaThread = 2 * D > 32 ? 32 : 0;  // not the MMA-issuing thread
+  if (kTmaStore && acc > 0 && tid == kTmaThread) {
     const uint32_t row = (uint32_t)(unit * D);
 #pragma unroll
     for (int kb = 0; kb < D / 32; ++kb)
@@ -637,7 +650,9 @@ __global__ void __launch_bounds__(2 * D, 2)
     Tin *wa = reinterpret_cast<Tin *>(p.ra) + unit * p.depth * D;
     Tin *wv = reinterpret_cast<Tin *>(p.rv) + unit * p.depth * D;
     Tin *wb = reinterpret_cast<Tin *>(p.rb) + unit * p.depth;
-    for (int idx = tid; idx < T * 3 * CH; idx += 2 * D) {
+    // warps 0 and 1 issue the MMA and the TMA store; the others copy
+    constexpr int base = 2 * D > 128 ? 64 : 0;
+    for (int idx = tid - base; idx >= 0 && idx < T * 3 * CH; idx += 2 * D - base) {
       const int t = idx / (3 * CH);
       const int r = idx - t * 3 * CH;
       const int which = r / CH, ch = r - (r / CH) * CH;
@@ -645,16 +660,17 @@ __global__ void __launch_bounds__(2 * D, 2)
       Tin *dst = (which == 0 ? wk : which == 1 ? wa : wv) + (size_t)t * D + ch * E;
       InVec<Tin>::store(dst, drf + t * Rec<D>::kStride + off + ch * E);
     }
-    if (tid < T) out_scalar<Tin>(wb + tid, drf[tid * Rec<D>::kStride + Rec<D>::kB]);
-  }
-  if (tid == 0) {
-    int32_t *c = p.ctrl + unit * 2;
-    c[0] = T;
-    c[1] = 0;
+    if (tid - base >= 0 && tid - base < T)
+      out_scalar<Tin>(wb + (tid - base), drf[(tid - base) * Rec<D>::kStride + Rec<D>::kB]);
+    if (tid == base) {
+      int32_t *c = p.ctrl + unit * 2;
+      c[0] = T;
+      c[1] = 0;
+    }
   }
   // one thread waits on the tensor cores (and for the TMA to have read the
   // tile); the others park on the barrier
-  if (kTmaStore && acc > 0 && tid == 0)
+  if (kTmaStore && acc > 0 && tid == kTmaThread)
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   bool ok = tid == 0 ? umma::mbar_wait(&s_mbar, 0, 1 << 22) : true;
   ok = __syncthreads_and(ok);
