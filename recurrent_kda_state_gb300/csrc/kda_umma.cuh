@@ -9,6 +9,7 @@
 // position c ^ (r % 8).  Tiles must start on a 1024-byte boundary.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace kda {
@@ -54,6 +55,53 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t da,
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
       :: "r"(d_tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+// Byte offset of element (row, k) of a K-major SW128 tile of 16-bit elements
+// with `rows` rows: K/64 blocks of rows x 128 bytes, 8 elements per 16-byte
+// chunk, same row/chunk swizzle as the fp32 tiles.
+__host__ __device__ __forceinline__ uint32_t sw128_off16(int row, int k, int rows) {
+  const int kb = k >> 6, kin = k & 63;
+  const int chunk = kin >> 3, within = kin & 7;
+  const int r8 = row & 7;
+  return (uint32_t)(kb * rows * 128 + (row >> 3) * 1024 + r8 * 128 +
+                    ((chunk ^ r8) << 4) + within * 2);
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator,
+// A and B K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) (+)= A * B^T for one K = 16 step; A is M x 16, B is N x 16 (bf16).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t da,
+                                         uint64_t db, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+// Two fp32 values as bf16 pairs hi + lo with hi = rn(x), lo = rn(x - hi):
+// hi + lo carries 16 significant bits, and the three products hi*hi,
+// hi*lo, lo*hi of two such splits reproduce an fp32 product to ~2^-16.
+// The first value goes to the low half of each word (lower address).
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t &hi,
+                                             uint32_t &lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(l);
 }
 
 // Arrive on `mbar` once every tcgen05 op issued so far by this thread is done.

@@ -298,10 +298,13 @@ def test_slot_permutation_invariance():
 
 # ------------------------------------------------------------ prefill
 def _run_prefill(lengths, starts, H, d, C, ckpt_every, dtype, max_ckpt, hs,
-                 seed, s0_std=0.0, skip_ckpt=()):
+                 seed, s0_std=0.0, skip_ckpt=(), alpha=None):
     rng = np.random.default_rng(seed)
     B = len(lengths)
-    tok = ki.round_to(ki.gen_tokens(rng, lengths, H, d), dtype)
+    tok = ki.gen_tokens(rng, lengths, H, d)
+    if alpha is not None:  # another decay distribution, same shape
+        tok["alpha"] = alpha(rng, tok["alpha"].shape).astype(np.float32)
+    tok = ki.round_to(tok, dtype)
     P = B * (1 + max_ckpt) + 1
     init = ki.initial_states(rng, P, H, d, d, s0_std)
     pool = K.StatePool(to_gpu_states(init).cuda())
@@ -334,12 +337,21 @@ def test_prefill_full_workload_sampled_heads():
     assert nck[0] == 8
 
 
-@pytest.mark.parametrize("C", [16, 32, 64])
-def test_prefill_ragged_and_offsets(C):
+@pytest.mark.parametrize("C,d", [(16, 64), (32, 64), (64, 64), (64, 128)])
+def test_prefill_ragged_and_offsets(C, d):
     lengths = [0, 1, C - 1, C, C + 1, 3 * C + 5, 100]
     starts = [0, 5, 0, 2 * C, C - 3, 7, 0]
-    _run_prefill(lengths, starts, 4, 64, C, 2 * C, "bf16", 3, [0, 1, 2, 3],
-                 seed=900 + C, s0_std=0.1, skip_ckpt=[(5, 1)])
+    _run_prefill(lengths, starts, 4, d, C, 2 * C, "bf16", 3, [0, 1, 2, 3],
+                 seed=900 + C + d, s0_std=0.1, skip_ckpt=[(5, 1)])
+
+
+def test_prefill_slow_decay_carries_state():
+    """alpha in [0.97, 1): the state carried across chunks dominates the
+    outputs (with the default alpha ~ 0.5 it fades within a chunk), so the
+    inter-chunk pass and the checkpoints are tested at full weight."""
+    _run_prefill([1000, 333, 64], [0, 17, 64], 3, 128, 64, 128, "bf16", 8,
+                 [0, 1, 2], seed=912, s0_std=0.5,
+                 alpha=lambda rng, shp: 1.0 - 0.03 * rng.random(shp))
 
 
 def test_prefill_tiny_dims_fp32():
@@ -503,6 +515,15 @@ def test_prefill_decay_range_flag():
     tok["alpha"][:] = 1e-3   # log-decay ~ -6.9 per token: -220 per half chunk
     pool = K.StatePool.zeros(1, 1, 16)
     K.kda_prefill_chunked(device_batch(tok, "f32"), pool, i32([0]), chunk=64)
+    assert K.kda_get_device_error() & K.KDA_DERR_RANGE
+
+
+def test_prefill_decay_range_flag_tensor_core_shape():
+    rng = np.random.default_rng(75)
+    tok = ki.round_to(ki.gen_tokens(rng, [64], 1, 128), "bf16")
+    tok["alpha"][:] = 1e-3
+    pool = K.StatePool.zeros(1, 1, 128)
+    K.kda_prefill_chunked(device_batch(tok, "bf16"), pool, i32([0]), chunk=64)
     assert K.kda_get_device_error() & K.KDA_DERR_RANGE
 
 
