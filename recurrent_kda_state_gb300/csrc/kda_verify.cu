@@ -24,10 +24,6 @@
 //   delta_t = beta_t (v_tj - (S^T kt_t)_j - sum_{s<t} A_ts delta_s)
 //   o_tj    = (S^T qt_t)_j + sum_{s<=t} B_ts delta_s
 // which is the recurrence unrolled over the drafted tokens.
-#include <cuda.h>
-
-#include <mutex>
-
 #include "kda_internal.cuh"
 #include "kda_umma.cuh"
 
@@ -215,22 +211,24 @@ __device__ __forceinline__ void load_all_records(
 // Shared-memory carve-up (bytes from a 1024-byte aligned base) for ring depth
 // `depth` and at most `maxT` tokens per row; TP = padded draft count (8 or
 // 16).
-//   a    tcgen05 A tile: the committed state, K-major 128B-swizzled (128 rows
-//        = value columns j, K = key rows c);
-//   rb   the replay records, later (once replayed) the B tile
-//        [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows, K-major 128B-swizzled);
+//   a    tcgen05 A tiles: the committed state as bf16 hi, then lo, K-major
+//        128B-swizzled (128 rows = value columns j, K = key rows c);
+//   rb   the replay records, later (once replayed) the bf16 B tile
+//        [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows, K-major 128B-swizzled)
+//        followed (kx) by K~ and Q~ in fp32, row-major [2 TP][D];
 //   drf  this launch's token records;  kh = k / gamma;  vb = v and beta of the
 //        drafted tokens;  am, bm = the T x T matrices of the triangular solve.
 template <int D>
 struct Smem {
-  int tp, a, rb, drf, kh, vb, am, bm, total;
+  int tp, a, rb, kx, drf, kh, vb, am, bm, total;
   __host__ __device__ Smem(int depth, int maxT) {
     tp = maxT <= 8 ? 8 : 16;
-    const int kblk = (D + 31) / 32;
+    const int kblk = (D + 63) / 64;  // bf16 K blocks
     const int rep_bytes = depth * Rec<D>::kStride * 4;
-    const int b_bytes = kblk * 4 * tp * 128;
+    const int b_bytes = kblk * 4 * tp * 128 + 2 * tp * D * 4;
     a = 0;
-    rb = kblk * 128 * 128;
+    rb = 2 * kblk * 128 * 128;
+    kx = rb + kblk * 4 * tp * 128;
     drf = rb + (((rep_bytes > b_bytes ? rep_bytes : b_bytes) + 1023) & ~1023);
     kh = drf + maxT * Rec<D>::kStride * 4;
     vb = kh + tp * D * 4;
@@ -242,9 +240,9 @@ struct Smem {
 
 // Chunk-form quantities of the drafts that do not depend on S, part 1: one
 // thread per (4 key channels, drafted row t): gamma_t = prod_{r<=t} alpha_r,
-// the B tile rows t, TP+t (gamma k, gamma q as fp32: the tensor cores read
-// their tf32 part) and 2TP+t, 3TP+t (the remainders past tf32), zero rows
-// past T, kh = k / gamma, and v, beta.  Returns whether
+// the bf16 B tile rows t, TP+t (gamma k, gamma q rounded to bf16) and 2TP+t,
+// 3TP+t (the remainders, rounded to bf16), zero rows past T, the fp32 values
+// (kx), kh = k / gamma, and v, beta.  Returns whether
 // gamma left [2^-60, 2^60] anywhere (then A and B use explicit products).
 template <int D, int TP>
 __device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
@@ -252,6 +250,7 @@ __device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
   constexpr int NT = 2 * D, N1 = 4 * TP;
   float *kh = reinterpret_cast<float *>(smb + L.kh);
   float *vb = reinterpret_cast<float *>(smb + L.vb);
+  float *kx = reinterpret_cast<float *>(smb + L.kx);
   unsigned char *sb = smb + L.rb;
   int unsafe = 0;
   for (int item = tid; item < (D / 4) * TP; item += NT) {
@@ -282,18 +281,19 @@ __device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
           *reinterpret_cast<const float4 *>(rr + Rec<D>::kV + 4 * c4);
       if (c4 == 0) vb[TP * D + t] = rr[Rec<D>::kB];
     }
-    // the tensor cores read fp32 operands as tf32 by dropping the low 13
-    // mantissa bits, so the hi rows take the values as they are
-    const float4 kh4 = make_float4(umma::tf32_hi(kt.x), umma::tf32_hi(kt.y),
-                                   umma::tf32_hi(kt.z), umma::tf32_hi(kt.w));
-    const float4 qh4 = make_float4(umma::tf32_hi(qt.x), umma::tf32_hi(qt.y),
-                                   umma::tf32_hi(qt.z), umma::tf32_hi(qt.w));
-    *reinterpret_cast<float4 *>(sb + umma::sw128_off(t, 4 * c4, N1)) = kt;
-    *reinterpret_cast<float4 *>(sb + umma::sw128_off(TP + t, 4 * c4, N1)) = qt;
-    *reinterpret_cast<float4 *>(sb + umma::sw128_off(2 * TP + t, 4 * c4, N1)) =
-        make_float4(kt.x - kh4.x, kt.y - kh4.y, kt.z - kh4.z, kt.w - kh4.w);
-    *reinterpret_cast<float4 *>(sb + umma::sw128_off(3 * TP + t, 4 * c4, N1)) =
-        make_float4(qt.x - qh4.x, qt.y - qh4.y, qt.z - qh4.z, qt.w - qh4.w);
+    *reinterpret_cast<float4 *>(kx + t * D + 4 * c4) = kt;
+    *reinterpret_cast<float4 *>(kx + (TP + t) * D + 4 * c4) = qt;
+    uint32_t h0, l0, h1, l1;
+    umma::split_bf16x2(kt.x, kt.y, h0, l0);
+    umma::split_bf16x2(kt.z, kt.w, h1, l1);
+    *reinterpret_cast<uint2 *>(sb + umma::sw128_off16(t, 4 * c4, N1)) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2 *>(sb + umma::sw128_off16(2 * TP + t, 4 * c4, N1)) =
+        make_uint2(l0, l1);
+    umma::split_bf16x2(qt.x, qt.y, h0, l0);
+    umma::split_bf16x2(qt.z, qt.w, h1, l1);
+    *reinterpret_cast<uint2 *>(sb + umma::sw128_off16(TP + t, 4 * c4, N1)) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2 *>(sb + umma::sw128_off16(3 * TP + t, 4 * c4, N1)) =
+        make_uint2(l0, l1);
   }
   return unsafe;
 }
@@ -304,11 +304,11 @@ template <int D, int TP>
 __device__ __forceinline__ void prep_pairs(unsigned char *smb,
                                            const Smem<D> &L, const float *drf,
                                            int T, int tid, int unsafe) {
-  constexpr int NT = 2 * D, N1 = 4 * TP;
+  constexpr int NT = 2 * D;
   const float *kh = reinterpret_cast<const float *>(smb + L.kh);
+  const float *kx = reinterpret_cast<const float *>(smb + L.kx);
   float *am = reinterpret_cast<float *>(smb + L.am);
   float *bmat = reinterpret_cast<float *>(smb + L.bm);
-  const unsigned char *sb = smb + L.rb;
   const int nb = T * (T + 1) / 2, npairs = T * T;
   const int rg = tid & 3;
   for (int base = 0; base < npairs * 4; base += NT) {
@@ -329,18 +329,13 @@ __device__ __forceinline__ void prep_pairs(unsigned char *smb,
         s = r;
       }
       if (!unsafe) {
-        // rows t (gamma k) and TP + t (gamma q) of the B tile hold the exact
-        // fp32 values; chunk m = rg + 4 u sits in 32-wide block u / 2 at
-        // position rg + 4 (u % 2)
-        const int rh = isB ? TP + t : t;
-        const unsigned char *hrow = sb + (rh >> 3) * 1024 + (rh & 7) * 128;
-        const int x0 = (rg ^ (rh & 7)) << 4, x1 = ((rg + 4) ^ (rh & 7)) << 4;
+        // gamma k (row t) or gamma q (row TP + t) in fp32
+        const float *xr = kx + (isB ? TP + t : t) * D;
         float acc2 = 0.f;
 #pragma unroll
         for (int u = 0; u < D / 16; ++u) {
           const int m = rg + 4 * u;
-          const float4 x = *reinterpret_cast<const float4 *>(
-              hrow + (u >> 1) * N1 * 128 + ((u & 1) ? x1 : x0));
+          const float4 x = *reinterpret_cast<const float4 *>(xr + 4 * m);
           const float4 y = *reinterpret_cast<const float4 *>(kh + s * D + 4 * m);
           acc = fmaf(x.x, y.x, acc);
           acc2 = fmaf(x.y, y.y, acc2);
@@ -367,31 +362,28 @@ __device__ __forceinline__ void prep_pairs(unsigned char *smb,
   }
 }
 
-// Thread's state slice -> A tile (row j, K = c): the values as they are (the
-// tensor cores use their tf32 part), or the remainder S - tf32(S).
+// Thread's state slice -> A tiles (row j, K = c): hi = rn_bf16(S) at sa and
+// lo = rn_bf16(S - hi) one tile further (hi + lo carries 16 significant bits).
 template <int D>
-__device__ __forceinline__ void write_state_tile(unsigned char *sa,
-                                                 const f2 (&S)[2][D / 8], int rg,
-                                                 int j0, bool lo_part) {
+__device__ __forceinline__ void write_state_tiles(unsigned char *sa,
+                                                  const f2 (&S)[2][D / 8], int rg,
+                                                  int j0) {
   constexpr int F = D / 16;
+  constexpr uint32_t kLo = ((D + 63) / 64) * 16384;
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    // row j = j0 + e; key chunk (rg + 4 f) lies in 32-wide block f / 2 at
-    // chunk position rg + 4 (f % 2), swizzled by j % 8
     const int j = j0 + e;
-    unsigned char *row = sa + (j >> 3) * 1024 + (j & 7) * 128;
-    const int x0 = (rg ^ (j & 7)) << 4, x1 = ((rg + 4) ^ (j & 7)) << 4;
 #pragma unroll
     for (int f = 0; f < F; ++f) {
       float x[4];
       asm("mov.b64 {%0, %1}, %2;" : "=f"(x[0]), "=f"(x[1]) : "l"(S[e][2 * f]));
       asm("mov.b64 {%0, %1}, %2;" : "=f"(x[2]), "=f"(x[3]) : "l"(S[e][2 * f + 1]));
-      if (lo_part) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) x[m] = x[m] - umma::tf32_hi(x[m]);
-      }
-      *reinterpret_cast<float4 *>(row + (f >> 1) * 16384 + ((f & 1) ? x1 : x0)) =
-          make_float4(x[0], x[1], x[2], x[3]);
+      uint32_t h0, l0, h1, l1;
+      umma::split_bf16x2(x[0], x[1], h0, l0);
+      umma::split_bf16x2(x[2], x[3], h1, l1);
+      const uint32_t off = umma::sw128_off16(j, 4 * (rg + 4 * f), 128);
+      *reinterpret_cast<uint2 *>(sa + off) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2 *>(sa + kLo + off) = make_uint2(l0, l1);
     }
   }
 }
@@ -412,17 +404,17 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
   float x[TP], y[TP];
 #pragma unroll
   for (int c8 = 0; c8 < TP; c8 += 8) {
-    uint32_t a[8], b[8], c[8], d[8];
+    uint32_t a[8], b[8];
     umma::tmem_ld8_async(ta + c8, a);
     umma::tmem_ld8_async(ta + 2 * TP + c8, b);
-    umma::tmem_ld8_async(ta + TP + c8, c);
-    umma::tmem_ld8_async(ta + 3 * TP + c8, d);
     umma::tmem_wait_ld();
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      x[c8 + m] = __uint_as_float(a[m]) + __uint_as_float(b[m]);
-      y[c8 + m] = __uint_as_float(c[m]) + __uint_as_float(d[m]);
-    }
+    for (int m = 0; m < 8; ++m) x[c8 + m] = __uint_as_float(a[m]) + __uint_as_float(b[m]);
+    umma::tmem_ld8_async(ta + TP + c8, a);
+    umma::tmem_ld8_async(ta + 3 * TP + c8, b);
+    umma::tmem_wait_ld();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) y[c8 + m] = __uint_as_float(a[m]) + __uint_as_float(b[m]);
   }
   if (j >= D) return;
   const float *vb = reinterpret_cast<const float *>(smb + L.vb);
@@ -451,7 +443,7 @@ __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
 
 template <int D, typename Tin, int TP>
 __global__ void __launch_bounds__(2 * D, 2)
-    verify_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap tmap) {
+    verify_kernel(const VerifyParams p) {
   constexpr int F = D / 16;
   extern __shared__ float4 smem4[];
   unsigned char *smb = reinterpret_cast<unsigned char *>(
@@ -603,14 +595,17 @@ __global__ void __launch_bounds__(2 * D, 2)
     return;
   }
 
-  // Drafts: X = S^T [K~ | Q~] on the tensor cores, 3xTF32:
-  //   pass 1  D  = S_hi [K~_hi Q~_hi K~_lo Q~_lo]^T   (N = 4 TP)
-  //   pass 2  D += S_lo [K~_hi Q~_hi]^T               (N = 2 TP, first columns)
+  // Drafts: X = S^T [K~ | Q~] on the tensor cores, bf16 splits, one round
+  // of MMAs into one accumulator:
+  //   D  = S_hi [K~_hi Q~_hi K~_lo Q~_lo]^T   (N = 4 TP)
+  //   D += S_lo [K~_hi Q~_hi]^T               (N = 2 TP, first columns)
   //   x_t = D[t] + D[2TP + t],  y_t = D[TP + t] + D[3TP + t]
-  constexpr int N1 = 4 * TP, N2 = 2 * TP, NK = D / 8;
+  // i.e. hi*hi + lo*hi + hi*lo of every product.
+  constexpr int N1 = 4 * TP, N2 = 2 * TP, NK = D / 16;  // K steps of 16
+  constexpr uint32_t kLoA = ((D + 63) / 64) * 16384;     // S_lo tile offset
   unsigned char *sa = smb + L.a;
   __syncthreads();  // every replay read of the records is done (B reuses them)
-  write_state_tile<D>(sa, S, rg, j0, false);
+  write_state_tiles<D>(sa, S, rg, j0);
   int unsafe = prep_tiles<D, TP>(smb, L, drf, T, tid);
   umma::fence_smem_to_async();
   umma::fence_before_sync();
@@ -619,30 +614,21 @@ __global__ void __launch_bounds__(2 * D, 2)
   const uint32_t tmem = s_tmem;
   const uint32_t a_base = umma::smem_u32(sa), b_base = umma::smem_u32(smb + L.rb);
   if (tid == 0) {
-    const uint32_t id1 = umma::idesc_tf32(128, N1);
+    const uint32_t id1 = umma::idesc_bf16(128, N1), id2 = umma::idesc_bf16(128, N2);
     for (int s = 0; s < NK; ++s)
-      umma::mma_tf32(tmem, umma::sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32),
+      umma::mma_bf16(tmem, umma::sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32),
                      umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
                      id1, s > 0 ? 1u : 0u);
+    for (int s = 0; s < NK; ++s)
+      umma::mma_bf16(tmem, umma::sdesc_sw128(a_base + kLoA + (s >> 2) * 16384 + (s & 3) * 32),
+                     umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
+                     id2, 1u);
     umma::commit(&s_mbar);
   }
-  // the committed state leaves from the A tile (raw fp32, K-major 128B
-  // swizzled = the tensor map's box layout) through the TMA
-  constexpr bool kTmaStore = D >= 32;
-  constexpr int kTmaThread = 2 * D > 32 ? 32 : 0;  // not the MMA-issuing thread
-  if (kTmaStore && acc > 0 && tid == kTmaThread) {
-    const uint32_t row = (uint32_t)(unit * D);
-#pragma unroll
-    for (int kb = 0; kb < D / 32; ++kb)
-      asm volatile(
-          "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-          :: "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(32 * kb), "r"(row),
-             "r"(a_base + kb * 16384) : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  }
-  // overlapped with pass 1: pair dots, ring append, ring word
+  // overlapped with the MMAs: the committed state, pair dots, ring append,
+  // ring word
+  if (acc > 0) store_state();
   prep_pairs<D, TP>(smb, L, drf, T, tid, unsafe);
-  if (!kTmaStore && acc > 0) store_state();
   {
     constexpr int E = InVec<Tin>::kElems;
     constexpr int CH = D / E;
@@ -650,8 +636,8 @@ __global__ void __launch_bounds__(2 * D, 2)
     Tin *wa = reinterpret_cast<Tin *>(p.ra) + unit * p.depth * D;
     Tin *wv = reinterpret_cast<Tin *>(p.rv) + unit * p.depth * D;
     Tin *wb = reinterpret_cast<Tin *>(p.rb) + unit * p.depth;
-    // warps 0 and 1 issue the MMA and the TMA store; the others copy
-    constexpr int base = 2 * D > 128 ? 64 : 0;
+    // warp 0 issues the MMAs; the others copy
+    constexpr int base = 2 * D > 64 ? 32 : 0;
     for (int idx = tid - base; idx >= 0 && idx < T * 3 * CH; idx += 2 * D - base) {
       const int t = idx / (3 * CH);
       const int r = idx - t * 3 * CH;
@@ -668,34 +654,10 @@ __global__ void __launch_bounds__(2 * D, 2)
       c[1] = 0;
     }
   }
-  // one thread waits on the tensor cores (and for the TMA to have read the
-  // tile); the others park on the barrier
-  if (kTmaStore && acc > 0 && tid == kTmaThread)
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  // one thread waits on the tensor cores; the others park on the barrier
   bool ok = tid == 0 ? umma::mbar_wait(&s_mbar, 0, 1 << 22) : true;
   ok = __syncthreads_and(ok);
-  int waiting = ok ? -1 : 0;  // phase still owed by the tensor cores
-  if (ok) {
-    write_state_tile<D>(sa, S, rg, j0, true);
-    umma::fence_smem_to_async();
-  }
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  if (ok) {
-    bool ok2 = true;
-    if (tid == 0) {
-      const uint32_t id2 = umma::idesc_tf32(128, N2);
-      for (int s = 0; s < NK; ++s)
-        umma::mma_tf32(tmem, umma::sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32),
-                       umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
-                       id2, 1u);
-      umma::commit(&s_mbar);
-      ok2 = umma::mbar_wait(&s_mbar, 1, 1 << 22);
-    }
-    ok = __syncthreads_and(ok2);
-    if (!ok) waiting = 1;
-  }
+  const int waiting = 0;  // the phase still owed by the tensor cores
   umma::fence_after_sync();
   if (!ok) {
     if (tid == 0) {
@@ -773,43 +735,34 @@ __global__ void ring_reset_kernel(const CommitParams p) {
   c[1] = 0;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
-                                  void *, const cuuint64_t *, const cuuint64_t *,
-                                  const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// Tensor map of a state pool viewed as rows of D fp32 (row = one value column
-// of one (slot, head) state), box 32 x min(D, 128), 128-byte swizzle: one box
-// is one K-block of the verify kernel's A tile.
-cudaError_t state_tensor_map(CUtensorMap *tm, float *pool, int P, int H, int D) {
-  memset(tm, 0, sizeof(*tm));
-  if (D < 32) return cudaSuccess;  // the kernel stores small states directly
-  EncodeTiledFn enc = encode_tiled();
-  if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)P * H * D};
-  const cuuint64_t gstride[1] = {(cuuint64_t)D * sizeof(float)};
-  const cuuint32_t box[2] = {32, (cuuint32_t)(D < 128 ? D : 128)};
-  const cuuint32_t estride[2] = {1, 1};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, gdim, gstride,
-                         box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+// CTAs of `kern` that fit on one SM at once: the shared-memory, register
+// and thread limits of the device against the kernel's needs (taken as the
+// larger of this and the runtime's occupancy answer, which can assume a
+// smaller shared-memory carveout than the launch gets).  0 if unknown.
+int resident_ctas(const void *kern, int threads, size_t dyn_smem) {
+  int dev = 0, smem_sm = 0, regs_sm = 0, thr_sm = 0, reserved = 0, api = 0;
+  cudaFuncAttributes fa;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaFuncGetAttributes(&fa, kern) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+          cudaSuccess)
+    return 0;
+  const size_t per_block = dyn_smem + fa.sharedSizeBytes + (size_t)reserved;
+  const int warps = (threads + 31) / 32;
+  const int regs_block = warps * (((fa.numRegs * 32) + 255) / 256) * 256;
+  int n = thr_sm / threads;
+  if (per_block > 0 && (int)((size_t)smem_sm / per_block) < n) n = (int)(smem_sm / per_block);
+  if (regs_block > 0 && regs_sm / regs_block < n) n = regs_sm / regs_block;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&api, kern, threads, dyn_smem) ==
+          cudaSuccess &&
+      api > n)
+    n = api;
+  return n;
 }
 
 template <int D, typename Tin>
@@ -821,20 +774,20 @@ cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  // all of the unified L1 as shared memory: two CTAs per SM at d = 128
+  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        (int)cudaSharedmemCarveoutMaxShared);
+  if (ce != cudaSuccess) return ce;
   // CTAs resident in the first wave: they prefetch the later waves' states.
-  int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 2 * D, smem) ==
-          cudaSuccess)
+  const int per_sm = resident_ctas(reinterpret_cast<const void *>(kern), 2 * D, smem);
+  int dev = 0, sms = 0;
+  if (per_sm > 0 && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
     p.prefetch_stride = per_sm * sms;
   else
     p.prefetch_stride = 0;
-  CUtensorMap tm;
-  cudaError_t te = state_tensor_map(&tm, p.pool, p.P, p.H, D);
-  if (te != cudaSuccess) return te;
   dim3 grid(p.H, p.B);
-  kern<<<grid, 2 * D, smem, s>>>(p, tm);
+  kern<<<grid, 2 * D, smem, s>>>(p);
   return cudaGetLastError();
 }
 
