@@ -160,7 +160,8 @@ cudaError_t launch_ring_reset(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_slot_copy(const SlotCopyParams &p, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,
                            cudaStream_t s);
-// Tensor-core prefill (d_k = d_v = 128, chunk 64, bf16 inputs; no workspace).
+// Tensor-core prefill (d_k = d_v = 128, chunk 64, bf16 inputs, heads a
+// multiple of 8; no workspace).
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 
 }  // namespace kda

@@ -1,5 +1,5 @@
 // Chunked prefill on the tensor cores (tcgen05, accumulators in TMEM) for
-// d_k = d_v = 128, chunk 64, bf16 inputs, with the in-pass checkpoints of
+// d_k = d_v = 128, chunk 64, bf16 inputs, heads a multiple of 8, with the in-pass checkpoints of
 // "KDA checkpoints stay inside the prefill" (vLLM Kimi K3 optimisation page).
 //
 // One CTA per (value-column slice of NC columns, head, sequence) walks the
@@ -27,6 +27,10 @@
 //
 // Shared-memory operand tiles are K-major with the 128-byte swizzle (see
 // kda_umma.cuh); the TMEM accumulators sit at fixed columns.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_umma.cuh"
 
@@ -43,11 +47,11 @@ struct Lay {
   static constexpr uint32_t GA_LO = 32768;
   static constexpr uint32_t GB_HI = 65536;   // K^: 64 x 128
   static constexpr uint32_t GB_LO = 81920;
-  static constexpr uint32_t AF = 65536;      // after R1: A fp32 64 x 64
-  static constexpr uint32_t XF = 81920;      //           X fp32 64 x 64
+  static constexpr uint32_t AF = 65536;      // after R1: A fp32 64 x 68
+  static constexpr uint32_t XF = 82944;      //           X fp32 64 x 68
   static constexpr uint32_t UT_HI = 65536;   // after the solve: U^T NC x 64
   static constexpr uint32_t UT_LO = UT_HI + kNC * 128;
-  static constexpr uint32_t B2_HI = 98304;   // [K~^T; V^T]: (128 + NC) x 64
+  static constexpr uint32_t B2_HI = 101376;  // [K~^T; V^T]: (128 + NC) x 64
   static constexpr uint32_t B2_LO = B2_HI + (128 + kNC) * 128;  // K~^T lo
   static constexpr uint32_t KH_HI = B2_LO + 16384;  // K^^T: 128 x 64
   static constexpr uint32_t KH_LO = KH_HI + 16384;
@@ -64,8 +68,10 @@ struct Lay {
   static constexpr uint32_t ECM = EGC + 512;         // e^{g_C - g_m} [128]
   static constexpr uint32_t PT = ECM + 512;          // solve blocks 3 x 256
   static constexpr uint32_t TOT4 = PT + 3072;        // quarter sums [4][128]
-  static constexpr uint32_t MBAR = TOT4 + 2048;      // u64
-  static constexpr uint32_t TSLOT = MBAR + 8;        // u32
+  static constexpr uint32_t BST = TOT4 + 2048;       // staged beta bf16 [64][8]
+  static constexpr uint32_t MBAR = BST + 1024;       // u64: tensor cores
+  static constexpr uint32_t SBAR = MBAR + 8;         // u64: staging copies
+  static constexpr uint32_t TSLOT = SBAR + 8;        // u32
   static constexpr uint32_t END = TSLOT + 8;
   static constexpr size_t kBytes = END + 1024;       // + alignment slack
 };
@@ -73,6 +79,8 @@ static_assert(Lay::B2_LO % 1024 == 0 && Lay::KH_HI % 1024 == 0 &&
                   Lay::SB_HI % 1024 == 0 && Lay::UT_LO % 1024 == 0,
               "tiles on 1024-byte boundaries");
 static_assert(Lay::UT_LO + kNC * 128 <= Lay::B2_HI, "U^T fits the K^ region");
+static_assert(Lay::XF + 64 * 68 * 4 <= Lay::B2_HI && Lay::XF >= Lay::AF + 64 * 68 * 4,
+              "A and X fit before the R2 B tile");
 // The next chunk's raw rows are staged while this chunk's R3/R4 run, in
 // regions free from the end of R2 to the next E1: q, k (bf16 [64][128]) in
 // the R2 B tile, alpha in the X array, the V slice after U^T.
@@ -87,11 +95,10 @@ constexpr uint32_t kAccG = 0, kAcc2 = 64, kAcc3 = 64 + 128 + kNC,
                    kAcc4 = kAcc3 + kNC;
 static_assert(kAcc4 + kNC <= 512, "TMEM columns");
 
-// Swizzled index of element (r, c) of a 64 x 64 fp32 array (16-byte chunks
-// permuted by row so that row-parallel float4 accesses avoid bank conflicts).
-__device__ __forceinline__ int fo(int r, int c) {
-  return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
-}
+// Index of element (r, c) of a 64 x 64 fp32 array with rows 68 floats apart:
+// rows stay 16-byte aligned and a column's 8 consecutive rows fall in
+// distinct banks.
+__device__ __forceinline__ int fo(int r, int c) { return r * 68 + c; }
 
 __device__ __forceinline__ void st_u16(uint8_t *base, uint32_t off, uint16_t v) {
   *reinterpret_cast<uint16_t *>(base + off) = v;
@@ -118,70 +125,64 @@ __device__ __forceinline__ float4 ld4(const float *M, int r, int c) {
 }
 
 // One block distance d of the off-diagonal pass: for the 4 - d blocks
-// (a, b) = (blk + d, blk), P_ab = sum_{b<=r<a} A_ar X_rb (16 x 16 each, one
-// element per thread and loop trip; operands loaded before the FMAs).
+// (a, b) = (blk + d, blk), P_ab = sum_{b<=r<a} A_ar X_rb (16 x 16 each).
+// Thread -> row i and four columns j0..j0+3 of one block (threads past the
+// 64 (4 - d) strips idle); X rows and A rows are read as float4.
 template <int d>
 __device__ __forceinline__ void offdiag_sum(const float *A, const float *X,
                                             float *P, int tid) {
+  if (tid < 64 * (4 - d)) {
+    const int blk = tid >> 6, i = (tid >> 2) & 15, j0 = (tid & 3) * 4;
+    const int a = blk + d, b = blk;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int it = 0; it < (4 - d) * 256 / kThreads; ++it) {
-    const int e = tid + it * kThreads;
-    if (e < (4 - d) * 256) {
-      const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const int a = blk + d, b = blk;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int rr = 0; rr < d; ++rr) {
-        const int rb = b + rr;
-        float4 av[4];
-        float xv[16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) av[k] = ld4(A, 16 * a + i, 16 * rb + 4 * k);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) xv[r] = X[fo(16 * rb + r, 16 * b + j)];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[0] = fmaf(av[k].x, xv[4 * k], acc[0]);
-          acc[1] = fmaf(av[k].y, xv[4 * k + 1], acc[1]);
-          acc[2] = fmaf(av[k].z, xv[4 * k + 2], acc[2]);
-          acc[3] = fmaf(av[k].w, xv[4 * k + 3], acc[3]);
-        }
-      }
-      P[blk * 256 + i * 16 + j] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-    }
-  }
-}
-
-// X_ab = -X_aa P_ab for the blocks of distance d.
-template <int d>
-__device__ __forceinline__ void offdiag_apply(const float *P, float *X, int tid) {
-#pragma unroll
-  for (int it = 0; it < (4 - d) * 256 / kThreads; ++it) {
-    const int e = tid + it * kThreads;
-    if (e < (4 - d) * 256) {
-      const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const int a = blk + d, b = blk;
-      float4 xv[4];
-      float pv[16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) xv[k] = ld4(X, 16 * a + i, 16 * a + 4 * k);
-#pragma unroll
-      for (int r = 0; r < 16; ++r) pv[r] = P[blk * 256 + r * 16 + j];
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int rr = 0; rr < d; ++rr) {
+      const int rb = b + rr;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        acc[0] = fmaf(xv[k].x, pv[4 * k], acc[0]);
-        acc[1] = fmaf(xv[k].y, pv[4 * k + 1], acc[1]);
-        acc[2] = fmaf(xv[k].z, pv[4 * k + 2], acc[2]);
-        acc[3] = fmaf(xv[k].w, pv[4 * k + 3], acc[3]);
+        const float4 av = ld4(A, 16 * a + i, 16 * rb + 4 * k);
+        const float aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 x = ld4(X, 16 * rb + 4 * k + m, 16 * b + j0);
+          acc.x = fmaf(aw[m], x.x, acc.x);
+          acc.y = fmaf(aw[m], x.y, acc.y);
+          acc.z = fmaf(aw[m], x.z, acc.z);
+          acc.w = fmaf(aw[m], x.w, acc.w);
+        }
       }
-      X[fo(16 * a + i, 16 * b + j)] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
     }
+    *reinterpret_cast<float4 *>(P + blk * 256 + i * 16 + j0) = acc;
   }
 }
 
-// X = (I + A)^{-1} for a strictly lower-triangular 64 x 64 A (swizzled fp32
-// arrays), by 16 x 16 blocks: diagonal blocks by forward substitution (one
+// X_ab = -X_aa P_ab for the blocks of distance d (same thread mapping).
+template <int d>
+__device__ __forceinline__ void offdiag_apply(const float *P, float *X, int tid) {
+  if (tid < 64 * (4 - d)) {
+    const int blk = tid >> 6, i = (tid >> 2) & 15, j0 = (tid & 3) * 4;
+    const int a = blk + d, b = blk;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 xv = ld4(X, 16 * a + i, 16 * a + 4 * k);
+      const float xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 pv = *reinterpret_cast<const float4 *>(P + blk * 256 + (4 * k + m) * 16 + j0);
+        acc.x = fmaf(xw[m], pv.x, acc.x);
+        acc.y = fmaf(xw[m], pv.y, acc.y);
+        acc.z = fmaf(xw[m], pv.z, acc.z);
+        acc.w = fmaf(xw[m], pv.w, acc.w);
+      }
+    }
+    *reinterpret_cast<float4 *>(X + fo(16 * a + i, 16 * b + j0)) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+}
+
+// X = (I + A)^{-1} for a strictly lower-triangular 64 x 64 A (fp32 arrays,
+// row stride 68), by 16 x 16 blocks: diagonal blocks by forward substitution (one
 // column per thread, each row of A read as four float4), then
 // X_ab = -X_aa sum_{b<=r<a} A_ar X_rb by block distance a - b = 1, 2, 3.
 // X's strictly upper part is not written.
@@ -223,8 +224,10 @@ __device__ void unit_lower_inverse(const float *A, float *X, float *P, int tid) 
   __syncthreads();
 }
 
-__device__ __forceinline__ uint64_t dsc(uint32_t addr) {
-  return umma::sdesc_sw128(addr);
+// Descriptor of a tile `off` bytes past the one `d` describes (the start
+// address field counts 16-byte units).
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t off) {
+  return d + (off >> 4);
 }
 
 // Thread 0 waits for the last commit (bounded); every thread learns whether
@@ -246,28 +249,43 @@ __device__ __forceinline__ void tiles_ready() {
   umma::fence_after_sync();
 }
 
-// 16-byte global -> shared copy; src_bytes = 0 writes zeros (src unread).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src,
-                                           int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
-               :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-               :: "l"(p), "r"(bytes) : "memory");
+// Tensor maps of the packed inputs viewed as [N][H][D] (3-D, innermost D):
+// boxes of 64 tokens x 1 head x 128 channels (q, k, alpha) or x NC channels
+// (v); rows past N read as zeros.
+struct InputMaps {
+  CUtensorMap q, k, a, v, b;  // b: beta [N][H] as 2-D, boxes of 8 heads x 64 tokens
+};
+
+// One TMA load of a 2-D box of `tm` at (x, token) into shared memory,
+// completing its bytes on the mbarrier's transaction count.
+__device__ __forceinline__ void tma_load2(uint32_t dst, const CUtensorMap *tm, int x,
+                                          int tok, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(tok), "r"(mbar)
+      : "memory");
 }
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 *p) {
-  return __bfloat162float(*p);
+// One TMA load of a box of `tm` at (x, head, token) into shared memory,
+// completing its bytes on the mbarrier's transaction count.
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *tm, int x,
+                                          int head, int tok, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(head), "r"(tok),
+         "r"(mbar) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(mbar), "r"(bytes) : "memory");
+}
+
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
   extern __shared__ float4 smem4[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
@@ -302,13 +320,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
   }
 
   if (tid < 32) umma::tmem_alloc(tslot, 512);
-  if (tid == 0) umma::mbar_init(mbar, 1);
+  if (tid == 0) {
+    umma::mbar_init(mbar, 1);
+    umma::mbar_init(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), 1);
+  }
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);  // lane quadrant
   uint32_t phase = 0;
+  const uint32_t sbar = sb + Lay::SBAR;
+  const uint64_t dGA = umma::sdesc_sw128(sb + Lay::GA_HI);  // all tiles from here
+  uint32_t sphase = 0;        // next phase of the staging barrier
+  bool stage_owed = false;    // copies issued and not yet waited for
 
   // S[c][col0 + 16 hf + jj], fp32, for the whole pass
   float S[16];
@@ -318,48 +343,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     for (int jj = 0; jj < 16; ++jj)
       S[jj] = src[(size_t)(col0 + 16 * hf + jj) * kD + c];
   }
-  const __nv_bfloat16 *qin = reinterpret_cast<const __nv_bfloat16 *>(p.q);
-  const __nv_bfloat16 *kin = reinterpret_cast<const __nv_bfloat16 *>(p.k);
-  const __nv_bfloat16 *vin = reinterpret_cast<const __nv_bfloat16 *>(p.v);
-  const __nv_bfloat16 *ain = reinterpret_cast<const __nv_bfloat16 *>(p.alpha);
-  const __nv_bfloat16 *bin = reinterpret_cast<const __nv_bfloat16 *>(p.beta);
 
   const int r0 = p0 % kC;
   const int nch = (r0 + L + kC - 1) / kC;
-  // Copies of chunk qq's raw rows into the staging areas (rows past the
-  // chunk read as zeros), its beta into a register, and an L2 prefetch of
-  // chunk qq + 1's rows.
-  float beta_next = 0.f;
+  // TMA loads of chunk qq's 64 rows of q, k, alpha, the V slice and beta
+  // (the 8 heads around h) into the staging areas (rows past the chunk are
+  // masked where they are read), completing on the staging barrier.
   auto stage = [&](int qq) {
-    const int s0 = max(0, qq * kC - r0), nn = min(L, (qq + 1) * kC - r0) - s0;
-    const size_t row0 = ((size_t)(cu0 + s0) * H + h) * kD;
-    for (int e = tid; e < 3 * 64 * 16; e += kThreads) {
-      const int tens = e >> 10, t = (e >> 4) & 63, ch = e & 15;
-      const __nv_bfloat16 *src = (tens == 0 ? qin : tens == 1 ? kin : ain) + row0 +
-                                 (size_t)min(t, nn - 1) * H * kD + ch * 8;
-      cp_async16(sb + (tens == 0 ? kStgQ : tens == 1 ? kStgK : kStgA) + t * 256 + ch * 16,
-                 src, t < nn ? 16 : 0);
+    const int s0 = max(0, qq * kC - r0);
+    if (tid == 0) {
+      mbar_expect_tx(sbar, 3 * 64 * 2 * kD + 64 * 2 * kNC + 64 * 16);
+      tma_load3(sb + kStgQ, &maps.q, 0, h, cu0 + s0, sbar);
+      tma_load3(sb + kStgK, &maps.k, 0, h, cu0 + s0, sbar);
+      tma_load3(sb + kStgA, &maps.a, 0, h, cu0 + s0, sbar);
+      tma_load3(sb + kStgV, &maps.v, col0, h, cu0 + s0, sbar);
+      tma_load2(sb + Lay::BST, &maps.b, h & ~7, cu0 + s0, sbar);
     }
-    {
-      const int t = tid >> 2, ch = tid & 3;
-      cp_async16(sb + kStgV + t * 64 + ch * 16,
-                 vin + row0 + (size_t)min(t, nn - 1) * H * kD + col0 + ch * 8,
-                 t < nn ? 16 : 0);
-    }
-    cp_async_commit();
-    if (tid < kC)
-      beta_next = tid < nn ? bf(bin + (size_t)(cu0 + s0 + tid) * H + h) : 0.f;
-    if (qq + 1 < nch) {
-      const int s1 = (qq + 1) * kC - r0, e1 = min(L, s1 + kC);
-      const int t = tid & 63, tens = tid >> 6;
-      if (s1 + t < e1) {
-        const size_t r = ((size_t)(cu0 + s1 + t) * H + h) * kD;
-        if (tens < 3)
-          prefetch_l2((tens == 0 ? qin : tens == 1 ? kin : ain) + r, 256);
-        else
-          prefetch_l2(vin + r + col0, 2 * kNC);
-      }
-    }
+    stage_owed = true;
   };
   stage(0);
   bool ok = true;
@@ -372,9 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     // (channel pair cp, token quarter tq) takes channels 2cp, 2cp+1 of rows
     // 16tq .. 16tq+15: cumulative log-decay (padded rows: alpha = 1), then the
     // scaled operand tiles; S~ from the state rows this thread owns.
-    cp_async_wait_all();
-    if (tid < kC) bet[tid] = beta_next;
-    __syncthreads();
+    if (!(ok = tc_wait(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), sphase, tid))) break;
+    stage_owed = false;
+    if (tid < kC) {
+      const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + Lay::BST)[tid * 8 + (h & 7)];
+      bet[tid] = tid < n ? __uint_as_float((uint32_t)bw << 16) : 0.f;
+    }
     const int cp = tid & 63, tq = tid >> 6, c2 = 2 * cp, tb0 = 16 * tq;
     float la0[16], la1[16];
     uint32_t kr[16], qr[16];
@@ -386,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
       for (int u = 0; u < 16; ++u) {
         const int t = tb0 + u;
         const uint32_t aw = sa[t * 64 + cp];
-        kr[u] = sk[t * 64 + cp];
-        qr[u] = sq[t * 64 + cp];
+        kr[u] = t < n ? sk[t * 64 + cp] : 0u;
+        qr[u] = t < n ? sq[t * 64 + cp] : 0u;
         la0[u] = t < n ? __logf(__uint_as_float(aw << 16)) : 0.f;
         la1[u] = t < n ? __logf(__uint_as_float(aw & 0xffff0000u)) : 0.f;
       }
@@ -399,7 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int ta = 8 * tg + 2 * e;
-        vw[e] = (uint32_t)vs[ta * kNC + j] | ((uint32_t)vs[(ta + 1) * kNC + j] << 16);
+        vw[e] = (ta < n ? (uint32_t)vs[ta * kNC + j] : 0u) |
+                (ta + 1 < n ? (uint32_t)vs[(ta + 1) * kNC + j] << 16 : 0u);
       }
     }
 #pragma unroll
@@ -505,11 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     if (tid == 0) {
       const uint32_t id = umma::idesc_bf16(128, 64);
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = sb + (ps == 1 ? Lay::GA_LO : Lay::GA_HI);
-        const uint32_t b = sb + (ps == 2 ? Lay::GB_LO : Lay::GB_HI);
+        const uint32_t a = ps == 1 ? Lay::GA_LO : Lay::GA_HI;
+        const uint32_t b = ps == 2 ? Lay::GB_LO : Lay::GB_HI;
         for (int kk = 0; kk < 8; ++kk)
-          umma::mma_bf16(tmem + kAccG, dsc(a + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         dsc(b + (kk >> 2) * 8192 + (kk & 3) * 32), id,
+          umma::mma_bf16(tmem + kAccG, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
+                         dadd(dGA, b + (kk >> 2) * 8192 + (kk & 3) * 32), id,
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
@@ -573,11 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     // ---- R2: [T; M] [K~^T; V^T]^T -> rows 0..63: W~ (cols 0..127), U' (128..)
     if (tid == 0) {
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = sb + (ps == 1 ? Lay::TM_LO : Lay::TM_HI);
-        const uint32_t b = sb + (ps == 2 ? Lay::B2_LO : Lay::B2_HI);
+        const uint32_t a = ps == 1 ? Lay::TM_LO : Lay::TM_HI;
+        const uint32_t b = ps == 2 ? Lay::B2_LO : Lay::B2_HI;
         const uint32_t id = umma::idesc_bf16(128, ps == 2 ? 128 : 128 + kNC);
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc2, dsc(a + kk * 32), dsc(b + kk * 32), id,
+          umma::mma_bf16(tmem + kAcc2, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
@@ -605,11 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     if (tid == 0) {
       const uint32_t id = umma::idesc_bf16(128, kNC);
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = sb + (ps == 1 ? Lay::GA_LO : Lay::GA_HI);
-        const uint32_t b = sb + (ps == 2 ? Lay::SB_LO : Lay::SB_HI);
+        const uint32_t a = ps == 1 ? Lay::GA_LO : Lay::GA_HI;
+        const uint32_t b = ps == 2 ? Lay::SB_LO : Lay::SB_HI;
         for (int kk = 0; kk < 8; ++kk)
-          umma::mma_bf16(tmem + kAcc3, dsc(a + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         dsc(b + (kk >> 2) * (kNC * 128) + (kk & 3) * 32), id,
+          umma::mma_bf16(tmem + kAcc3, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
+                         dadd(dGA, b + (kk >> 2) * (kNC * 128) + (kk & 3) * 32), id,
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
@@ -634,17 +638,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
     if (tid == 0) {
       const uint32_t id = umma::idesc_bf16(128, kNC);
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = sb + (ps == 1 ? Lay::KH_LO : Lay::KH_HI);
-        const uint32_t b = sb + (ps == 2 ? Lay::UT_LO : Lay::UT_HI);
+        const uint32_t a = ps == 1 ? Lay::KH_LO : Lay::KH_HI;
+        const uint32_t b = ps == 2 ? Lay::UT_LO : Lay::UT_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc4, dsc(a + kk * 32), dsc(b + kk * 32), id,
+          umma::mma_bf16(tmem + kAcc4, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
                          (uint32_t)(ps | kk));
       }
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = sb + (ps == 1 ? Lay::TM_LO : Lay::TM_HI);
-        const uint32_t b = sb + (ps == 2 ? Lay::UT_LO : Lay::UT_HI);
+        const uint32_t a = ps == 1 ? Lay::TM_LO : Lay::TM_HI;
+        const uint32_t b = ps == 2 ? Lay::UT_LO : Lay::UT_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc3, dsc(a + kk * 32), dsc(b + kk * 32), id, 1u);
+          umma::mma_bf16(tmem + kAcc3, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id, 1u);
       }
       umma::commit(mbar);
     }
@@ -699,7 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) dst[(size_t)(col0 + 16 * hf + jj) * kD + c] = S[jj];
   }
-  cp_async_wait_all();  // no copy into shared memory outlives the CTA
+  // no copy into shared memory outlives the CTA
+  if (stage_owed && tid == 0)
+    umma::mbar_wait(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), sphase, 1 << 26);
   umma::fence_before_sync();
   __syncthreads();
   if (tid < 32) umma::tmem_dealloc(tmem, 512);
@@ -707,14 +713,77 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 
 }  // namespace
 
-// d_k = d_v = 128, chunk 64, bf16 inputs; no workspace.
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [N][H][D] bf16 as a 3-D tensor map with boxes of `box_x` channels x 1 head
+// x 64 tokens, no swizzle, zero fill past N.
+cudaError_t input_map(CUtensorMap *tm, const void *base, int N, int H, int box_x) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)N};
+  const cuuint64_t gstride[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)kC};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                         gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// beta [N][H] bf16 as a 2-D tensor map with boxes of 8 heads x 64 tokens
+// (H a multiple of 8: the row stride must be a multiple of 16 bytes).
+cudaError_t beta_map(CUtensorMap *tm, const void *base, int N, int H) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {(cuuint64_t)H, (cuuint64_t)N};
+  const cuuint64_t gstride[1] = {(cuuint64_t)H * 2};
+  const cuuint32_t box[2] = {8, (cuuint32_t)kC};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                         gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+// d_k = d_v = 128, chunk 64, bf16 inputs, H a multiple of 8; no workspace.
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
-  if (p.B == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Lay::kBytes);
+  if (p.B == 0 || p.N == 0) return cudaSuccess;
+  InputMaps maps;
+  cudaError_t e = input_map(&maps.q, p.q, p.N, p.H, kD);
+  if (e == cudaSuccess) e = input_map(&maps.k, p.k, p.N, p.H, kD);
+  if (e == cudaSuccess) e = input_map(&maps.a, p.alpha, p.N, p.H, kD);
+  if (e == cudaSuccess) e = input_map(&maps.v, p.v, p.N, p.H, kNC);
+  if (e == cudaSuccess) e = beta_map(&maps.b, p.beta, p.N, p.H);
   if (e != cudaSuccess) return e;
-  prefill_tc_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, Lay::kBytes, s>>>(p);
+  e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  prefill_tc_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, Lay::kBytes, s>>>(p, maps);
   return cudaGetLastError();
 }
 

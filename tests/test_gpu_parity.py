@@ -341,7 +341,8 @@ def test_prefill_full_workload_sampled_heads():
 def test_prefill_ragged_and_offsets(C, d):
     lengths = [0, 1, C - 1, C, C + 1, 3 * C + 5, 100]
     starts = [0, 5, 0, 2 * C, C - 3, 7, 0]
-    _run_prefill(lengths, starts, 4, d, C, 2 * C, "bf16", 3, [0, 1, 2, 3],
+    H = 8 if d == 128 else 4  # d=128, chunk 64, 8 heads: the tensor-core kernel
+    _run_prefill(lengths, starts, H, d, C, 2 * C, "bf16", 3, [0, 1, H // 2 + 1, H - 1],
                  seed=900 + C + d, s0_std=0.1, skip_ckpt=[(5, 1)])
 
 
@@ -349,8 +350,8 @@ def test_prefill_slow_decay_carries_state():
     """alpha in [0.97, 1): the state carried across chunks dominates the
     outputs (with the default alpha ~ 0.5 it fades within a chunk), so the
     inter-chunk pass and the checkpoints are tested at full weight."""
-    _run_prefill([1000, 333, 64], [0, 17, 64], 3, 128, 64, 128, "bf16", 8,
-                 [0, 1, 2], seed=912, s0_std=0.5,
+    _run_prefill([1000, 333, 64], [0, 17, 64], 8, 128, 64, 128, "bf16", 8,
+                 [0, 3, 7], seed=912, s0_std=0.5,
                  alpha=lambda rng, shp: 1.0 - 0.03 * rng.random(shp))
 
 
@@ -363,8 +364,8 @@ def test_prefill_chunk_size_independent():
     rng_lengths = [300, 129]
     outs = []
     for C in (16, 32, 64):
-        tb, pool, _ = _run_prefill(rng_lengths, [0, 0], 2, 128, C, 64, "bf16",
-                                   1, [0, 1], seed=44, s0_std=0.02)
+        tb, pool, _ = _run_prefill(rng_lengths, [0, 0], 8, 128, C, 64, "bf16",
+                                   1, [0, 7], seed=44, s0_std=0.02)
         outs.append((tb.o.cpu().numpy(), pool.data[:2].cpu().numpy()))
     for o, s in outs[1:]:
         assert np.max(np.abs(o - outs[0][0])) <= 2e-3
@@ -375,7 +376,7 @@ def test_prefill_then_verify_from_checkpoint():
     """Partial prefix hit: fork a checkpoint into a fresh slot, prefill the
     rest of the prompt from its absolute position, then verify drafts."""
     rng = np.random.default_rng(61)
-    H, d, C = 4, 128, 64
+    H, d, C = 8, 128, 64
     prompt = ki.round_to(ki.gen_tokens(rng, [256], H, d), "bf16")
     pool = K.StatePool.zeros(8, H, d)
     ring = K.ReplayRing(8, H, d, 8, torch.bfloat16)
@@ -411,7 +412,7 @@ def test_serving_shaped_reduced():
     the capped geometric (rho = 0.8802) until 64 tokens are committed."""
     w = ki.SERVING
     rng = np.random.default_rng(w.seed)
-    B, H, d, T, P = 3, 4, 128, 8, 3 + 12
+    B, H, d, T, P = 3, 8, 128, 8, 3 + 12
     prompt = ki.round_to(ki.gen_tokens(rng, [512] * B, H, d), "bf16")
     pool = K.StatePool.zeros(P, H, d)
     ring = K.ReplayRing(P, H, d, T, torch.bfloat16)
@@ -520,9 +521,9 @@ def test_prefill_decay_range_flag():
 
 def test_prefill_decay_range_flag_tensor_core_shape():
     rng = np.random.default_rng(75)
-    tok = ki.round_to(ki.gen_tokens(rng, [64], 1, 128), "bf16")
+    tok = ki.round_to(ki.gen_tokens(rng, [64], 8, 128), "bf16")
     tok["alpha"][:] = 1e-3
-    pool = K.StatePool.zeros(1, 1, 128)
+    pool = K.StatePool.zeros(1, 8, 128)
     K.kda_prefill_chunked(device_batch(tok, "bf16"), pool, i32([0]), chunk=64)
     assert K.kda_get_device_error() & K.KDA_DERR_RANGE
 

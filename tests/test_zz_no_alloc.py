@@ -55,7 +55,7 @@ def _prefill_pair(seed, lengths, starts, H, d, C, ckpt_every, max_ckpt):
 
 def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
     cases = [
-        (501, [200, 77], [0, 5], 4, 128, 64, 128, 2),
+        (501, [200, 77], [0, 5], 8, 128, 64, 128, 2),
         (502, [130, 1, 64], [64, 3, 0], 2, 64, 32, 64, 3),
     ]
     for seed, lengths, starts, H, d, C, E, mc in cases:
