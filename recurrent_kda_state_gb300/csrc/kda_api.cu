@@ -179,7 +179,8 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
   if ((st = check_ring(ring, tok->dtype, true))) return st;
   if (max_T < 0) return KDA_EINVAL;
   if (!is_spec && max_T > ring->depth) return KDA_EPROTO;
-  if (kda::verify_smem_bytes(tok->d_k, ring->depth, max_T) > kMaxSmem) return KDA_EINVAL;
+  if (kda::verify_smem_bytes(tok->d_k, ring->depth, max_T, tok->dtype) > kMaxSmem)
+    return KDA_EINVAL;
   if (tok->num_seqs == 0) return KDA_OK;
   if (!state_slots) return KDA_EINVAL;
   unsigned *err = device_error_word();

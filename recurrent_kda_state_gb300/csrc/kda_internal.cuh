@@ -148,7 +148,7 @@ __host__ __device__ inline size_t prefill_workspace_bytes(int N, int B, int H,
 
 // Verify launch geometry: dynamic shared memory for (D, ring depth, max_T),
 // and the longest speculative segment the kernel supports (ring depth limit).
-size_t verify_smem_bytes(int D, int depth, int max_T);
+size_t verify_smem_bytes(int D, int depth, int max_T, kda_dtype dt);
 int verify_max_spec_tokens();
 
 // Launchers: return cudaError_t of the launch.

@@ -56,30 +56,53 @@ __device__ __forceinline__ float sum2(f2 a) {  // lane0 + lane1, round to neares
   return __fadd_rn(x, y);
 }
 
-// Per-token record in shared memory (fp32): k[D] alpha[D] q[D] v[D] beta pad3.
-template <int D>
+// Per-token record in shared memory, in the input dtype (the values exactly
+// as they were given): k[D] alpha[D] q[D] v[D] beta, padded to 16 bytes.
+template <int D, typename Tin>
 struct Rec {
-  static constexpr int kStride = 4 * D + 4;
+  static constexpr int kStride = 4 * D + 16 / (int)sizeof(Tin);
   static constexpr int kK = 0, kA = D, kQ = 2 * D, kV = 3 * D, kB = 4 * D;
+  static constexpr int kBytes = kStride * (int)sizeof(Tin);
 };
+
+// Channels c .. c+3 of a record vector (c a multiple of 4) as two fp32 pairs
+// (c, c+1) and (c+2, c+3); exact for both input dtypes.
+__device__ __forceinline__ void ld4x(const float *p, f2 &a, f2 &b) {
+  const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(p);
+  a = v.x;
+  b = v.y;
+}
+__device__ __forceinline__ void ld4x(const __nv_bfloat16 *p, f2 &a, f2 &b) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  a = pack2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+  b = pack2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
+// The same four channels as a float4.
+__device__ __forceinline__ float4 ld4f(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 ld4f(const __nv_bfloat16 *p) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
 
 // One token of the recurrence on the thread's slice of S, fixed rounding:
 //   S' = Diag(alpha) S;  dot_j = sum_c k_c S'_cj;  delta_j = beta (v_j - dot_j)
 //   S  = S' + k delta^T;  o_j = sum_c q_c S_cj  (when WANT_O)
 // The only code that advances a committed state: replay, decode and
 // materialize all call it, so identical inputs give identical bits.
-template <int D, bool WANT_O>
-__device__ __forceinline__ void kda_step(f2 (&S)[2][D / 8], const float *rec,
+template <int D, bool WANT_O, typename Tin>
+__device__ __forceinline__ void kda_step(f2 (&S)[2][D / 8], const Tin *rec,
                                          int rg, int j0, float &o0, float &o1) {
   constexpr int F = D / 16;
-  const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(rec + Rec<D>::kK);
-  const ulonglong2 *a2 = reinterpret_cast<const ulonglong2 *>(rec + Rec<D>::kA);
-  const ulonglong2 *q2 = reinterpret_cast<const ulonglong2 *>(rec + Rec<D>::kQ);
+  typedef Rec<D, Tin> R;
   f2 dA0 = 0, dB0 = 0, dA1 = 0, dB1 = 0;
 #pragma unroll
   for (int f = 0; f < F; ++f) {
-    const ulonglong2 kk = k2[rg + 4 * f];
-    const ulonglong2 aa = a2[rg + 4 * f];
+    ulonglong2 kk, aa;
+    ld4x(rec + R::kK + 4 * (rg + 4 * f), kk.x, kk.y);
+    ld4x(rec + R::kA + 4 * (rg + 4 * f), aa.x, aa.y);
     S[0][2 * f] = mul2(S[0][2 * f], aa.x);
     S[0][2 * f + 1] = mul2(S[0][2 * f + 1], aa.y);
     S[1][2 * f] = mul2(S[1][2 * f], aa.x);
@@ -95,20 +118,22 @@ __device__ __forceinline__ void kda_step(f2 (&S)[2][D / 8], const float *rec,
   d1 = __fadd_rn(d1, __shfl_xor_sync(kFull, d1, 1));
   d0 = __fadd_rn(d0, __shfl_xor_sync(kFull, d0, 2));
   d1 = __fadd_rn(d1, __shfl_xor_sync(kFull, d1, 2));
-  const float beta = rec[Rec<D>::kB];
-  const float del0 = __fmul_rn(beta, __fsub_rn(rec[Rec<D>::kV + j0], d0));
-  const float del1 = __fmul_rn(beta, __fsub_rn(rec[Rec<D>::kV + j0 + 1], d1));
+  const float beta = in_scalar<Tin>(rec + R::kB);
+  const float del0 = __fmul_rn(beta, __fsub_rn(in_scalar<Tin>(rec + R::kV + j0), d0));
+  const float del1 = __fmul_rn(beta, __fsub_rn(in_scalar<Tin>(rec + R::kV + j0 + 1), d1));
   const f2 D0 = pack2(del0, del0), D1 = pack2(del1, del1);
   f2 oA0 = 0, oB0 = 0, oA1 = 0, oB1 = 0;
 #pragma unroll
   for (int f = 0; f < F; ++f) {
-    const ulonglong2 kk = k2[rg + 4 * f];
+    ulonglong2 kk;
+    ld4x(rec + R::kK + 4 * (rg + 4 * f), kk.x, kk.y);
     S[0][2 * f] = fma2(kk.x, D0, S[0][2 * f]);
     S[0][2 * f + 1] = fma2(kk.y, D0, S[0][2 * f + 1]);
     S[1][2 * f] = fma2(kk.x, D1, S[1][2 * f]);
     S[1][2 * f + 1] = fma2(kk.y, D1, S[1][2 * f + 1]);
     if (WANT_O) {
-      const ulonglong2 qq = q2[rg + 4 * f];
+      ulonglong2 qq;
+      ld4x(rec + R::kQ + 4 * (rg + 4 * f), qq.x, qq.y);
       oA0 = fma2(qq.x, S[0][2 * f], oA0);
       oB0 = fma2(qq.y, S[0][2 * f + 1], oB0);
       oA1 = fma2(qq.x, S[1][2 * f], oA1);
@@ -127,38 +152,19 @@ __device__ __forceinline__ void kda_step(f2 (&S)[2][D / 8], const float *rec,
   }
 }
 
-// Raw 16-byte vector of inputs -> fp32 (4 or 8 values).
-template <typename Tin>
-__device__ __forceinline__ void cvt16(const uint4 &raw, float *dst);
-template <>
-__device__ __forceinline__ void cvt16<float>(const uint4 &raw, float *dst) {
-  *reinterpret_cast<float4 *>(dst) =
-      make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y),
-                  __uint_as_float(raw.z), __uint_as_float(raw.w));
-}
-template <>
-__device__ __forceinline__ void cvt16<__nv_bfloat16>(const uint4 &raw, float *dst) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  *reinterpret_cast<float4 *>(dst) =
-      make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xffff0000u),
-                  __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xffff0000u));
-  *reinterpret_cast<float4 *>(dst + 4) =
-      make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xffff0000u),
-                  __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xffff0000u));
-}
-
 // Ring entries to replay (k, alpha, v, beta of `acc` entries) and this
-// launch's tokens (k, alpha, v, q, beta of T rows) -> fp32 records in shared
-// memory.  Vector rows are numbered ring-first (3 per entry) then token rows
-// (4 per token); thread tid always copies 16-byte chunk tid % CH of rows
-// tid / CH, + NT / CH, ...  All of a thread's loads are issued before any of
-// them is converted.
+// launch's tokens (k, alpha, v, q, beta of T rows) -> records in shared
+// memory, copied as they are.  Vector rows are numbered ring-first (3 per
+// entry) then token rows (4 per token); thread tid always copies 16-byte
+// chunk tid % CH of rows tid / CH, + NT / CH, ...  All of a thread's loads
+// are issued before any of them is stored.
 template <int D, typename Tin>
 __device__ __forceinline__ void load_all_records(
-    float *rep, float *drf, int acc, int T, const Tin *rk, const Tin *ra,
+    Tin *rep, Tin *drf, int acc, int T, const Tin *rk, const Tin *ra,
     const Tin *rv, const Tin *rb, const Tin *tk, const Tin *ta, const Tin *tv,
     const Tin *tq, const Tin *tb, size_t tok_stride, size_t beta_stride,
     int tid) {
+  typedef Rec<D, Tin> RC;
   constexpr int NT = 2 * D;
   constexpr int E = InVec<Tin>::kElems;
   constexpr int CH = D / E;         // power of two
@@ -166,18 +172,18 @@ __device__ __forceinline__ void load_all_records(
   constexpr int R = 4;              // loads in flight per thread
   const int ch = tid % CH;
   const int nring = acc * 3, nrows = nring + T * 4;
-  float bval = 0.f;
-  float *bdst = nullptr;
+  Tin bval;
+  Tin *bdst = nullptr;
   if (tid < acc) {
-    bval = in_scalar<Tin>(rb + tid);
-    bdst = rep + tid * Rec<D>::kStride + Rec<D>::kB;
+    bval = rb[tid];
+    bdst = rep + tid * RC::kStride + RC::kB;
   } else if (tid < acc + T) {
-    bval = in_scalar<Tin>(tb + (size_t)(tid - acc) * beta_stride);
-    bdst = drf + (tid - acc) * Rec<D>::kStride + Rec<D>::kB;
+    bval = tb[(size_t)(tid - acc) * beta_stride];
+    bdst = drf + (tid - acc) * RC::kStride + RC::kB;
   }
   for (int base = tid / CH; base < nrows; base += R * RSTEP) {
     uint4 buf[R];
-    float *dst[R];
+    Tin *dst[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int row = base + r * RSTEP;
@@ -187,23 +193,23 @@ __device__ __forceinline__ void load_all_records(
         if (row < nring) {
           const int t = row / 3, which = row - 3 * (row / 3);
           src = (which == 0 ? rk : which == 1 ? ra : rv) + t * D + ch * E;
-          dst[r] = rep + t * Rec<D>::kStride +
-                   (which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV) + ch * E;
+          dst[r] = rep + t * RC::kStride +
+                   (which == 0 ? RC::kK : which == 1 ? RC::kA : RC::kV) + ch * E;
         } else {
           const int rr = row - nring;
           const int t = rr >> 2, which = rr & 3;
           const Tin *base_ptr = which == 0 ? tk : which == 1 ? ta : which == 2 ? tv : tq;
           src = base_ptr + (size_t)t * tok_stride + ch * E;
-          dst[r] = drf + t * Rec<D>::kStride +
-                   (which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA
-                    : which == 2 ? Rec<D>::kV : Rec<D>::kQ) + ch * E;
+          dst[r] = drf + t * RC::kStride +
+                   (which == 0 ? RC::kK : which == 1 ? RC::kA
+                    : which == 2 ? RC::kV : RC::kQ) + ch * E;
         }
         buf[r] = *reinterpret_cast<const uint4 *>(src);
       }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r)
-      if (dst[r]) cvt16<Tin>(buf[r], dst[r]);
+      if (dst[r]) *reinterpret_cast<uint4 *>(dst[r]) = buf[r];
   }
   if (bdst) *bdst = bval;
 }
@@ -213,24 +219,26 @@ __device__ __forceinline__ void load_all_records(
 // 16).
 //   a    tcgen05 A tiles: the committed state as bf16 hi, then lo, K-major
 //        128B-swizzled (128 rows = value columns j, K = key rows c);
-//   rb   the replay records, later (once replayed) the bf16 B tile
-//        [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows, K-major 128B-swizzled)
-//        followed (kx) by K~ and Q~ in fp32, row-major [2 TP][D];
-//   drf  this launch's token records;  kh = k / gamma;  vb = v and beta of the
-//        drafted tokens;  am, bm = the T x T matrices of the triangular solve.
-template <int D>
+//   rep  the ring entries to replay;  drf  this launch's token records (both
+//        in the input dtype);
+//   rb   the bf16 B tile [K~_hi, Q~_hi, K~_lo, Q~_lo] (4 TP rows, K-major
+//        128B-swizzled), then (kx) K~ and Q~ in fp32, row-major [2 TP][D];
+//   kh = k / gamma;  vb = v and beta of the drafted tokens;  am, bm = the
+//   T x T matrices of the triangular solve.
+// Nothing of the drafts shares space with the replay records, so the drafts'
+// state-independent parts run before the replay.
+template <int D, typename Tin>
 struct Smem {
-  int tp, a, rb, kx, drf, kh, vb, am, bm, total;
+  int tp, a, rep, drf, rb, kx, kh, vb, am, bm, total;
   __host__ __device__ Smem(int depth, int maxT) {
     tp = maxT <= 8 ? 8 : 16;
     const int kblk = (D + 63) / 64;  // bf16 K blocks
-    const int rep_bytes = depth * Rec<D>::kStride * 4;
-    const int b_bytes = kblk * 4 * tp * 128 + 2 * tp * D * 4;
     a = 0;
-    rb = 2 * kblk * 128 * 128;
+    rep = 2 * kblk * 128 * 128;
+    drf = rep + depth * Rec<D, Tin>::kBytes;
+    rb = (drf + maxT * Rec<D, Tin>::kBytes + 1023) & ~1023;
     kx = rb + kblk * 4 * tp * 128;
-    drf = rb + (((rep_bytes > b_bytes ? rep_bytes : b_bytes) + 1023) & ~1023);
-    kh = drf + maxT * Rec<D>::kStride * 4;
+    kh = kx + 2 * tp * D * 4;
     vb = kh + tp * D * 4;
     am = vb + (tp * D + tp) * 4;
     bm = am + kTMax * kTMax * 4;
@@ -244,9 +252,10 @@ struct Smem {
 // 3TP+t (the remainders, rounded to bf16), zero rows past T, the fp32 values
 // (kx), kh = k / gamma, and v, beta.  Returns whether
 // gamma left [2^-60, 2^60] anywhere (then A and B use explicit products).
-template <int D, int TP>
-__device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
-                                          const float *drf, int T, int tid) {
+template <int D, int TP, typename Tin>
+__device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D, Tin> &L,
+                                          const Tin *drf, int T, int tid) {
+  typedef Rec<D, Tin> R;
   constexpr int NT = 2 * D, N1 = 4 * TP;
   float *kh = reinterpret_cast<float *>(smb + L.kh);
   float *vb = reinterpret_cast<float *>(smb + L.vb);
@@ -257,18 +266,17 @@ __device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
     const int c4 = item % (D / 4), t = item / (D / 4);
     float4 kt = make_float4(0.f, 0.f, 0.f, 0.f), qt = kt;
     if (t < T) {
-      float4 g = *reinterpret_cast<const float4 *>(drf + Rec<D>::kA + 4 * c4);
+      float4 g = ld4f(drf + R::kA + 4 * c4);
 #pragma unroll
       for (int r = 1; r < TP; ++r) {
         if (r <= t) {
-          const float4 a = *reinterpret_cast<const float4 *>(
-              drf + r * Rec<D>::kStride + Rec<D>::kA + 4 * c4);
+          const float4 a = ld4f(drf + r * R::kStride + R::kA + 4 * c4);
           g.x *= a.x; g.y *= a.y; g.z *= a.z; g.w *= a.w;
         }
       }
-      const float *rr = drf + t * Rec<D>::kStride;
-      const float4 k = *reinterpret_cast<const float4 *>(rr + Rec<D>::kK + 4 * c4);
-      const float4 q = *reinterpret_cast<const float4 *>(rr + Rec<D>::kQ + 4 * c4);
+      const Tin *rr = drf + t * R::kStride;
+      const float4 k = ld4f(rr + R::kK + 4 * c4);
+      const float4 q = ld4f(rr + R::kQ + 4 * c4);
       kt = make_float4(g.x * k.x, g.y * k.y, g.z * k.z, g.w * k.w);
       qt = make_float4(g.x * q.x, g.y * q.y, g.z * q.z, g.w * q.w);
       const float gm = fminf(fminf(g.x, g.y), fminf(g.z, g.w));
@@ -277,9 +285,8 @@ __device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
       *reinterpret_cast<float4 *>(kh + t * D + 4 * c4) =
           make_float4(__fdividef(k.x, g.x), __fdividef(k.y, g.y),
                       __fdividef(k.z, g.z), __fdividef(k.w, g.w));
-      *reinterpret_cast<float4 *>(vb + t * D + 4 * c4) =
-          *reinterpret_cast<const float4 *>(rr + Rec<D>::kV + 4 * c4);
-      if (c4 == 0) vb[TP * D + t] = rr[Rec<D>::kB];
+      *reinterpret_cast<float4 *>(vb + t * D + 4 * c4) = ld4f(rr + R::kV + 4 * c4);
+      if (c4 == 0) vb[TP * D + t] = in_scalar<Tin>(rr + R::kB);
     }
     *reinterpret_cast<float4 *>(kx + t * D + 4 * c4) = kt;
     *reinterpret_cast<float4 *>(kx + (TP + t) * D + 4 * c4) = qt;
@@ -300,10 +307,11 @@ __device__ __forceinline__ int prep_tiles(unsigned char *smb, const Smem<D> &L,
 
 // Part 2: the T^2 pair dots (B: s <= t, then A: s < t; A without beta),
 // 4 lanes per pair, each lane a quarter of the key channels.
-template <int D, int TP>
+template <int D, int TP, typename Tin>
 __device__ __forceinline__ void prep_pairs(unsigned char *smb,
-                                           const Smem<D> &L, const float *drf,
+                                           const Smem<D, Tin> &L, const Tin *drf,
                                            int T, int tid, int unsafe) {
+  typedef Rec<D, Tin> R;
   constexpr int NT = 2 * D;
   const float *kh = reinterpret_cast<const float *>(smb + L.kh);
   const float *kx = reinterpret_cast<const float *>(smb + L.kx);
@@ -347,9 +355,10 @@ __device__ __forceinline__ void prep_pairs(unsigned char *smb,
         // decay products taken explicitly when gamma leaves the safe range
         for (int c = rg; c < D; c += 4) {
           float pr = 1.f;
-          for (int u = s + 1; u <= t; ++u) pr *= drf[u * Rec<D>::kStride + Rec<D>::kA + c];
-          const float x = drf[t * Rec<D>::kStride + (isB ? Rec<D>::kQ : Rec<D>::kK) + c];
-          acc = fmaf(x * drf[s * Rec<D>::kStride + Rec<D>::kK + c], pr, acc);
+          for (int u = s + 1; u <= t; ++u)
+            pr *= in_scalar<Tin>(drf + u * R::kStride + R::kA + c);
+          const float x = in_scalar<Tin>(drf + t * R::kStride + (isB ? R::kQ : R::kK) + c);
+          acc = fmaf(x * in_scalar<Tin>(drf + s * R::kStride + R::kK + c), pr, acc);
         }
       }
     }
@@ -393,10 +402,10 @@ __device__ __forceinline__ void write_state_tiles(unsigned char *sa,
 // delta_t = beta_t (v_tj - x_t - sum_{s<t} A_ts delta_s),
 // o_tj = y_t + sum_{s<=t} B_ts delta_s.  Only t with t % ng == grp are
 // written.  Every lane of the warp must call this (TMEM load).
-template <int D, int TP>
+template <int D, int TP, typename Tin>
 __device__ __forceinline__ void draft_outputs(const VerifyParams &p,
                                               const unsigned char *smb,
-                                              const Smem<D> &L, uint32_t ta,
+                                              const Smem<D, Tin> &L, uint32_t ta,
                                               int j, int grp, int ng, int T,
                                               int tok0, int h) {
   // x_t = D[t] + D[2TP + t] and y_t = D[TP + t] + D[3TP + t], read 8
@@ -456,7 +465,8 @@ __global__ void __launch_bounds__(2 * D, 2)
   const int i = blockIdx.y;
   const int tid = threadIdx.x;
   const int H = p.H;
-  const Smem<D> L(p.depth, p.max_T);
+  const Smem<D, Tin> L(p.depth, p.max_T);
+  typedef Rec<D, Tin> R;
   const int rg = tid & 3;
   const int j0 = 2 * (tid >> 2);
 
@@ -511,8 +521,8 @@ __global__ void __launch_bounds__(2 * D, 2)
     s_acc = okc ? acc : -1;
     if (spec && T > 0) umma::mbar_init(&s_mbar, 1);
   }
-  float *rep = reinterpret_cast<float *>(smb + L.rb);
-  float *drf = reinterpret_cast<float *>(smb + L.drf);
+  Tin *rep = reinterpret_cast<Tin *>(smb + L.rep);
+  Tin *drf = reinterpret_cast<Tin *>(smb + L.drf);
   {
     const size_t row = (size_t)tok0 * H + h;
     const Tin *tq = reinterpret_cast<const Tin *>(p.q);
@@ -554,10 +564,19 @@ __global__ void __launch_bounds__(2 * D, 2)
     }
   }
 
+  // The drafts' parts that do not depend on the state (decayed keys and
+  // queries, the B tile, the T x T pair dots) while the state's loads land.
+  int unsafe = 0;
+  if (drafts) {
+    unsafe = prep_tiles<D, TP, Tin>(smb, L, drf, T, tid);
+    unsafe = __syncthreads_or(unsafe);
+    prep_pairs<D, TP, Tin>(smb, L, drf, T, tid, unsafe);
+  }
+
   // Lazy commit: replay the accepted entries onto the state.
   float o0 = 0.f, o1 = 0.f;
   for (int t = 0; t < acc; ++t)
-    kda_step<D, false>(S, rep + t * Rec<D>::kStride, rg, j0, o0, o1);
+    kda_step<D, false, Tin>(S, rep + t * R::kStride, rg, j0, o0, o1);
 
   auto store_state = [&]() {
     ulonglong2 *c0 = reinterpret_cast<ulonglong2 *>(st + (size_t)j0 * D);
@@ -572,7 +591,7 @@ __global__ void __launch_bounds__(2 * D, 2)
   if (!spec) {
     // ordinary decode (or materialize): apply and commit
     for (int t = 0; t < T; ++t) {
-      kda_step<D, true>(S, drf + t * Rec<D>::kStride, rg, j0, o0, o1);
+      kda_step<D, true, Tin>(S, drf + t * R::kStride, rg, j0, o0, o1);
       if (rg == 0)
         *reinterpret_cast<float2 *>(p.o + ((size_t)(tok0 + t) * H + h) * D + j0) =
             make_float2(o0, o1);
@@ -604,12 +623,10 @@ __global__ void __launch_bounds__(2 * D, 2)
   constexpr int N1 = 4 * TP, N2 = 2 * TP, NK = D / 16;  // K steps of 16
   constexpr uint32_t kLoA = ((D + 63) / 64) * 16384;     // S_lo tile offset
   unsigned char *sa = smb + L.a;
-  __syncthreads();  // every replay read of the records is done (B reuses them)
   write_state_tiles<D>(sa, S, rg, j0);
-  int unsafe = prep_tiles<D, TP>(smb, L, drf, T, tid);
   umma::fence_smem_to_async();
   umma::fence_before_sync();
-  unsafe = __syncthreads_or(unsafe);
+  __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = s_tmem;
   const uint32_t a_base = umma::smem_u32(sa), b_base = umma::smem_u32(smb + L.rb);
@@ -625,10 +642,8 @@ __global__ void __launch_bounds__(2 * D, 2)
                      id2, 1u);
     umma::commit(&s_mbar);
   }
-  // overlapped with the MMAs: the committed state, pair dots, ring append,
-  // ring word
+  // overlapped with the MMAs: the committed state, ring append, ring word
   if (acc > 0) store_state();
-  prep_pairs<D, TP>(smb, L, drf, T, tid, unsafe);
   {
     constexpr int E = InVec<Tin>::kElems;
     constexpr int CH = D / E;
@@ -642,12 +657,13 @@ __global__ void __launch_bounds__(2 * D, 2)
       const int t = idx / (3 * CH);
       const int r = idx - t * 3 * CH;
       const int which = r / CH, ch = r - (r / CH) * CH;
-      const int off = which == 0 ? Rec<D>::kK : which == 1 ? Rec<D>::kA : Rec<D>::kV;
+      const int off = which == 0 ? R::kK : which == 1 ? R::kA : R::kV;
       Tin *dst = (which == 0 ? wk : which == 1 ? wa : wv) + (size_t)t * D + ch * E;
-      InVec<Tin>::store(dst, drf + t * Rec<D>::kStride + off + ch * E);
+      *reinterpret_cast<uint4 *>(dst) =
+          *reinterpret_cast<const uint4 *>(drf + t * R::kStride + off + ch * E);
     }
     if (tid - base >= 0 && tid - base < T)
-      out_scalar<Tin>(wb + (tid - base), drf[(tid - base) * Rec<D>::kStride + Rec<D>::kB]);
+      wb[tid - base] = drf[(tid - base) * R::kStride + R::kB];
     if (tid == base) {
       int32_t *c = p.ctrl + unit * 2;
       c[0] = T;
@@ -674,8 +690,8 @@ __global__ void __launch_bounds__(2 * D, 2)
     if (32 * q < D) {
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16);
       const int ng = D >= 64 ? D / 64 : 1;  // (2 D threads) / 128
-      draft_outputs<D, TP>(p, smb, L, ta, (q << 5) + (tid & 31), w >> 2, ng, T,
-                           tok0, h);
+      draft_outputs<D, TP, Tin>(p, smb, L, ta, (q << 5) + (tid & 31), w >> 2, ng, T,
+                                tok0, h);
     }
   }
   umma::fence_before_sync();
@@ -767,7 +783,8 @@ int resident_ctas(const void *kern, int threads, size_t dyn_smem) {
 
 template <int D, typename Tin>
 cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
-  const size_t smem = verify_smem_bytes(D, p.depth, p.max_T);
+  const size_t smem = verify_smem_bytes(D, p.depth, p.max_T,
+                                       sizeof(Tin) == 2 ? KDA_BF16 : KDA_F32);
   auto kern = p.max_T <= 8 ? verify_kernel<D, Tin, 8> : verify_kernel<D, Tin, 16>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(
@@ -793,14 +810,20 @@ cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
 
 }  // namespace
 
-size_t verify_smem_bytes(int D, int depth, int max_T) {
+size_t verify_smem_bytes(int D, int depth, int max_T, kda_dtype dt) {
+#define KDA_S(DD)                                                            \
+  case DD:                                                                   \
+    return dt == KDA_BF16 ? Smem<DD, __nv_bfloat16>(depth, max_T).total      \
+                          : Smem<DD, float>(depth, max_T).total;
   switch (D) {
-    case 16: return Smem<16>(depth, max_T).total;
-    case 32: return Smem<32>(depth, max_T).total;
-    case 64: return Smem<64>(depth, max_T).total;
-    case 128: return Smem<128>(depth, max_T).total;
-    default: return 0;
+    KDA_S(16)
+    KDA_S(32)
+    KDA_S(64)
+    KDA_S(128)
+    default:
+      return 0;
   }
+#undef KDA_S
 }
 
 int verify_max_spec_tokens() { return kTMax; }
