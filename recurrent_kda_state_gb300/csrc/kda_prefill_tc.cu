@@ -447,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ecm[c2] = __expf(gC0 - gm0);
         ecm[c2 + 1] = __expf(gC1 - gm1);
       }
-      float kt0[8], kt1[8], kh0[8], kh1[8];
+      // bf16 halves of K~ and K^ for channels (c2, c2 + 1) of the last 8
+      // rows: the transposed tiles take them as they are (byte permutes)
+      uint32_t ktH[8], ktL[8], khH[8], khL[8];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const int t = tb0 + u;
@@ -459,31 +461,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
         uint32_t hi, lo;
         uint32_t off = umma::sw128_off16(t, c2, 128);
-        umma::split_bf16x2(f0 * k0, f1 * k1, hi, lo);
-        *reinterpret_cast<uint32_t *>(sm + Lay::GA_HI + off) = hi;
-        *reinterpret_cast<uint32_t *>(sm + Lay::GA_LO + off) = lo;
+        umma::split_bf16x2(f0 * k0, f1 * k1, ktH[u & 7], ktL[u & 7]);
+        *reinterpret_cast<uint32_t *>(sm + Lay::GA_HI + off) = ktH[u & 7];
+        *reinterpret_cast<uint32_t *>(sm + Lay::GA_LO + off) = ktL[u & 7];
         off = umma::sw128_off16(64 + t, c2, 128);
         umma::split_bf16x2(f0 * q0, f1 * q1, hi, lo);
         *reinterpret_cast<uint32_t *>(sm + Lay::GA_HI + off) = hi;
         *reinterpret_cast<uint32_t *>(sm + Lay::GA_LO + off) = lo;
         off = umma::sw128_off16(t, c2, 64);
-        umma::split_bf16x2(fi0 * k0, fi1 * k1, hi, lo);
-        *reinterpret_cast<uint32_t *>(sm + Lay::GB_HI + off) = hi;
-        *reinterpret_cast<uint32_t *>(sm + Lay::GB_LO + off) = lo;
-        kt0[u & 7] = f0 * k0;
-        kt1[u & 7] = f1 * k1;
-        kh0[u & 7] = fi0 * k0;
-        kh1[u & 7] = fi1 * k1;
+        umma::split_bf16x2(fi0 * k0, fi1 * k1, khH[u & 7], khL[u & 7]);
+        *reinterpret_cast<uint32_t *>(sm + Lay::GB_HI + off) = khH[u & 7];
+        *reinterpret_cast<uint32_t *>(sm + Lay::GB_LO + off) = khL[u & 7];
         if ((u & 7) == 7) {
           const int tb = t - 7;
-          put8(sm, Lay::B2_HI + umma::sw128_off16(c2, tb, 128 + kNC),
-               Lay::B2_LO + umma::sw128_off16(c2, tb, 128), kt0);
-          put8(sm, Lay::B2_HI + umma::sw128_off16(c2 + 1, tb, 128 + kNC),
-               Lay::B2_LO + umma::sw128_off16(c2 + 1, tb, 128), kt1);
-          put8(sm, Lay::KH_HI + umma::sw128_off16(c2, tb, 128),
-               Lay::KH_LO + umma::sw128_off16(c2, tb, 128), kh0);
-          put8(sm, Lay::KH_HI + umma::sw128_off16(c2 + 1, tb, 128),
-               Lay::KH_LO + umma::sw128_off16(c2 + 1, tb, 128), kh1);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {  // row c2 + e: low (e = 0) or high halves
+            const uint32_t sel = e ? 0x7632u : 0x5410u;
+            const int row = c2 + e;
+            st_v4(sm, Lay::B2_HI + umma::sw128_off16(row, tb, 128 + kNC),
+                  __byte_perm(ktH[0], ktH[1], sel), __byte_perm(ktH[2], ktH[3], sel),
+                  __byte_perm(ktH[4], ktH[5], sel), __byte_perm(ktH[6], ktH[7], sel));
+            st_v4(sm, Lay::B2_LO + umma::sw128_off16(row, tb, 128),
+                  __byte_perm(ktL[0], ktL[1], sel), __byte_perm(ktL[2], ktL[3], sel),
+                  __byte_perm(ktL[4], ktL[5], sel), __byte_perm(ktL[6], ktL[7], sel));
+            st_v4(sm, Lay::KH_HI + umma::sw128_off16(row, tb, 128),
+                  __byte_perm(khH[0], khH[1], sel), __byte_perm(khH[2], khH[3], sel),
+                  __byte_perm(khH[4], khH[5], sel), __byte_perm(khH[6], khH[7], sel));
+            st_v4(sm, Lay::KH_LO + umma::sw128_off16(row, tb, 128),
+                  __byte_perm(khL[0], khL[1], sel), __byte_perm(khL[2], khL[3], sel),
+                  __byte_perm(khL[4], khL[5], sel), __byte_perm(khL[6], khL[7], sel));
+          }
         }
       }
     }
