@@ -556,9 +556,20 @@ __global__ void __launch_bounds__(2 * D, 2)
       for (int u = b + p.prefetch_stride; u < p.B * H; u += p.prefetch_stride) {
         const int su = p.state_slots[u / H];
         if (su >= 0 && su < p.P) {
-          const float *pu = p.pool + ((size_t)su * H + (u - (u / H) * H)) * D * D;
+          const size_t uu = (size_t)su * H + (u - (u / H) * H);
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                       :: "l"(pu), "r"(D * D * 4) : "memory");
+                       :: "l"(p.pool + uu * D * D), "r"(D * D * 4) : "memory");
+          // and its ring entries (k, alpha, v)
+          const uint32_t rbytes = (uint32_t)(p.depth * D * sizeof(Tin));
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                       :: "l"(reinterpret_cast<const Tin *>(p.rk) + uu * p.depth * D),
+                          "r"(rbytes) : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                       :: "l"(reinterpret_cast<const Tin *>(p.ra) + uu * p.depth * D),
+                          "r"(rbytes) : "memory");
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                       :: "l"(reinterpret_cast<const Tin *>(p.rv) + uu * p.depth * D),
+                          "r"(rbytes) : "memory");
         }
       }
     }
@@ -631,15 +642,18 @@ __global__ void __launch_bounds__(2 * D, 2)
   const uint32_t tmem = s_tmem;
   const uint32_t a_base = umma::smem_u32(sa), b_base = umma::smem_u32(smb + L.rb);
   if (tid == 0) {
+    // descriptors of later K steps differ only in the start address field
+    // (16-byte units)
     const uint32_t id1 = umma::idesc_bf16(128, N1), id2 = umma::idesc_bf16(128, N2);
+    const uint64_t da = umma::sdesc_sw128(a_base), db = umma::sdesc_sw128(b_base);
+#pragma unroll
     for (int s = 0; s < NK; ++s)
-      umma::mma_bf16(tmem, umma::sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32),
-                     umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
-                     id1, s > 0 ? 1u : 0u);
+      umma::mma_bf16(tmem, da + (((s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                     db + (((s >> 2) * N1 * 128 + (s & 3) * 32) >> 4), id1, s > 0 ? 1u : 0u);
+#pragma unroll
     for (int s = 0; s < NK; ++s)
-      umma::mma_bf16(tmem, umma::sdesc_sw128(a_base + kLoA + (s >> 2) * 16384 + (s & 3) * 32),
-                     umma::sdesc_sw128(b_base + (s >> 2) * N1 * 128 + (s & 3) * 32),
-                     id2, 1u);
+      umma::mma_bf16(tmem, da + ((kLoA + (s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                     db + (((s >> 2) * N1 * 128 + (s & 3) * 32) >> 4), id2, 1u);
     umma::commit(&s_mbar);
   }
   // overlapped with the MMAs: the committed state, ring append, ring word

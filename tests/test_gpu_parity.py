@@ -355,6 +355,14 @@ def test_prefill_slow_decay_carries_state():
                  alpha=lambda rng, shp: 1.0 - 0.03 * rng.random(shp))
 
 
+def test_prefill_d128_chunk64_fallback_heads():
+    """d=128, chunk 64 with a head count that is not a multiple of 8 takes
+    the CUDA-core kernels (the tensor-core kernel's beta map needs 16-byte
+    rows); same bar against the oracle."""
+    _run_prefill([200, 64, 1], [0, 64, 3], 4, 128, 64, 64, "bf16", 3,
+                 [0, 1, 2, 3], seed=913, s0_std=0.1)
+
+
 def test_prefill_tiny_dims_fp32():
     _run_prefill([64, 37, 5], [0, 16, 3], 2, 16, 16, 32, "f32", 2, [0, 1],
                  seed=5, s0_std=0.05)
