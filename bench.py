@@ -192,6 +192,29 @@ def oracle_spec_rate(seconds, heads_sampled=2, seed=ki.SEED_SPEC):
 
 
 # ----------------------------------------------------------- reference arm
+# ---------------------------------------------------------- replicas (N > 1)
+# The path has no exchange step: every rank runs an independent replica of
+# the workload (weak scaling).  These are the host-side pieces of that.
+def replica_rng(rank, seed=None):
+    """Each replica draws its own inputs from its own seeded stream."""
+    return np.random.default_rng((ki.SEED_SPEC if seed is None else seed) + 7919 * rank)
+
+
+def max_over_ranks(x, dist, device="cpu"):
+    """The largest value of x over the ranks (x itself without a group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens_per_rank, world, ms):
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -329,7 +352,7 @@ def run_kda(args, rank, world, local_rank):
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     touched = B * H * D * D * 4
     NL = max(1, math.ceil(4 * l2 / touched))
-    rng = np.random.default_rng(ki.SEED_SPEC + 7919 * rank)
+    rng = replica_rng(rank)
     slots_np = ki.slot_table(rng, B, P)
     slots = torch.as_tensor(slots_np, device=dev)
     pools = [K.StatePool.zeros(P, H, D, device=dev) for _ in range(NL)]
@@ -401,12 +424,8 @@ def run_kda(args, rank, world, local_rank):
     w1 = time.time()
     barrier()
     clocks.stop()
-    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     bits = K.kda_get_device_error()
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     # per-launch verify durations over the timed region
     durs, abytes = [], []
     for s in range(args.warmup, total_steps):
@@ -419,8 +438,8 @@ def run_kda(args, rank, world, local_rank):
     mean_dur_s = float(np.mean(durs)) * 1e-3
     achieved = float(np.mean(abytes)) / mean_dur_s / 1e9
     peak, peak_kind = load_peaks()
-    tokens = B * T * args.steps * NL * world
-    value = tokens / (ms * 1e-3)
+    tokens_rank = B * T * args.steps * NL
+    value = job_rate(tokens_rank, world, ms)
 
     # end to end: inputs from pinned host memory, outputs back, same graphs
     host_in = [sets[g][0].cpu().pin_memory() for g in range(G)]
@@ -441,11 +460,7 @@ def run_kda(args, rank, world, local_rank):
             host_out.copy_(outs[s % G], non_blocking=True)
         f1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = f0.elapsed_time(f1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1), dist, dev)
 
     prefill = run_prefill(torch, K, dev)
     cpu = None
@@ -479,7 +494,7 @@ def run_kda(args, rank, world, local_rank):
                      "mean_launch_us": mean_dur_s * 1e6,
                      "alg_bytes_per_launch": float(np.mean(abytes))},
         "cpu_baseline": cpu,
-        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (NL + 1) * args.steps,
         "clocks": clocks.summary(w0, w1),
