@@ -309,8 +309,8 @@ def run_prefill(torch, K, dev):
     pool.data[0].copy_(torch.from_numpy(np.swapaxes(init[0], -1, -2).copy()))
     slots = torch.tensor([0], dtype=torch.int32, device=dev)
     ck = torch.arange(1, 1 + L // E, dtype=torch.int32, device=dev).view(1, -1)
-    ws_bytes = K.kda_prefill_workspace_size(L, 1, H, D, D, C)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws_bytes = K.kda_prefill_workspace_size(L, 1, H, D, D, C, K.KDA_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     stream = torch.cuda.current_stream()
     for _ in range(3):
         K.kda_prefill_chunked(tb, pool, slots, C, E, ck, workspace=ws)
@@ -335,8 +335,8 @@ def run_prefill(torch, K, dev):
         "workspace_bytes": ws_bytes,
         "note": "one tcgen05 kernel: chunk (WY/UT) form per (32-column value "
                 "slice, head, sequence), bf16 hi/lo operands (three kind::f16 "
-                "MMAs per product), fp32 state in registers; the workspace "
-                "argument is not used at this shape",
+                "MMAs per product), fp32 state in registers; no workspace "
+                "at this shape",
         "tensor_pipe": prefill_tensor_profile(),
     }
 

@@ -145,7 +145,9 @@ typedef struct {
  * dropped.  ckpt_every == 0 disables checkpoints (ckpt_slots may be NULL).
  * Requirements: chunk in {16, 32, 64}; ckpt_every % chunk == 0; workspace of
  * at least kda_prefill_workspace_size(...) bytes, 256-byte aligned, owned by
- * the caller and not used by another call until this one completes.
+ * the caller and not used by another call until this one completes.  When
+ * that size is 0 (bf16 inputs at d_k = d_v = 128, chunk 64, heads a multiple
+ * of 8: the tensor-core kernel) the workspace is not used and may be NULL.
  * The target slots must have no pending commit (see kda_materialize).
  */
 int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
@@ -154,11 +156,13 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
                         const int32_t *start_pos, void *workspace,
                         size_t workspace_bytes, kda_stream_t stream);
 
-/* Bytes of workspace kda_prefill_chunked needs for these sizes (0 on bad
- * arguments). */
+/* Bytes of workspace kda_prefill_chunked needs for these sizes and input
+ * dtype: 0 when it needs none (bf16 inputs at d_k = d_v = 128, chunk 64,
+ * heads a multiple of 8), and 0 on bad arguments (which the prefill call
+ * itself rejects). */
 size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
                                   int32_t num_heads, int32_t d_k, int32_t d_v,
-                                  int32_t chunk);
+                                  int32_t chunk, kda_dtype dtype);
 
 /*
  * kda_prefill_chunked_noalloc -- kda_prefill_chunked for callers that cannot
@@ -176,8 +180,9 @@ size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
  * Arguments, outputs and semantics are those of kda_prefill_chunked; the
  * caller still passes inputs, outputs, pool and slot tables.
  *   - Returns KDA_ENOSPC, before any CUDA call, when
- *     kda_prefill_workspace_size(...) for these sizes exceeds
- *     KDA_NOALLOC_SCRATCH_BYTES.
+ *     kda_prefill_workspace_size(...) for these sizes and dtype exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES; shapes that need no workspace run without
+ *     touching the array.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one array and it keeps the last call's contents

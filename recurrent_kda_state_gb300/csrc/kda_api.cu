@@ -116,10 +116,12 @@ const char *kda_status_string(int status) {
 
 size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
                                   int32_t num_heads, int32_t d_k, int32_t d_v,
-                                  int32_t chunk) {
+                                  int32_t chunk, kda_dtype dtype) {
   if (num_tokens < 0 || num_seqs < 0 || num_heads < 1 || d_k != d_v ||
-      !dim_ok(d_k) || (chunk != 16 && chunk != 32 && chunk != 64))
+      !dim_ok(d_k) || (chunk != 16 && chunk != 32 && chunk != 64) ||
+      (dtype != KDA_F32 && dtype != KDA_BF16))
     return 0;
+  if (kda::prefill_uses_tc(dtype, num_heads, d_k, d_v, chunk)) return 0;
   return kda::prefill_workspace_bytes(num_tokens, num_seqs, num_heads, d_k, chunk);
 }
 
@@ -136,11 +138,15 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
   if (ckpt_every > 0 && ckpt_every % chunk != 0) return KDA_EINVAL;
   if (ckpt_every > 0 && max_ckpt > 0 && !ckpt_slots) return KDA_EINVAL;
   if (tok->num_seqs == 0) return KDA_OK;
-  if (!state_slots || !workspace) return KDA_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return KDA_EALIGN;
-  const size_t need = kda::prefill_workspace_bytes(
-      tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, chunk);
-  if (workspace_bytes < need) return KDA_ENOSPC;
+  if (!state_slots) return KDA_EINVAL;
+  const bool tc = kda::prefill_uses_tc(tok->dtype, tok->num_heads, tok->d_k, tok->d_v, chunk);
+  if (!tc) {  // the CUDA-core kernels work in the caller's workspace
+    if (!workspace) return KDA_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return KDA_EALIGN;
+    const size_t need = kda::prefill_workspace_bytes(
+        tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, chunk);
+    if (workspace_bytes < need) return KDA_ENOSPC;
+  }
   if ((long long)tok->num_tokens / chunk + 2LL * tok->num_seqs > 0x7fffffffLL)
     return KDA_ESHAPE;
   unsigned *err = device_error_word();

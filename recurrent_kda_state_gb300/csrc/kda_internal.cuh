@@ -140,6 +140,13 @@ __host__ __device__ inline size_t prefill_entry_floats(int D, int C) {
 __host__ __device__ inline int prefill_max_chunks(int N, int B, int C) {
   return N / C + 2 * B;
 }
+// The tensor-core prefill (no workspace) takes bf16 inputs at d_k = d_v = 128,
+// chunk 64, with a head count that is a multiple of 8; other shapes run the
+// CUDA-core kernels on the caller's workspace.
+__host__ __device__ inline bool prefill_uses_tc(int dtype, int H, int d_k, int d_v,
+                                                int C) {
+  return dtype == KDA_BF16 && d_k == 128 && d_v == 128 && C == 64 && H % 8 == 0;
+}
 __host__ __device__ inline size_t prefill_workspace_bytes(int N, int B, int H,
                                                           int D, int C) {
   return prefill_table_bytes(B) + (size_t)prefill_max_chunks(N, B, C) * H *

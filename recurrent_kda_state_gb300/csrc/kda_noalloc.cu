@@ -42,8 +42,13 @@ extern "C" int kda_prefill_chunked_noalloc(const kda_tokens *tok,
   if (!tok || !pool) return KDA_EINVAL;
   if (tok->num_seqs == 0) return KDA_OK;
   const size_t need = kda_prefill_workspace_size(
-      tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, tok->d_v, chunk);
-  if (need == 0) return KDA_EINVAL;
+      tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, tok->d_v, chunk,
+      tok->dtype);
+  // 0: no scratch needed (tensor-core shape) or bad arguments, which
+  // kda_prefill_chunked reports itself
+  if (need == 0)
+    return kda_prefill_chunked(tok, pool, state_slots, ckpt_slots, max_ckpt,
+                               ckpt_every, chunk, start_pos, nullptr, 0, stream);
   if (need > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ENOSPC;
   unsigned char *ws = scratch_address();
   if (!ws) return KDA_ECUDA;

@@ -503,7 +503,7 @@ cudaError_t launch_prefill_c(const PrefillParams &p, int C, cudaStream_t s) {
 cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,
                            cudaStream_t s) {
   if (p.B == 0) return cudaSuccess;
-  if (D == 128 && C == 64 && dt == KDA_BF16 && p.H % 8 == 0) return launch_prefill_tc(p, s);
+  if (prefill_uses_tc(dt, p.H, D, D, C)) return launch_prefill_tc(p, s);
 #define KDA_P(DD)                                                            \
   case DD:                                                                   \
     return dt == KDA_BF16 ? launch_prefill_c<DD, __nv_bfloat16>(p, C, s)     \

@@ -64,7 +64,7 @@ def lib():
                                           _P, ctypes.c_size_t, _P]
         L.kda_prefill_chunked_noalloc.argtypes = [tp, pp, _P, _P, _I32, _I32,
                                                   _I32, _P, _P]
-        L.kda_prefill_workspace_size.argtypes = [_I32] * 6
+        L.kda_prefill_workspace_size.argtypes = [_I32] * 6 + [ctypes.c_int]
         L.kda_prefill_workspace_size.restype = ctypes.c_size_t
         L.kda_verify.argtypes = [tp, _I32, pp, _P, rp, _P, _P]
         L.kda_commit.argtypes = [_P, _P, _I32, pp, rp, _P]
@@ -163,9 +163,11 @@ class TokenBatch:
                             cu_seqlens.numel() - 1, N, H, dk, dv)
 
 
-def kda_prefill_workspace_size(num_tokens, num_seqs, H, d_k, d_v, chunk):
+def kda_prefill_workspace_size(num_tokens, num_seqs, H, d_k, d_v, chunk, dtype):
+    """Workspace bytes for these sizes and input dtype (KDA_F32 / KDA_BF16);
+    0 when the call needs none."""
     return int(lib().kda_prefill_workspace_size(num_tokens, num_seqs, H, d_k,
-                                                d_v, chunk))
+                                                d_v, chunk, dtype))
 
 
 def kda_prefill_chunked(tok, pool, state_slots, chunk, ckpt_every=0,
@@ -176,14 +178,14 @@ def kda_prefill_chunked(tok, pool, state_slots, chunk, ckpt_every=0,
     if workspace is None:
         nbytes = kda_prefill_workspace_size(tok.c.num_tokens, tok.c.num_seqs,
                                             tok.c.num_heads, tok.c.d_k,
-                                            tok.c.d_v, chunk)
-        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8,
-                                device=tok.k.device)
+                                            tok.c.d_v, chunk, tok.c.dtype)
+        if nbytes > 0:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=tok.k.device)
     _check(lib().kda_prefill_chunked(
         ctypes.byref(tok.c), ctypes.byref(pool.c), _ptr(state_slots),
         _ptr(ckpt_slots), max_ckpt, ckpt_every, chunk, _ptr(start_pos),
-        _ptr(workspace), workspace.numel(), _stream(stream)),
-        "kda_prefill_chunked")
+        _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)), "kda_prefill_chunked")
     return workspace
 
 

@@ -81,7 +81,7 @@ def test_prefill_validation(L):
     by = ctypes.byref
     s = ctypes.c_void_p(0x40000)
     ws = ctypes.c_void_p(0x100000)
-    need = L.kda_prefill_workspace_size(4, 1, 2, 16, 16, 16)
+    need = L.kda_prefill_workspace_size(4, 1, 2, 16, 16, 16, kda.KDA_F32)
     assert need > 0
     # chunk not supported
     assert L.kda_prefill_chunked(by(tok), by(pool), s, None, 0, 0, 24, None, ws,
@@ -95,7 +95,10 @@ def test_prefill_validation(L):
     assert L.kda_prefill_chunked(by(tok), by(pool), s, None, 0, 0, 16, None,
                                  ctypes.c_void_p(0x100010), need,
                                  None) == kda.KDA_EALIGN
-    assert L.kda_prefill_workspace_size(4, 1, 2, 16, 16, 24) == 0
+    assert L.kda_prefill_workspace_size(4, 1, 2, 16, 16, 24, kda.KDA_F32) == 0
+    # no workspace at all is refused where one is needed
+    assert L.kda_prefill_chunked(by(tok), by(pool), s, None, 0, 0, 16, None, None,
+                                 0, None) == kda.KDA_EINVAL
 
 
 def test_workspace_size_formula(L):
@@ -104,7 +107,14 @@ def test_workspace_size_formula(L):
     N, B, H, D, C = 8192, 1, 32, 128, 64
     entry = (4 * C * D + C * C + D + 63) // 64 * 64
     want = 256 + (N // C + 2 * B) * H * entry * 4
-    assert L.kda_prefill_workspace_size(N, B, H, D, D, C) == want
+    assert L.kda_prefill_workspace_size(N, B, H, D, D, C, kda.KDA_F32) == want
+    # bf16 at d=128, chunk 64, heads a multiple of 8: the tensor-core kernel
+    # needs no workspace; other bf16 shapes follow the formula
+    assert L.kda_prefill_workspace_size(N, B, H, D, D, C, kda.KDA_BF16) == 0
+    assert L.kda_prefill_workspace_size(N, B, 4, D, D, C, kda.KDA_BF16) == \
+        256 + (N // C + 2 * B) * 4 * entry * 4
+    assert L.kda_prefill_workspace_size(N, B, H, D, D, 32, kda.KDA_BF16) > 0
+    assert L.kda_prefill_workspace_size(N, B, H, D, D, C, 7) == 0
 
 
 def test_commit_and_slot_validation(L):

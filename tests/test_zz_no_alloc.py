@@ -57,6 +57,7 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
     cases = [
         (501, [200, 77], [0, 5], 8, 128, 64, 128, 2),
         (502, [130, 1, 64], [64, 3, 0], 2, 64, 32, 64, 3),
+        (503, [200, 77], [0, 5], 4, 128, 64, 128, 2),  # d=128, 4 heads: scratch
     ]
     for seed, lengths, starts, H, d, C, E, mc in cases:
         (o_ref, s_ref), (o_na, s_na) = _prefill_pair(seed, lengths, starts, H, d,
@@ -67,9 +68,9 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
-    H, d, C = 32, 128, 64
-    N = 8192  # needs ~600 MB of workspace, far above the fixed scratch
-    need = K.kda_prefill_workspace_size(N, 1, H, d, d, C)
+    H, d, C = 32, 64, 64  # d=64: the CUDA-core kernels, which need a workspace
+    N = 8192  # needs ~340 MB of workspace, far above the fixed scratch
+    need = K.kda_prefill_workspace_size(N, 1, H, d, d, C, K.KDA_BF16)
     assert need > K.KDA_NOALLOC_SCRATCH_BYTES
     z = torch.zeros(N, H, d, dtype=torch.bfloat16, device="cuda")
     tb = K.TokenBatch(z, z, z, z, torch.zeros(N, H, dtype=torch.bfloat16,
