@@ -230,10 +230,10 @@ __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t off) {
   return d + (off >> 4);
 }
 
-// Thread 0 waits for the last commit (bounded); every thread learns whether
+// Every thread waits for the barrier's phase (bounded); they agree whether
 // it completed.  On success the phase advances.
 __device__ __forceinline__ bool tc_wait(uint64_t *mbar, uint32_t &phase, int tid) {
-  const bool ok = tid == 0 ? umma::mbar_wait(mbar, phase, kSpin) : true;
+  const bool ok = umma::mbar_wait(mbar, phase, kSpin);
   const bool all = __syncthreads_and(ok) != 0;
   if (all) phase ^= 1u;
   umma::fence_after_sync();
