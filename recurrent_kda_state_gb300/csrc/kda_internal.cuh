@@ -22,9 +22,6 @@ struct InVec<float> {
     const float4 a = *reinterpret_cast<const float4 *>(p);
     dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
   }
-  __device__ __forceinline__ static void store(float *p, const float *src) {
-    *reinterpret_cast<float4 *>(p) = make_float4(src[0], src[1], src[2], src[3]);
-  }
 };
 
 template <>
@@ -39,15 +36,6 @@ struct InVec<__nv_bfloat16> {
       dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
   }
-  // Exact for values that came from bf16 (the ring stores copies of inputs).
-  __device__ __forceinline__ static void store(__nv_bfloat16 *p, const float *src) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      w[i] = (__float_as_uint(src[2 * i]) >> 16) |
-             (__float_as_uint(src[2 * i + 1]) & 0xffff0000u);
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
 };
 
 template <typename Tin>
@@ -58,15 +46,6 @@ template <>
 __device__ __forceinline__ float in_scalar<__nv_bfloat16>(const __nv_bfloat16 *p) {
   return __bfloat162float(*p);
 }
-template <typename Tin>
-__device__ __forceinline__ void out_scalar(Tin *p, float x);
-template <>
-__device__ __forceinline__ void out_scalar<float>(float *p, float x) { *p = x; }
-template <>
-__device__ __forceinline__ void out_scalar<__nv_bfloat16>(__nv_bfloat16 *p, float x) {
-  *reinterpret_cast<uint16_t *>(p) = (uint16_t)(__float_as_uint(x) >> 16);
-}
-
 __device__ __forceinline__ void set_error(unsigned int *err, unsigned int bit) {
   atomicOr(err, bit);
 }

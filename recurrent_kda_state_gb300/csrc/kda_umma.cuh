@@ -3,8 +3,8 @@
 // memory (TMEM), completion through an mbarrier.
 //
 // Operand layout used everywhere in this library: "K-major, 128-byte swizzle".
-// A tile of R rows (R a multiple of 8) and K fp32/tf32 columns is stored as
-// K/32 blocks of R x 128 bytes; inside a block, row r occupies 128 bytes at
+// A tile of R rows (R a multiple of 8) and K bf16 columns is stored as K/64
+// blocks of R x 128 bytes; inside a block, row r occupies 128 bytes at
 // (r / 8) * 1024 + (r % 8) * 128 and its 16-byte chunk c sits at chunk
 // position c ^ (r % 8).  Tiles must start on a 1024-byte boundary.
 #pragma once
@@ -17,15 +17,6 @@ namespace umma {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Byte offset of element (row, k) of a K-major SW128 tile with `rows` rows.
-__host__ __device__ __forceinline__ uint32_t sw128_off(int row, int k, int rows) {
-  const int kb = k >> 5, kin = k & 31;
-  const int chunk = kin >> 2, within = kin & 3;
-  const int r8 = row & 7;
-  return (uint32_t)(kb * rows * 128 + (row >> 3) * 1024 + r8 * 128 +
-                    ((chunk ^ r8) << 4) + within * 4);
 }
 
 // Shared-memory matrix descriptor: start address, leading byte offset (unused
@@ -41,25 +32,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor: kind::tf32, fp32 accumulator, A and B K-major.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-// D (TMEM) (+)= A * B^T for one K = 8 step; A is M x 8, B is N x 8 (tf32).
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t da,
-                                         uint64_t db, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
-}
-
 // Byte offset of element (row, k) of a K-major SW128 tile of 16-bit elements
 // with `rows` rows: K/64 blocks of rows x 128 bytes, 8 elements per 16-byte
-// chunk, same row/chunk swizzle as the fp32 tiles.
+// chunk, swizzled as above.
 __host__ __device__ __forceinline__ uint32_t sw128_off16(int row, int k, int rows) {
   const int kb = k >> 6, kin = k & 63;
   const int chunk = kin >> 3, within = kin & 7;
@@ -173,19 +148,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 8 consecutive TMEM columns of this thread's lane -> registers.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-        "=r"(r[6]), "=r"(r[7])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // 8 consecutive TMEM columns -> registers without waiting; the values are
 // valid only after tmem_wait_ld().
 __device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t (&r)[8]) {
@@ -197,11 +159,6 @@ __device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// tf32 part of an fp32 value (low 13 mantissa bits cleared), exact.
-__device__ __forceinline__ float tf32_hi(float x) {
-  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
 }  // namespace umma
