@@ -13,9 +13,10 @@ B * T * NL * steps / time.  Each step is one CUDA graph captured from the
 public API calls, with timing events around every verify launch.
 
 Extra keys: `roofline` (verify kernel vs HBM), `cpu_baseline` (the fp64
-oracle on the host cores, bounded sample), `e2e` (same metric with the
-step's inputs copied from pinned host memory and outputs copied back inside
-the timed region), `prefill` (chunked prefill with in-pass checkpoints,
+oracle on the host cores, bounded sample), `e2e` (same metric with every
+step's inputs copied from pinned host memory and its outputs copied back
+inside the timed region, the copies of neighbouring steps overlapping the
+compute on their own streams), `prefill` (chunked prefill with in-pass checkpoints,
 1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region),
 `clocks` (nvidia-smi samples during the timed region).
 
@@ -447,18 +448,46 @@ def run_kda(args, rank, world, local_rank):
     host_out = torch.empty(outs.shape[1:], dtype=torch.float32).pin_memory()
     h2d = sets[0][0].numel() * 2 + B * 4
     d2h = host_out.numel() * 4
-    barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for s in range(args.warmup, total_steps):
+    # Pipelined as a serving loop would run it: one stream copies step s+1's
+    # inputs in while step s computes, another reads step s's outputs back;
+    # events keep each of the G input sets and output buffers from being
+    # overwritten while in use.  Every step's copies are in the timed region.
+    h2d_s = torch.cuda.Stream(device=dev)
+    d2h_s = torch.cuda.Stream(device=dev)
+    first = args.warmup
+    ev_in, ev_cmp, ev_out = {}, {}, {}
+
+    def issue_h2d(s):
+        with torch.cuda.stream(h2d_s):
+            if s - G >= first:
+                h2d_s.wait_event(ev_cmp[s - G])   # input set s % G is free
             sets[s % G][0].copy_(host_in[s % G], non_blocking=True)
             acc[s % A].copy_(host_acc[s % A], non_blocking=True)
+            ev_in[s] = torch.cuda.Event()
+            ev_in[s].record(h2d_s)
+
+    barrier()
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(h2d_s)
+    issue_h2d(first)
+    for s in range(first, total_steps):
+        if s + 1 < total_steps:
+            issue_h2d(s + 1)
+        stream.wait_event(ev_in[s])
+        if s - G >= first:
+            stream.wait_event(ev_out[s - G])      # output buffer s % G read back
+        with torch.cuda.stream(stream):
             graphs[s].replay()
+        ev_cmp[s] = torch.cuda.Event()
+        ev_cmp[s].record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(ev_cmp[s])
             host_out.copy_(outs[s % G], non_blocking=True)
-        f1.record(stream)
+            ev_out[s] = torch.cuda.Event()
+            ev_out[s].record(d2h_s)
+    f1.record(d2h_s)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dist, dev)
 
