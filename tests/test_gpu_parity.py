@@ -111,6 +111,34 @@ def test_spec_verify_fp32_small_dims():
                   seed=77 + d)
 
 
+def test_spec_verify_ragged_drafts_depth16():
+    """Ring depth 16 and up to 16 drafted tokens (the 16-row draft tiles), with
+    ragged draft counts per sequence (including 0 and 1); accepted lengths
+    up to each sequence's own count; d=128, bf16, all heads followed."""
+    rng = np.random.default_rng(916)
+    B, H, d, P, D16 = 6, 8, 128, 12, 16
+    slots_np = ki.slot_table(rng, B, P)
+    slots = i32(slots_np)
+    pool = K.StatePool.zeros(P, H, d)
+    ring = K.ReplayRing(P, H, d, D16, torch.bfloat16)
+    sess = oracle.OracleSession(P, H, d, d)
+    hs = list(range(H))
+    for step in range(5):
+        lens = [16, 0, 5, 9, 1, 12] if step % 2 == 0 else [3, 16, 0, 8, 11, 2]
+        tok = ki.round_to(ki.gen_tokens(rng, lens, H, d), "bf16")
+        a = np.array([rng.integers(0, n + 1) for n in lens], dtype=np.int32)
+        tb = device_batch(tok, "bf16")
+        K.kda_verify(tb, D16, pool, slots, ring)
+        K.kda_commit(i32(a), slots, pool, ring)
+        o_ref = sess.verify(tok, slots_np)
+        sess.commit(a, slots_np)
+        assert_outputs(tb.o.cpu().numpy(), o_ref)
+    K.kda_materialize(slots, pool, ring)
+    for s_ in slots_np:
+        assert_states(from_gpu_states(pool.data[s_]), sess.pool[s_])
+    assert K.kda_get_device_error() == 0
+
+
 # ------------------------------------------------------ bit-exact replay
 def _random_pool(rng, P, H, d, std=0.3):
     return K.StatePool(to_gpu_states(
