@@ -18,7 +18,11 @@ step's inputs copied from pinned host memory and its outputs copied back
 inside the timed region, the copies of neighbouring steps overlapping the
 compute on their own streams), `prefill` (chunked prefill with in-pass checkpoints,
 1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region),
-`clocks` (nvidia-smi samples during the timed region).
+`clocks` (nvidia-smi samples during the timed region),
+`ablation_direct_snapshots` (the design ReplaySSM replaces -- the state
+stored at every drafted position, the accepted one copied at commit -- on the
+same workload, its own timed region; with both designs' algorithmic bytes
+per step and state-cache bytes per sequence at a 46.48 GiB budget).
 
 `--impl reference` times the oracle itself on the host cores on the same
 workload (rank 0 only).
@@ -342,6 +346,105 @@ def run_prefill(torch, K, dev):
     }
 
 
+CACHE_BUDGET_GIB = 46.48   # the pages' KV/state cache budget for the comparison
+
+
+def state_cache_bytes(d=D, h=H, t=T, depth=DEPTH):
+    """Per-sequence state-cache bytes of one KDA layer in each design: the
+    committed state plus, for ReplaySSM, the ring (k, alpha, v bf16 + beta
+    per entry, and the control pair), for direct snapshots, T more states."""
+    state = h * d * d * 4
+    ring = h * depth * (3 * d * 2 + 2) + h * 2 * 4
+    return {"replay_ssm": state + ring, "direct_snapshots": state * (1 + t)}
+
+
+def snapshot_unit_bytes(a, d=D, t=T):
+    """Algorithmic HBM bytes of one (sequence, head) unit of one step of the
+    direct design: verify reads the state and the T drafted tokens' inputs,
+    writes T outputs and T state snapshots; the commit copies snapshot a - 1
+    into the pool when a > 0; slot and accepted-length words."""
+    verify = d * d * 4 + t * (4 * d * 2 + 2) + t * d * 4 + t * d * d * 4 + 4
+    commit = 2 * d * d * 4 * (a > 0) + 8
+    return verify, commit
+
+
+def run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np, G, A,
+                          steps=64, warmup=4):
+    """The direct per-position snapshot design on the same workload: per step
+    kda_verify_snapshot on each of NL layers, then kda_commit_snapshot of the
+    step's accepted lengths on each layer.  Own pools (zero), own timed
+    region, CUDA events around every launch."""
+    pools = [K.StatePool.zeros(P, H, D, device=dev) for _ in range(NL)]
+    snaps = [K.snapshot_buffer(B, T, pools[l]) for l in range(NL)]
+    stream = torch.cuda.Stream(device=dev)
+    graphs, events = [], []
+    with torch.cuda.stream(stream):
+        for s in range(warmup + steps):
+            g = torch.cuda.CUDAGraph()
+            ev = [[torch.cuda.Event(enable_timing=True, external=True)
+                   for _ in range(4)] for _ in range(NL)] if s >= warmup else None
+            g.capture_begin()
+            for l in range(NL):
+                if ev:
+                    ev[l][0].record(stream)
+                K.kda_verify_snapshot(batches[s % G][l], T, pools[l], slots,
+                                      snaps[l], stream=stream)
+                if ev:
+                    ev[l][1].record(stream)
+            for l in range(NL):
+                if ev:
+                    ev[l][2].record(stream)
+                K.kda_commit_snapshot(acc[s % A], slots, pools[l], snaps[l],
+                                      stream=stream)
+                if ev:
+                    ev[l][3].record(stream)
+            g.capture_end()
+            graphs.append(g)
+            events.append(ev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(warmup):
+            graphs[s].replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for s in range(warmup, warmup + steps):
+            graphs[s].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    bits = K.kda_get_device_error()
+    v_us, c_us, v_bytes, c_bytes = [], [], [], []
+    for s in range(warmup, warmup + steps):
+        per = [snapshot_unit_bytes(int(x)) for x in acc_np[s % A]]
+        vb = float(sum(p[0] for p in per) * H)
+        cb = float(sum(p[1] for p in per) * H)
+        for l in range(NL):
+            ev = events[s][l]
+            v_us.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            c_us.append(ev[2].elapsed_time(ev[3]) * 1e3)
+            v_bytes.append(vb)
+            c_bytes.append(cb)
+    del graphs, snaps, pools
+    torch.cuda.empty_cache()
+    v_mean, c_mean = float(np.mean(v_us)), float(np.mean(c_us))
+    return {
+        "value": B * T * steps * NL / (ms * 1e-3), "unit": "tokens/s",
+        "ms_per_step": ms / steps, "steps": steps, "warmup": warmup,
+        "kda_layers": NL,
+        "verify_launch_us": v_mean, "commit_launch_us": c_mean,
+        "alg_bytes_per_layer_step": float(np.mean(v_bytes) + np.mean(c_bytes)),
+        "verify_achieved_gbs": float(np.mean(v_bytes)) / (v_mean * 1e-6) / 1e9,
+        "commit_achieved_gbs": float(np.mean(c_bytes)) / (c_mean * 1e-6) / 1e9,
+        "device_error_bits": bits,
+        "note": "direct design: T state snapshots written per (sequence, head) "
+                "per step, the accepted one copied into the pool; same inputs, "
+                "slots and accepted lengths as the main line",
+    }
+
+
 def run_kda(args, rank, world, local_rank):
     import torch
     from recurrent_kda_state_gb300 import kda as K
@@ -492,6 +595,19 @@ def run_kda(args, rank, world, local_rank):
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dist, dev)
 
     prefill = run_prefill(torch, K, dev)
+    direct = run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np,
+                                   G, A)
+    cache = state_cache_bytes()
+    budget = CACHE_BUDGET_GIB * 2 ** 30
+    replay_step_bytes = float(np.mean(abytes)) + B * H * 8
+    direct.update({
+        "replay_alg_bytes_per_layer_step": replay_step_bytes,
+        "replay_ms_per_step": ms / args.steps,
+        "replay_speedup": direct["ms_per_step"] / (ms / args.steps),
+        "state_cache_bytes_per_seq_layer": cache,
+        "seqs_per_layer_at_budget": {k: int(budget // v) for k, v in cache.items()},
+        "cache_budget_gib": CACHE_BUDGET_GIB,
+    })
     cpu = None
     if rank == 0:
         rate, cores, desc, _ = oracle_spec_rate(args.cpu_seconds)
@@ -529,6 +645,7 @@ def run_kda(args, rank, world, local_rank):
         "clocks": clocks.summary(w0, w1),
         "device_error_bits": bits,
         "prefill": prefill,
+        "ablation_direct_snapshots": direct,
     }
     print(json.dumps(line), flush=True)
 

@@ -271,6 +271,39 @@ int kda_gather_states(const kda_state_pool *pool, const int32_t *slots,
 int kda_copy_slots(kda_state_pool *pool, const int32_t *src,
                    const int32_t *dst, int32_t n, kda_stream_t stream);
 
+/*
+ * kda_verify_snapshot -- the direct design that ReplaySSM replaces, kept as
+ * an ablation baseline ("ReplaySSM shrinks rollback state": storing the
+ * state at every drafted position costs T state writes per step).
+ *
+ * For every sequence i and head h, with slot s = state_slots[i] and the
+ * segment's T_i <= max_T <= 16 drafted tokens: the state of (s, h) is
+ * advanced token by token, o receives each token's output, and the state
+ * after drafted token t (0-based) is written to snapshot (i, t):
+ *   snapshots: device fp32 [num_seqs][max_T][H][d_v][d_k] (each snapshot in
+ *   the pool's per-slot layout), owned by the caller; entries t >= T_i are
+ *   not written.
+ * The pool is only read.  Snapshot (i, t) holds the same bits as the state
+ * that a ReplaySSM commit of t + 1 tokens rebuilds from the same state and
+ * inputs.  The slots must have no pending ReplaySSM commit.  A segment
+ * longer than max_T sets KDA_DERR_DEPTH and skips the sequence.
+ */
+int kda_verify_snapshot(const kda_tokens *tok, int32_t max_T,
+                        const kda_state_pool *pool, const int32_t *state_slots,
+                        float *snapshots, kda_stream_t stream);
+
+/*
+ * kda_commit_snapshot -- commit of the direct design: for every sequence i
+ * with a = accepted_len[i] > 0 (device), every head of pool[state_slots[i]]
+ * receives snapshot (i, a - 1) of the preceding kda_verify_snapshot (same
+ * max_T); a == 0 leaves the state untouched.  a must not exceed that
+ * verify's T_i; a < 0 or a > max_T sets KDA_DERR_ACCEPT and skips the row.
+ */
+int kda_commit_snapshot(const int32_t *accepted_len, const int32_t *state_slots,
+                        int32_t num_seqs, kda_state_pool *pool,
+                        const float *snapshots, int32_t max_T,
+                        kda_stream_t stream);
+
 /* kda_get_device_error -- synchronize `stream`, read the device error word
  * of the current device into *host_bits (host pointer), clear it, and return
  * KDA_EDEVICE if any bit was set, else KDA_OK. */

@@ -329,6 +329,66 @@ int kda_copy_slots(kda_state_pool *pool, const int32_t *src, const int32_t *dst,
   return cuda_status(kda::launch_slot_copy(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int kda_verify_snapshot(const kda_tokens *tok, int32_t max_T,
+                        const kda_state_pool *pool, const int32_t *state_slots,
+                        float *snapshots, kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if ((st = check_tokens(tok, pool))) return st;
+  if (max_T < 1 || max_T > kda::verify_max_spec_tokens()) return KDA_EINVAL;
+  if (tok->num_seqs == 0) return KDA_OK;
+  if (!state_slots || !snapshots) return KDA_EINVAL;
+  if (!aligned16(snapshots)) return KDA_EALIGN;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::SnapshotParams p = {};
+  p.q = tok->q;
+  p.k = tok->k;
+  p.v = tok->v;
+  p.alpha = tok->alpha;
+  p.beta = tok->beta;
+  p.o = tok->o;
+  p.cu_seqlens = tok->cu_seqlens;
+  p.state_slots = state_slots;
+  p.pool = pool->base;
+  p.snap = snapshots;
+  p.err = err;
+  p.B = tok->num_seqs;
+  p.N = tok->num_tokens;
+  p.H = pool->num_heads;
+  p.P = pool->num_slots;
+  p.max_T = max_T;
+  return cuda_status(kda::launch_verify_snapshot(
+      p, tok->dtype, tok->d_k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int kda_commit_snapshot(const int32_t *accepted_len, const int32_t *state_slots,
+                        int32_t num_seqs, kda_state_pool *pool,
+                        const float *snapshots, int32_t max_T,
+                        kda_stream_t stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if (num_seqs < 0 || num_seqs > kMaxGridY) return KDA_EINVAL;
+  if (max_T < 1 || max_T > kda::verify_max_spec_tokens()) return KDA_EINVAL;
+  if (num_seqs == 0) return KDA_OK;
+  if (!accepted_len || !state_slots || !snapshots) return KDA_EINVAL;
+  if (!aligned16(snapshots)) return KDA_EALIGN;
+  unsigned *err = device_error_word();
+  if (!err) return KDA_ECUDA;
+  kda::SnapshotParams p = {};
+  p.accepted_len = accepted_len;
+  p.state_slots = state_slots;
+  p.pool = pool->base;
+  p.snap = const_cast<float *>(snapshots);
+  p.err = err;
+  p.B = num_seqs;
+  p.H = pool->num_heads;
+  p.P = pool->num_slots;
+  p.max_T = max_T;
+  return cuda_status(kda::launch_commit_snapshot(
+      p, pool->d_k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int kda_get_device_error(int32_t *host_bits, kda_stream_t stream) {
   if (!host_bits) return KDA_EINVAL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

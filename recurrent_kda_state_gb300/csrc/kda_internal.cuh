@@ -83,6 +83,21 @@ struct CommitLayersParams {
   int B, H, P, L;
 };
 
+// Direct per-position snapshots (the design ReplaySSM replaces): verify that
+// stores the state after every drafted token, and a commit that copies the
+// accepted one into the pool.
+struct SnapshotParams {
+  const void *q, *k, *v, *alpha, *beta;
+  float *o;
+  const int32_t *cu_seqlens;
+  const int32_t *state_slots;
+  const int32_t *accepted_len;  // commit only
+  float *pool;
+  float *snap;                  // [B][max_T][H][d_v][d_k]
+  unsigned int *err;
+  int B, N, H, P, max_T;
+};
+
 struct SlotCopyParams {
   const float *src_base;
   float *dst_base;
@@ -144,6 +159,9 @@ cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_commit_layers(const CommitLayersParams &p, cudaStream_t s);
 cudaError_t launch_ring_reset(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_slot_copy(const SlotCopyParams &p, cudaStream_t s);
+cudaError_t launch_verify_snapshot(const SnapshotParams &p, kda_dtype dt, int D,
+                                   cudaStream_t s);
+cudaError_t launch_commit_snapshot(const SnapshotParams &p, int D, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,
                            cudaStream_t s);
 // Tensor-core prefill (d_k = d_v = 128, chunk 64, bf16 inputs, heads a

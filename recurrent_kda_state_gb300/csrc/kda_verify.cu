@@ -765,6 +765,106 @@ __global__ void ring_reset_kernel(const CommitParams p) {
   c[1] = 0;
 }
 
+// ---------------------------------------------------------------------------
+// Direct per-position snapshots, the design that ReplaySSM replaces ("ReplaySSM
+// shrinks rollback state": a direct implementation stores the state at every
+// drafted position, T extra state writes per step).  Kept as the ablation
+// baseline.  One CTA per (sequence, head) with the thread mapping of
+// verify_kernel; every drafted token is applied with kda_step and the state
+// after token t is written to snapshot t, so snapshot a - 1 holds the same
+// bits as the state a ReplaySSM commit of a tokens rebuilds.
+template <int D, typename Tin>
+__global__ void __launch_bounds__(2 * D, 2)
+    verify_snapshot_kernel(const SnapshotParams p) {
+  constexpr int F = D / 16;
+  typedef Rec<D, Tin> R;
+  extern __shared__ float4 smem4[];
+  Tin *drf = reinterpret_cast<Tin *>(smem4);
+  const int h = blockIdx.x, i = blockIdx.y, tid = threadIdx.x, H = p.H;
+  const int rg = tid & 3, j0 = 2 * (tid >> 2);
+  const int slot = p.state_slots[i];
+  const int c0 = p.cu_seqlens[i], c1 = p.cu_seqlens[i + 1];
+  int bad = 0;
+  if (slot < 0 || slot >= p.P) bad = KDA_DERR_SLOT;
+  else if (c0 < 0 || c1 < c0 || c1 > p.N) bad = KDA_DERR_SEGMENT;
+  else if (c1 - c0 > p.max_T) bad = KDA_DERR_DEPTH;
+  if (bad) {
+    if (tid == 0) set_error(p.err, (unsigned)bad);
+    return;
+  }
+  const int T = c1 - c0;
+  const float *st = p.pool + ((size_t)slot * H + h) * D * D;
+  f2 S[2][2 * F];
+  {
+    const ulonglong2 *a0 = reinterpret_cast<const ulonglong2 *>(st + (size_t)j0 * D);
+    const ulonglong2 *a1 = a0 + D / 4;
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+      const ulonglong2 x = a0[rg + 4 * f];
+      const ulonglong2 y = a1[rg + 4 * f];
+      S[0][2 * f] = x.x; S[0][2 * f + 1] = x.y;
+      S[1][2 * f] = y.x; S[1][2 * f + 1] = y.y;
+    }
+  }
+  if (T > 0) {
+    const size_t row = (size_t)c0 * H + h;
+    load_all_records<D, Tin>(
+        nullptr, drf, 0, T, nullptr, nullptr, nullptr, nullptr,
+        reinterpret_cast<const Tin *>(p.k) + row * D,
+        reinterpret_cast<const Tin *>(p.alpha) + row * D,
+        reinterpret_cast<const Tin *>(p.v) + row * D,
+        reinterpret_cast<const Tin *>(p.q) + row * D,
+        reinterpret_cast<const Tin *>(p.beta) + row, (size_t)H * D, (size_t)H, tid);
+  }
+  __syncthreads();
+  float o0 = 0.f, o1 = 0.f;
+  for (int t = 0; t < T; ++t) {
+    kda_step<D, true, Tin>(S, drf + t * R::kStride, rg, j0, o0, o1);
+    if (rg == 0)
+      *reinterpret_cast<float2 *>(p.o + ((size_t)(c0 + t) * H + h) * D + j0) =
+          make_float2(o0, o1);
+    float *sn = p.snap + (((size_t)i * p.max_T + t) * H + h) * D * D;
+    ulonglong2 *w0 = reinterpret_cast<ulonglong2 *>(sn + (size_t)j0 * D);
+    ulonglong2 *w1 = w0 + D / 4;
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+      w0[rg + 4 * f] = make_ulonglong2(S[0][2 * f], S[0][2 * f + 1]);
+      w1[rg + 4 * f] = make_ulonglong2(S[1][2 * f], S[1][2 * f + 1]);
+    }
+  }
+}
+
+// Commit of the direct design: pool(slot, h) = snapshot accepted_len - 1 of
+// its row (a plain copy; nothing when 0 tokens were accepted).  One CTA per
+// (sequence, head), every thread's loads issued before its stores.
+template <int D>
+__global__ void __launch_bounds__(256) commit_snapshot_kernel(const SnapshotParams p) {
+  constexpr int N4 = D * D / 4;
+  constexpr int PER = (N4 + 255) / 256;
+  const int h = blockIdx.x, i = blockIdx.y, tid = threadIdx.x, H = p.H;
+  const int a = p.accepted_len[i];
+  const int slot = p.state_slots[i];
+  if (a < 0 || a > p.max_T) {
+    if (tid == 0) set_error(p.err, KDA_DERR_ACCEPT);
+    return;
+  }
+  if (slot < 0 || slot >= p.P) {
+    if (tid == 0) set_error(p.err, KDA_DERR_SLOT);
+    return;
+  }
+  if (a == 0) return;
+  const float4 *src = reinterpret_cast<const float4 *>(
+      p.snap + (((size_t)i * p.max_T + (a - 1)) * H + h) * D * D);
+  float4 *dst = reinterpret_cast<float4 *>(p.pool + ((size_t)slot * H + h) * D * D);
+  float4 buf[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r)
+    if (tid + 256 * r < N4) buf[r] = src[tid + 256 * r];
+#pragma unroll
+  for (int r = 0; r < PER; ++r)
+    if (tid + 256 * r < N4) dst[tid + 256 * r] = buf[r];
+}
+
 // CTAs of `kern` that fit on one SM at once: the shared-memory, register
 // and thread limits of the device against the kernel's needs (taken as the
 // larger of this and the runtime's occupancy answer, which can assume a
@@ -878,6 +978,44 @@ cudaError_t launch_ring_reset(const CommitParams &p, cudaStream_t s) {
   const int n = p.B * p.H;
   if (n == 0) return cudaSuccess;
   ring_reset_kernel<<<(n + 255) / 256, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, typename Tin>
+cudaError_t launch_verify_snapshot_t(const SnapshotParams &p, cudaStream_t s) {
+  const size_t smem = (size_t)p.max_T * Rec<D, Tin>::kBytes;  // <= 33 KB
+  verify_snapshot_kernel<D, Tin><<<dim3(p.H, p.B), 2 * D, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_snapshot(const SnapshotParams &p, kda_dtype dt, int D,
+                                   cudaStream_t s) {
+  if (p.B == 0) return cudaSuccess;
+#define KDA_SV(DD)                                                          \
+  case DD:                                                                  \
+    return dt == KDA_BF16 ? launch_verify_snapshot_t<DD, __nv_bfloat16>(p, s) \
+                          : launch_verify_snapshot_t<DD, float>(p, s);
+  switch (D) {
+    KDA_SV(16)
+    KDA_SV(32)
+    KDA_SV(64)
+    KDA_SV(128)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef KDA_SV
+}
+
+cudaError_t launch_commit_snapshot(const SnapshotParams &p, int D, cudaStream_t s) {
+  if (p.B == 0) return cudaSuccess;
+  const dim3 grid(p.H, p.B);
+  switch (D) {
+    case 16: commit_snapshot_kernel<16><<<grid, 256, 0, s>>>(p); break;
+    case 32: commit_snapshot_kernel<32><<<grid, 256, 0, s>>>(p); break;
+    case 64: commit_snapshot_kernel<64><<<grid, 256, 0, s>>>(p); break;
+    case 128: commit_snapshot_kernel<128><<<grid, 256, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -44,7 +44,8 @@ class kda_replay_ring(ctypes.Structure):
 EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_noalloc",
            "kda_prefill_workspace_size", "kda_verify",
            "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
-           "kda_gather_states", "kda_copy_slots", "kda_get_device_error",
+           "kda_gather_states", "kda_copy_slots", "kda_verify_snapshot",
+           "kda_commit_snapshot", "kda_get_device_error",
            "kda_status_string", "kda_version")
 
 _lib = None
@@ -73,6 +74,8 @@ def lib():
         L.kda_ring_reset.argtypes = [_P, _I32, pp, rp, _P]
         L.kda_gather_states.argtypes = [pp, _P, _I32, _P, _P]
         L.kda_copy_slots.argtypes = [pp, _P, _P, _I32, _P]
+        L.kda_verify_snapshot.argtypes = [tp, _I32, pp, _P, _P, _P]
+        L.kda_commit_snapshot.argtypes = [_P, _P, _I32, pp, _P, _I32, _P]
         L.kda_get_device_error.argtypes = [ctypes.POINTER(_I32), _P]
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
@@ -250,6 +253,28 @@ def kda_gather_states(pool, slots, out=None, stream=None):
 def kda_copy_slots(pool, src, dst, stream=None):
     _check(lib().kda_copy_slots(ctypes.byref(pool.c), _ptr(src), _ptr(dst),
                                 src.numel(), _stream(stream)), "kda_copy_slots")
+
+
+def snapshot_buffer(num_seqs, max_T, pool):
+    """Per-position snapshots [num_seqs][max_T][H][d_v][d_k] fp32 for
+    kda_verify_snapshot (the direct design's extra state cache)."""
+    P, H, dv, dk = pool.data.shape
+    return torch.empty(num_seqs, max_T, H, dv, dk, dtype=torch.float32,
+                       device=pool.data.device)
+
+
+def kda_verify_snapshot(tok, max_T, pool, state_slots, snapshots, stream=None):
+    _check(lib().kda_verify_snapshot(ctypes.byref(tok.c), max_T,
+                                     ctypes.byref(pool.c), _ptr(state_slots),
+                                     _ptr(snapshots), _stream(stream)),
+           "kda_verify_snapshot")
+
+
+def kda_commit_snapshot(accepted_len, state_slots, pool, snapshots, stream=None):
+    _check(lib().kda_commit_snapshot(_ptr(accepted_len), _ptr(state_slots),
+                                     state_slots.numel(), ctypes.byref(pool.c),
+                                     _ptr(snapshots), int(snapshots.shape[1]),
+                                     _stream(stream)), "kda_commit_snapshot")
 
 
 def kda_get_device_error(stream=None):

@@ -134,3 +134,29 @@ def test_commit_and_slot_validation(L):
     assert L.kda_commit_layers(s, s, 1, by(pool), None, 2, None) == kda.KDA_EINVAL
     assert L.kda_commit_layers(s, s, 0, by(pool), rings, 2, None) == kda.KDA_OK
     assert L.kda_get_device_error(None, None) == kda.KDA_EINVAL
+
+
+def test_snapshot_validation(L):
+    """The direct-snapshot ablation calls reject bad arguments on the host."""
+    pool, tok = _pool(), _tokens()
+    by = ctypes.byref
+    s = ctypes.c_void_p(0x40000)
+    snap = ctypes.c_void_p(0x60000)
+    assert L.kda_verify_snapshot(None, 4, by(pool), s, snap, None) == kda.KDA_EINVAL
+    assert L.kda_verify_snapshot(by(tok), 0, by(pool), s, snap, None) == kda.KDA_EINVAL
+    assert L.kda_verify_snapshot(by(tok), 17, by(pool), s, snap, None) == kda.KDA_EINVAL
+    assert L.kda_verify_snapshot(by(tok), 4, by(pool), s, None, None) == kda.KDA_EINVAL
+    assert L.kda_verify_snapshot(by(tok), 4, by(pool), None, snap, None) == kda.KDA_EINVAL
+    assert L.kda_verify_snapshot(by(tok), 4, by(pool), s, ctypes.c_void_p(0x60004),
+                                 None) == kda.KDA_EALIGN
+    bad = _pool(d=48)
+    assert L.kda_verify_snapshot(by(tok), 4, by(bad), s, snap, None) == kda.KDA_ESHAPE
+    none = _tokens(B=0, N=0)
+    assert L.kda_verify_snapshot(by(none), 4, by(pool), None, None, None) == kda.KDA_OK
+    assert L.kda_commit_snapshot(None, s, 1, by(pool), snap, 4, None) == kda.KDA_EINVAL
+    assert L.kda_commit_snapshot(s, s, 1, by(pool), None, 4, None) == kda.KDA_EINVAL
+    assert L.kda_commit_snapshot(s, s, -1, by(pool), snap, 4, None) == kda.KDA_EINVAL
+    assert L.kda_commit_snapshot(s, s, 1, by(pool), snap, 0, None) == kda.KDA_EINVAL
+    assert L.kda_commit_snapshot(s, s, 1, by(pool), ctypes.c_void_p(0x60008), 4,
+                                 None) == kda.KDA_EALIGN
+    assert L.kda_commit_snapshot(s, s, 0, by(pool), snap, 4, None) == kda.KDA_OK
