@@ -145,9 +145,13 @@ typedef struct {
  * dropped.  ckpt_every == 0 disables checkpoints (ckpt_slots may be NULL).
  * Requirements: chunk in {16, 32, 64}; ckpt_every % chunk == 0; workspace of
  * at least kda_prefill_workspace_size(...) bytes, 256-byte aligned, owned by
- * the caller and not used by another call until this one completes.  When
- * that size is 0 (bf16 inputs at d_k = d_v = 128, chunk 64, heads a multiple
- * of 8: the tensor-core kernel) the workspace is not used and may be NULL.
+ * the caller and not used by another call until this one completes.
+ * At the tensor-core shape (bf16 inputs, d_k = d_v = 128, chunk 64, heads a
+ * multiple of 8) the workspace is optional: with one, the chunks' state-
+ * independent operands are computed for all chunks at once into it and a
+ * second pass walks the chunks (the faster path for long sequences); with
+ * NULL, one pass per (value slice, head, sequence) does everything.  Both
+ * meet the same tolerances; they are not bit-identical to each other.
  * The target slots must have no pending commit (see kda_materialize).
  */
 int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
@@ -157,8 +161,8 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
                         size_t workspace_bytes, kda_stream_t stream);
 
 /* Bytes of workspace kda_prefill_chunked needs for these sizes and input
- * dtype: 0 when it needs none (bf16 inputs at d_k = d_v = 128, chunk 64,
- * heads a multiple of 8), and 0 on bad arguments (which the prefill call
+ * dtype (at the tensor-core shape: for the two-pass path, about 162 KiB per
+ * (chunk of 64 tokens, head)), and 0 on bad arguments (which the prefill call
  * itself rejects). */
 size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
                                   int32_t num_heads, int32_t d_k, int32_t d_v,
@@ -181,8 +185,8 @@ size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
  * caller still passes inputs, outputs, pool and slot tables.
  *   - Returns KDA_ENOSPC, before any CUDA call, when
  *     kda_prefill_workspace_size(...) for these sizes and dtype exceeds
- *     KDA_NOALLOC_SCRATCH_BYTES; shapes that need no workspace run without
- *     touching the array.
+ *     KDA_NOALLOC_SCRATCH_BYTES, except at the tensor-core shape, which then
+ *     runs the single pass without touching the array.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - Every call shares the one array and it keeps the last call's contents

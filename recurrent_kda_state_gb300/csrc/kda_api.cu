@@ -121,7 +121,8 @@ size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
       !dim_ok(d_k) || (chunk != 16 && chunk != 32 && chunk != 64) ||
       (dtype != KDA_F32 && dtype != KDA_BF16))
     return 0;
-  if (kda::prefill_uses_tc(dtype, num_heads, d_k, d_v, chunk)) return 0;
+  if (kda::prefill_uses_tc(dtype, num_heads, d_k, d_v, chunk))
+    return kda::prefill_tc_workspace_bytes(num_tokens, num_seqs, num_heads);
   return kda::prefill_workspace_bytes(num_tokens, num_seqs, num_heads, d_k, chunk);
 }
 
@@ -140,11 +141,16 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
   if (tok->num_seqs == 0) return KDA_OK;
   if (!state_slots) return KDA_EINVAL;
   const bool tc = kda::prefill_uses_tc(tok->dtype, tok->num_heads, tok->d_k, tok->d_v, chunk);
-  if (!tc) {  // the CUDA-core kernels work in the caller's workspace
-    if (!workspace) return KDA_EINVAL;
+  // the CUDA-core kernels and the two-pass tensor-core kernels work in the
+  // caller's workspace; at the tensor-core shape a NULL workspace selects the
+  // single pass
+  if (!tc && !workspace) return KDA_EINVAL;
+  if (workspace) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return KDA_EALIGN;
-    const size_t need = kda::prefill_workspace_bytes(
-        tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, chunk);
+    const size_t need =
+        tc ? kda::prefill_tc_workspace_bytes(tok->num_tokens, tok->num_seqs, tok->num_heads)
+           : kda::prefill_workspace_bytes(tok->num_tokens, tok->num_seqs, tok->num_heads,
+                                          tok->d_k, chunk);
     if (workspace_bytes < need) return KDA_ENOSPC;
   }
   if ((long long)tok->num_tokens / chunk + 2LL * tok->num_seqs > 0x7fffffffLL)

@@ -146,6 +146,44 @@ __host__ __device__ inline size_t prefill_workspace_bytes(int N, int B, int H,
   return prefill_table_bytes(B) + (size_t)prefill_max_chunks(N, B, C) * H *
                                       prefill_entry_floats(D, C) * sizeof(float);
 }
+// Two-pass tensor-core prefill (the tensor-core shape with a workspace): the
+// chunk table, then per (chunk, head) one entry of kTcEntryBytes holding the
+// chunk's state-independent operands as shared-memory images (see
+// kda_prefill_tc.cu), entries 1024-byte aligned from the workspace base.
+constexpr size_t kTcEntryBytes = 165888;
+__host__ __device__ inline size_t prefill_tc_entries_offset(int B) {
+  return (prefill_table_bytes(B) + 1023) & ~(size_t)1023;
+}
+__host__ __device__ inline size_t prefill_tc_workspace_bytes(int N, int B, int H) {
+  return prefill_tc_entries_offset(B) +
+         (size_t)prefill_max_chunks(N, B, 64) * H * kTcEntryBytes;
+}
+
+// Chunk g of the workspace chunk table (prefix sums of the sequences' chunk
+// counts): its sequence, its index in the sequence, and its rows.
+struct ChunkLoc {
+  int i, q, tok0, n, end_local, L, p0;
+};
+__device__ __forceinline__ ChunkLoc locate_chunk(const PrefillParams &p, int g,
+                                                 int C) {
+  const int *table = reinterpret_cast<const int *>(p.ws);
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (table[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  ChunkLoc c;
+  c.i = lo;
+  c.q = g - table[lo];
+  c.L = p.cu_seqlens[lo + 1] - p.cu_seqlens[lo];
+  c.p0 = p.start_pos ? p.start_pos[lo] : 0;
+  const int r = c.p0 % C;
+  const int s_loc = max(0, c.q * C - r);
+  c.end_local = min(c.L, (c.q + 1) * C - r);
+  c.n = c.end_local - s_loc;
+  c.tok0 = p.cu_seqlens[lo] + s_loc;
+  return c;
+}
 
 // Verify launch geometry: dynamic shared memory for (D, ring depth, max_T),
 // and the longest speculative segment the kernel supports (ring depth limit).
@@ -165,7 +203,10 @@ cudaError_t launch_commit_snapshot(const SnapshotParams &p, int D, cudaStream_t 
 cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,
                            cudaStream_t s);
 // Tensor-core prefill (d_k = d_v = 128, chunk 64, bf16 inputs, heads a
-// multiple of 8; no workspace).
+// multiple of 8): two passes through the workspace when p.ws is set, else one
+// pass with no workspace.
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
+// The chunk table at the start of the workspace (one thread).
+cudaError_t launch_chunk_table(const PrefillParams &p, int C, cudaStream_t s);
 
 }  // namespace kda

@@ -44,9 +44,12 @@ extern "C" int kda_prefill_chunked_noalloc(const kda_tokens *tok,
   const size_t need = kda_prefill_workspace_size(
       tok->num_tokens, tok->num_seqs, tok->num_heads, tok->d_k, tok->d_v, chunk,
       tok->dtype);
-  // 0: no scratch needed (tensor-core shape) or bad arguments, which
-  // kda_prefill_chunked reports itself
-  if (need == 0)
+  // 0: bad arguments, which kda_prefill_chunked reports itself; at the
+  // tensor-core shape a workspace larger than the scratch selects the
+  // single pass, which needs none
+  const bool tc = kda::prefill_uses_tc(tok->dtype, tok->num_heads, tok->d_k, tok->d_v,
+                                       chunk);
+  if (need == 0 || (tc && need > KDA_NOALLOC_SCRATCH_BYTES))
     return kda_prefill_chunked(tok, pool, state_slots, ckpt_slots, max_ckpt,
                                ckpt_every, chunk, start_pos, nullptr, 0, stream);
   if (need > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ENOSPC;

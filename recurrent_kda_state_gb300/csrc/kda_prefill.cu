@@ -61,31 +61,6 @@ __global__ void chunk_table_kernel(const PrefillParams p, int C) {
   table[p.B] = off;
 }
 
-struct ChunkLoc {
-  int i, q, tok0, n, end_local, L, p0;
-};
-
-__device__ __forceinline__ ChunkLoc locate_chunk(const PrefillParams &p, int g,
-                                                 int C) {
-  const int *table = reinterpret_cast<const int *>(p.ws);
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (table[mid] <= g) lo = mid; else hi = mid - 1;
-  }
-  ChunkLoc c;
-  c.i = lo;
-  c.q = g - table[lo];
-  c.L = p.cu_seqlens[lo + 1] - p.cu_seqlens[lo];
-  c.p0 = p.start_pos ? p.start_pos[lo] : 0;
-  const int r = c.p0 % C;
-  const int s_loc = max(0, c.q * C - r);
-  c.end_local = min(c.L, (c.q + 1) * C - r);
-  c.n = c.end_local - s_loc;
-  c.tok0 = p.cu_seqlens[lo] + s_loc;
-  return c;
-}
-
 // Load rows t < n of one input vector (head h) as fp32 into dst[t * ld + c];
 // rows n..C-1 are filled with `pad`.  Optional elementwise transform.
 template <int D, int C, typename Tin, typename F>
@@ -499,6 +474,11 @@ cudaError_t launch_prefill_c(const PrefillParams &p, int C, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_chunk_table(const PrefillParams &p, int C, cudaStream_t s) {
+  chunk_table_kernel<<<1, 32, 0, s>>>(p, C);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill(const PrefillParams &p, kda_dtype dt, int D, int C,
                            cudaStream_t s) {

@@ -718,6 +718,607 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < 32) umma::tmem_dealloc(tmem, 512);
 }
 
+
+// ---------------------------------------------------------------------------
+// Two passes through a workspace.  The fused kernel above spends most of a
+// chunk on work that does not depend on the state (E1, R1, the inverse, R2)
+// inside the sequential chunk chain, and repeats it in each value slice.
+// With a workspace that work runs once per (chunk, head), for all chunks at
+// once, and the chain keeps R3, R4 and the state update:
+//   pass 1, prefill_tc_chunk_kernel: one CTA per (chunk, head): E1, R1, the
+//     inverse and R2 as above with R2 over all 128 value columns, then the
+//     chunk's workspace entry: the [W~; Q~], K^^T and [T; M] tiles as the
+//     shared-memory images the MMAs read (bf16 hi/lo, 128B-swizzled, 1024-byte
+//     aligned, so a bulk copy restores the swizzle), U' as fp32 in four
+//     32-column slices, and e^{g_m}, e^{g_C}, e^{g_C - g_m};
+//   pass 2, prefill_tc_pass_kernel: one CTA per (value slice, head, sequence)
+//     walks the chunks: S~ tile, R3, U = U' - W S, R4, outputs, state,
+//     checkpoints, while the bulk-copy engine brings the next chunk's entry in
+//     as soon as each of its buffers is free.
+
+struct Entry {                                 // byte offsets in an entry
+  static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
+  static constexpr uint32_t KT = 65536;        // K^^T hi, lo, [T; M] hi, lo
+  static constexpr uint32_t UP = 131072;       // U' [4 slices][64][32] fp32
+  static constexpr uint32_t VEC = 163840;      // e^{g_m}, e^{g_C}, e^{g_C-g_m}
+  static constexpr uint32_t END = VEC + 3 * 128 * 4;
+};
+static_assert(Entry::END <= kTcEntryBytes && kTcEntryBytes % 1024 == 0, "entry");
+
+struct LayP {                                  // pass 1
+  static constexpr uint32_t GA_HI = 0, GA_LO = 32768;
+  static constexpr uint32_t GB_HI = 65536, GB_LO = 81920;  // K^ (R1)
+  static constexpr uint32_t AF = 65536, XF = 82944;         // after R1
+  static constexpr uint32_t B2_HI = 101376;    // [K~^T; V^T]: 256 x 64
+  static constexpr uint32_t B2_LO = B2_HI + 256 * 128;      // K~^T lo
+  static constexpr uint32_t KH_HI = B2_LO + 16384, KH_LO = KH_HI + 16384;
+  static constexpr uint32_t TM_HI = KH_LO + 16384, TM_LO = TM_HI + 16384;
+  static constexpr uint32_t MISC = TM_LO + 16384;
+  static constexpr uint32_t BET = MISC, GM = BET + 256, GC = GM + 512;
+  static constexpr uint32_t EGC = GC + 512, ECM = EGC + 512, EGM = ECM + 512;
+  static constexpr uint32_t PT = EGM + 512, TOT4 = PT + 3072, BST = TOT4 + 2048;
+  static constexpr uint32_t MBAR = BST + 1024, SBAR = MBAR + 8, TSLOT = SBAR + 8;
+  static constexpr uint32_t END = TSLOT + 8;
+  static constexpr size_t kBytes = END + 1024;
+  // raw rows, consumed before E1 writes any tile over them
+  static constexpr uint32_t STG_Q = TM_HI, STG_K = TM_LO, STG_A = 65536, STG_V = 81920;
+};
+static_assert(LayP::B2_LO % 1024 == 0 && LayP::KH_HI % 1024 == 0 &&
+                  LayP::TM_HI % 1024 == 0 && LayP::KH_HI + 65536 == LayP::MISC,
+              "pass-1 tiles");
+static_assert(LayP::XF + 64 * 68 * 4 <= LayP::B2_HI, "A and X before the R2 B tile");
+static_assert(LayP::kBytes <= 232448, "pass-1 shared memory");
+
+struct LayS {                                  // pass 2
+  static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
+  static constexpr uint32_t KH_HI = 65536, KH_LO = 81920, TM_HI = 98304, TM_LO = 114688;
+  static constexpr uint32_t SB_HI = 131072, SB_LO = SB_HI + kNC * 256;
+  static constexpr uint32_t UT_HI = SB_LO + kNC * 256, UT_LO = UT_HI + kNC * 128;
+  // per chunk parity: U' slice [64][32] fp32, then the three vectors
+  static constexpr uint32_t SMALL = UT_LO + kNC * 128, SMALL_BYTES = 8192 + 1536;
+  static constexpr uint32_t MBAR = SMALL + 2 * SMALL_BYTES, G1 = MBAR + 8, G2 = G1 + 8;
+  static constexpr uint32_t TSLOT = G2 + 8, END = TSLOT + 8;
+  static constexpr size_t kBytes = END + 1024;
+};
+static_assert(LayS::SB_HI % 1024 == 0 && LayS::SB_LO % 1024 == 0 &&
+                  LayS::UT_HI % 1024 == 0 && LayS::UT_LO % 1024 == 0,
+              "pass-2 tiles");
+static_assert(LayS::kBytes <= 232448, "pass-2 shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_chunk_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
+  extern __shared__ float4 smem4[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = umma::smem_u32(sm);
+  float *bet = reinterpret_cast<float *>(sm + LayP::BET);
+  float *sgm = reinterpret_cast<float *>(sm + LayP::GM);
+  float *sgc = reinterpret_cast<float *>(sm + LayP::GC);
+  float *tot4 = reinterpret_cast<float *>(sm + LayP::TOT4);
+  float *egc = reinterpret_cast<float *>(sm + LayP::EGC);
+  float *ecm = reinterpret_cast<float *>(sm + LayP::ECM);
+  float *egmv = reinterpret_cast<float *>(sm + LayP::EGM);
+  float *Af = reinterpret_cast<float *>(sm + LayP::AF);
+  float *Xf = reinterpret_cast<float *>(sm + LayP::XF);
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + LayP::MBAR);
+  uint64_t *sbar_p = reinterpret_cast<uint64_t *>(sm + LayP::SBAR);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + LayP::TSLOT);
+
+  const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.H;
+  const int c = tid & 127, hf = tid >> 7;
+  if (g >= reinterpret_cast<const int *>(p.ws)[p.B]) return;
+  const ChunkLoc cl = locate_chunk(p, g, kC);
+  const int n = cl.n, tok0 = cl.tok0, m = n >> 1;
+
+  if (tid < 32) umma::tmem_alloc(tslot, 512);
+  if (tid == 0) {
+    umma::mbar_init(mbar, 1);
+    umma::mbar_init(sbar_p, 1);
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);
+  uint32_t phase = 0, sphase = 0;
+  const uint64_t dGA = umma::sdesc_sw128(sb);
+  if (tid == 0) {
+    const uint32_t sbar = sb + LayP::SBAR;
+    mbar_expect_tx(sbar, 4 * 64 * 2 * kD + 64 * 16);
+    tma_load3(sb + LayP::STG_Q, &maps.q, 0, h, tok0, sbar);
+    tma_load3(sb + LayP::STG_K, &maps.k, 0, h, tok0, sbar);
+    tma_load3(sb + LayP::STG_A, &maps.a, 0, h, tok0, sbar);
+    tma_load3(sb + LayP::STG_V, &maps.v, 0, h, tok0, sbar);
+    tma_load2(sb + LayP::BST, &maps.b, h & ~7, tok0, sbar);
+  }
+  bool ok = tc_wait(sbar_p, sphase, tid);
+  bool stage_owed = !ok, mma_owed = false;  // what a failed wait leaves in flight
+  if (ok) {
+    // ---- E1 (as in the fused kernel; V^T over all 128 value columns)
+    if (tid < kC) {
+      const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + LayP::BST)[tid * 8 + (h & 7)];
+      bet[tid] = tid < n ? __uint_as_float((uint32_t)bw << 16) : 0.f;
+    }
+    const int cp = tid & 63, tq = tid >> 6, c2 = 2 * cp, tb0 = 16 * tq;
+    float la0[16], la1[16];
+    uint32_t kr[16], qr[16];
+    {
+      const uint32_t *sq = reinterpret_cast<const uint32_t *>(sm + LayP::STG_Q);
+      const uint32_t *sk = reinterpret_cast<const uint32_t *>(sm + LayP::STG_K);
+      const uint32_t *sa = reinterpret_cast<const uint32_t *>(sm + LayP::STG_A);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int t = tb0 + u;
+        const uint32_t aw = sa[t * 64 + cp];
+        kr[u] = t < n ? sk[t * 64 + cp] : 0u;
+        qr[u] = t < n ? sq[t * 64 + cp] : 0u;
+        la0[u] = t < n ? __logf(__uint_as_float(aw << 16)) : 0.f;
+        la1[u] = t < n ? __logf(__uint_as_float(aw & 0xffff0000u)) : 0.f;
+      }
+    }
+    // V^T: thread (column j, token half vh) packs tokens 32 vh .. 32 vh + 31
+    uint32_t vw[16];
+    const int vj = tid & 127, vh = tid >> 7;
+    {
+      const uint16_t *vs = reinterpret_cast<const uint16_t *>(sm + LayP::STG_V);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int ta = 32 * vh + 2 * e;
+        vw[e] = (ta < n ? (uint32_t)vs[ta * kD + vj] : 0u) |
+                (ta + 1 < n ? (uint32_t)vs[(ta + 1) * kD + vj] << 16 : 0u);
+      }
+    }
+#pragma unroll
+    for (int u = 1; u < 16; ++u) {
+      la0[u] += la0[u - 1];
+      la1[u] += la1[u - 1];
+    }
+    tot4[tq * 128 + c2] = la0[15];
+    tot4[tq * 128 + c2 + 1] = la1[15];
+    __syncthreads();  // staging consumed; quarter sums visible
+    {
+      float add0 = 0.f, add1 = 0.f;
+      for (int w = 0; w < tq; ++w) {
+        add0 += tot4[w * 128 + c2];
+        add1 += tot4[w * 128 + c2 + 1];
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        la0[u] += add0;
+        la1[u] += add1;
+        if (tb0 + u == m) {
+          sgm[c2] = la0[u];
+          sgm[c2 + 1] = la1[u];
+        }
+      }
+      if (tq == 3) {
+        sgc[c2] = la0[15];
+        sgc[c2 + 1] = la1[15];
+      }
+    }
+    __syncthreads();
+    {
+      const float gm0 = sgm[c2], gm1 = sgm[c2 + 1];
+      if (tq == 0) {
+        const float gC0 = sgc[c2], gC1 = sgc[c2 + 1];
+        if (la0[0] - gm0 > 80.f || gm0 - gC0 > 80.f || la1[0] - gm1 > 80.f ||
+            gm1 - gC1 > 80.f)
+          set_error(p.err, KDA_DERR_RANGE);
+        egc[c2] = __expf(gC0);
+        egc[c2 + 1] = __expf(gC1);
+        ecm[c2] = __expf(gC0 - gm0);
+        ecm[c2 + 1] = __expf(gC1 - gm1);
+        egmv[c2] = __expf(gm0);
+        egmv[c2 + 1] = __expf(gm1);
+      }
+      uint32_t ktH[8], ktL[8], khH[8], khL[8];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int t = tb0 + u;
+        const float f0 = __expf(la0[u] - gm0), fi0 = __expf(gm0 - la0[u]);
+        const float f1 = __expf(la1[u] - gm1), fi1 = __expf(gm1 - la1[u]);
+        const float k0 = __uint_as_float(kr[u] << 16);
+        const float k1 = __uint_as_float(kr[u] & 0xffff0000u);
+        const float q0 = __uint_as_float(qr[u] << 16);
+        const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
+        uint32_t hi, lo;
+        uint32_t off = umma::sw128_off16(t, c2, 128);
+        umma::split_bf16x2(f0 * k0, f1 * k1, ktH[u & 7], ktL[u & 7]);
+        *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = ktH[u & 7];
+        *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = ktL[u & 7];
+        off = umma::sw128_off16(64 + t, c2, 128);
+        umma::split_bf16x2(f0 * q0, f1 * q1, hi, lo);
+        *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = hi;
+        *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = lo;
+        off = umma::sw128_off16(t, c2, 64);
+        umma::split_bf16x2(fi0 * k0, fi1 * k1, khH[u & 7], khL[u & 7]);
+        *reinterpret_cast<uint32_t *>(sm + LayP::GB_HI + off) = khH[u & 7];
+        *reinterpret_cast<uint32_t *>(sm + LayP::GB_LO + off) = khL[u & 7];
+        if ((u & 7) == 7) {
+          const int tb = t - 7;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t sel = e ? 0x7632u : 0x5410u;
+            const int row = c2 + e;
+            st_v4(sm, LayP::B2_HI + umma::sw128_off16(row, tb, 256),
+                  __byte_perm(ktH[0], ktH[1], sel), __byte_perm(ktH[2], ktH[3], sel),
+                  __byte_perm(ktH[4], ktH[5], sel), __byte_perm(ktH[6], ktH[7], sel));
+            st_v4(sm, LayP::B2_LO + umma::sw128_off16(row, tb, 128),
+                  __byte_perm(ktL[0], ktL[1], sel), __byte_perm(ktL[2], ktL[3], sel),
+                  __byte_perm(ktL[4], ktL[5], sel), __byte_perm(ktL[6], ktL[7], sel));
+            st_v4(sm, LayP::KH_HI + umma::sw128_off16(row, tb, 128),
+                  __byte_perm(khH[0], khH[1], sel), __byte_perm(khH[2], khH[3], sel),
+                  __byte_perm(khH[4], khH[5], sel), __byte_perm(khH[6], khH[7], sel));
+            st_v4(sm, LayP::KH_LO + umma::sw128_off16(row, tb, 128),
+                  __byte_perm(khL[0], khL[1], sel), __byte_perm(khL[2], khL[3], sel),
+                  __byte_perm(khL[4], khL[5], sel), __byte_perm(khL[6], khL[7], sel));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)  // V^T rows of the R2 B tile: exact bf16, hi only
+      st_v4(sm, LayP::B2_HI + umma::sw128_off16(128 + vj, 32 * vh + 8 * e, 256),
+            vw[4 * e], vw[4 * e + 1], vw[4 * e + 2], vw[4 * e + 3]);
+    tiles_ready();
+
+    // ---- R1: G = [K~; Q~] K^^T
+    if (tid == 0) {
+      const uint32_t id = umma::idesc_bf16(128, 64);
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 1 ? LayP::GA_LO : LayP::GA_HI;
+        const uint32_t b = ps == 2 ? LayP::GB_LO : LayP::GB_HI;
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_bf16(tmem + kAccG, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
+                         dadd(dGA, b + (kk >> 2) * 8192 + (kk & 3) * 32), id,
+                         (uint32_t)(ps | kk));
+      }
+      umma::commit(mbar);
+    }
+    ok = tc_wait(mbar, phase, tid);
+    mma_owed = !ok;
+  }
+  if (ok) {
+    {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> tile
+      float gv[32];
+      {
+        float g0[16], g1[16];
+        umma::tmem_ld16(tl + kAccG + 32 * hf, g0);
+        umma::tmem_ld16(tl + kAccG + 32 * hf + 16, g1);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          gv[e] = g0[e];
+          gv[16 + e] = g1[e];
+        }
+      }
+      if (c < 64) {
+        const int t = c;
+        const float bt = bet[t];
+#pragma unroll
+        for (int s4 = 0; s4 < 8; ++s4) {
+          const int s = 32 * hf + 4 * s4;
+          float4 v;
+          v.x = s < t ? bt * gv[4 * s4] : 0.f;
+          v.y = s + 1 < t ? bt * gv[4 * s4 + 1] : 0.f;
+          v.z = s + 2 < t ? bt * gv[4 * s4 + 2] : 0.f;
+          v.w = s + 3 < t ? bt * gv[4 * s4 + 3] : 0.f;
+          *reinterpret_cast<float4 *>(Af + fo(t, s)) = v;
+        }
+      } else {
+        const int t = c - 64;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int s = 32 * hf + 8 * ch;
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = s + e <= t ? gv[8 * ch + e] : 0.f;
+          put8(sm, LayP::TM_HI + umma::sw128_off16(64 + t, s, 128),
+               LayP::TM_LO + umma::sw128_off16(64 + t, s, 128), x);
+        }
+      }
+    }
+    __syncthreads();
+    unit_lower_inverse(Af, Xf, reinterpret_cast<float *>(sm + LayP::PT), tid);
+    {  // T = X diag(beta) -> rows 0..63 of the [T; M] tile
+      const int t = tid >> 2, s0 = (tid & 3) * 16;
+      float x[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        x[e] = s <= t ? Xf[fo(t, s)] * bet[s] : 0.f;
+      }
+      put8(sm, LayP::TM_HI + umma::sw128_off16(t, s0, 128),
+           LayP::TM_LO + umma::sw128_off16(t, s0, 128), x);
+      put8(sm, LayP::TM_HI + umma::sw128_off16(t, s0 + 8, 128),
+           LayP::TM_LO + umma::sw128_off16(t, s0 + 8, 128), x + 8);
+    }
+    tiles_ready();
+
+    // ---- R2: [T; M] [K~^T; V^T]^T -> rows 0..63: W~ (cols 0..127), U' (128..255)
+    if (tid == 0) {
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 1 ? LayP::TM_LO : LayP::TM_HI;
+        const uint32_t b = ps == 2 ? LayP::B2_LO : LayP::B2_HI;
+        const uint32_t id = umma::idesc_bf16(128, ps == 2 ? 128 : 256);
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_bf16(tmem + kAcc2, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
+                         (uint32_t)(ps | kk));
+      }
+      umma::commit(mbar);
+    }
+    ok = tc_wait(mbar, phase, tid);
+    mma_owed = !ok;
+  }
+  uint8_t *ent = p.ws + prefill_tc_entries_offset(p.B) + ((size_t)g * H + h) * kTcEntryBytes;
+  if (ok) {
+    if (c < 64) {  // W~ row t -> rows 0..63 of the [W~; Q~] tile; U' row t -> entry
+      const int t = c;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        float w[16];
+        const int k0 = 64 * hf + 16 * blk;
+        umma::tmem_ld16(tl + kAcc2 + k0, w);
+        put8(sm, LayP::GA_HI + umma::sw128_off16(t, k0, 128),
+             LayP::GA_LO + umma::sw128_off16(t, k0, 128), w);
+        put8(sm, LayP::GA_HI + umma::sw128_off16(t, k0 + 8, 128),
+             LayP::GA_LO + umma::sw128_off16(t, k0 + 8, 128), w + 8);
+      }
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        float u[16];
+        const int j0 = 64 * hf + 16 * blk;
+        umma::tmem_ld16(tl + kAcc2 + 128 + j0, u);
+        float4 *dst = reinterpret_cast<float4 *>(
+            ent + Entry::UP + (((j0 >> 5) * 64 + t) * 32 + (j0 & 31)) * 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[e] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+      }
+    }
+    tiles_ready();
+    if (tid == 0) {  // the tile images, by the bulk-copy engine
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        umma::bulk_s2g(ent + Entry::GA + 16384 * k, sb + LayP::GA_HI + 16384 * k, 16384);
+        umma::bulk_s2g(ent + Entry::KT + 16384 * k, sb + LayP::KH_HI + 16384 * k, 16384);
+      }
+      umma::bulk_commit();
+    }
+    if (tid < 128) {
+      float *vec = reinterpret_cast<float *>(ent + Entry::VEC);
+      vec[tid] = egmv[tid];
+      vec[128 + tid] = egc[tid];
+      vec[256 + tid] = ecm[tid];
+    }
+    if (tid == 0) umma::bulk_wait_read();  // shared memory stays until read
+  } else if (tid == 0) {
+    set_error(p.err, KDA_DERR_TIMEOUT);
+    // one more bounded chance for what is still in flight
+    if (mma_owed) umma::mbar_wait(mbar, phase, 1 << 26);
+    if (stage_owed) umma::mbar_wait(sbar_p, sphase, 1 << 26);
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) umma::tmem_dealloc(tmem, 512);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const PrefillParams p) {
+  extern __shared__ float4 smem4[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = umma::smem_u32(sm);
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + LayS::MBAR);
+  uint64_t *g1bar = reinterpret_cast<uint64_t *>(sm + LayS::G1);
+  uint64_t *g2bar = reinterpret_cast<uint64_t *>(sm + LayS::G2);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + LayS::TSLOT);
+
+  const int tid = threadIdx.x, sl = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+  const int H = p.H, col0 = sl * kNC;
+  const int c = tid & 127, hf = tid >> 7;
+  const int cu0 = p.cu_seqlens[i], cu1 = p.cu_seqlens[i + 1];
+  const int L = cu1 - cu0;
+  const int p0 = p.start_pos ? p.start_pos[i] : 0;
+  if (cu0 < 0 || L < 0 || cu1 > p.N || p0 < 0 || L == 0) return;  // flagged by the table
+  const int slot = p.state_slots[i];
+  if (slot < 0 || slot >= p.P) {
+    if (tid == 0 && sl == 0) set_error(p.err, KDA_DERR_SLOT);
+    return;
+  }
+  const int *table = reinterpret_cast<const int *>(p.ws);
+  const int g0 = table[i], nch = table[i + 1] - table[i];
+  if (nch <= 0) return;
+
+  if (tid < 32) umma::tmem_alloc(tslot, 64);
+  if (tid == 0) {
+    umma::mbar_init(mbar, 1);
+    umma::mbar_init(g1bar, 1);
+    umma::mbar_init(g2bar, 1);
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);
+  constexpr uint32_t kA3 = 0, kA4 = kNC;  // TMEM columns of the R3/R4 accumulators
+  uint32_t phase = 0, ph1 = 0, ph2 = 0;
+  bool owe1 = false, owe2 = false, mma_owed = false;
+  const uint64_t dGA = umma::sdesc_sw128(sb);
+  const uint8_t *ent0 = p.ws + prefill_tc_entries_offset(p.B);
+  auto entry = [&](int q) { return ent0 + ((size_t)(g0 + q) * H + h) * kTcEntryBytes; };
+  // buffers: [W~; Q~] and the small parts (parity q & 1); K^^T and [T; M]
+  auto issue_g1 = [&](int q) {
+    if (tid == 0) {
+      const uint8_t *e = entry(q);
+      const uint32_t bar = sb + LayS::G1, sp = sb + LayS::SMALL + (q & 1) * LayS::SMALL_BYTES;
+      mbar_expect_tx(bar, 65536 + LayS::SMALL_BYTES);
+      for (int k = 0; k < 4; ++k)
+        umma::bulk_g2s(sb + LayS::GA + 16384 * k, e + Entry::GA + 16384 * k, 16384, bar);
+      umma::bulk_g2s(sp, e + Entry::UP + sl * 8192, 8192, bar);
+      umma::bulk_g2s(sp + 8192, e + Entry::VEC, 1536, bar);
+    }
+    owe1 = true;
+  };
+  auto issue_g2 = [&](int q) {
+    if (tid == 0) {
+      const uint8_t *e = entry(q);
+      const uint32_t bar = sb + LayS::G2;
+      mbar_expect_tx(bar, 65536);
+      for (int k = 0; k < 4; ++k)
+        umma::bulk_g2s(sb + LayS::KH_HI + 16384 * k, e + Entry::KT + 16384 * k, 16384, bar);
+    }
+    owe2 = true;
+  };
+  issue_g1(0);
+  issue_g2(0);
+
+  float S[16];
+  {
+    const float *src = p.pool + ((size_t)slot * H + h) * kD * kD;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj)
+      S[jj] = src[(size_t)(col0 + 16 * hf + jj) * kD + c];
+  }
+  const int r0 = p0 % kC;
+  bool ok = true;
+  for (int q = 0; q < nch; ++q) {
+    const int s_loc = max(0, q * kC - r0);
+    const int e_loc = min(L, (q + 1) * kC - r0);
+    const int n = e_loc - s_loc, tok0 = cu0 + s_loc;
+    const float *up = reinterpret_cast<const float *>(sm + LayS::SMALL +
+                                                      (q & 1) * LayS::SMALL_BYTES);
+    const float *vec = up + 64 * kNC;
+    if (tid == 0 && q + 2 < nch) {  // two chunks ahead: into L2
+      const uint8_t *e = entry(q + 2);
+      umma::prefetch_l2(e + Entry::GA, 131072);
+      umma::prefetch_l2(e + Entry::UP + sl * 8192, 8192);
+      umma::prefetch_l2(e + Entry::VEC, 1536);
+    }
+    if (!(ok = tc_wait(g1bar, ph1, tid))) break;
+    owe1 = false;
+    {  // S~ = Diag(e^{g_m}) S -> S~^T tile (row j, k = channel)
+      const float egm = vec[c];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        uint16_t hi, lo;
+        umma::split_bf16(egm * S[jj], hi, lo);
+        const uint32_t off = umma::sw128_off16(16 * hf + jj, c, kNC);
+        st_u16(sm, LayS::SB_HI + off, hi);
+        st_u16(sm, LayS::SB_LO + off, lo);
+      }
+    }
+    tiles_ready();
+    // ---- R3: [W~; Q~] S~ -> W S (rows 0..63), Q S (rows 64..127)
+    if (tid == 0) {
+      const uint32_t id = umma::idesc_bf16(128, kNC);
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 1 ? LayS::GA + 32768 : LayS::GA;
+        const uint32_t b = ps == 2 ? LayS::SB_LO : LayS::SB_HI;
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_bf16(tmem + kA3, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
+                         dadd(dGA, b + (kk >> 2) * (kNC * 128) + (kk & 3) * 32), id,
+                         (uint32_t)(ps | kk));
+      }
+      umma::commit(mbar);
+    }
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = false;
+    if (q + 1 < nch) issue_g1(q + 1);  // [W~; Q~] is free; the other parity too
+    if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
+      const int t = c;
+      float ws[16];
+      umma::tmem_ld16(tl + kA3 + 16 * hf, ws);
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        uint16_t hi, lo;
+        umma::split_bf16(up[t * kNC + 16 * hf + jj] - ws[jj], hi, lo);
+        const uint32_t off = umma::sw128_off16(16 * hf + jj, t, kNC);
+        st_u16(sm, LayS::UT_HI + off, hi);
+        st_u16(sm, LayS::UT_LO + off, lo);
+      }
+    }
+    if (!(ok = tc_wait(g2bar, ph2, tid))) break;
+    owe2 = false;
+    tiles_ready();
+    // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
+    if (tid == 0) {
+      const uint32_t id = umma::idesc_bf16(128, kNC);
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 1 ? LayS::KH_LO : LayS::KH_HI;
+        const uint32_t b = ps == 2 ? LayS::UT_LO : LayS::UT_HI;
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_bf16(tmem + kA4, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
+                         (uint32_t)(ps | kk));
+      }
+      for (int ps = 0; ps < 3; ++ps) {
+        const uint32_t a = ps == 1 ? LayS::TM_LO : LayS::TM_HI;
+        const uint32_t b = ps == 2 ? LayS::UT_LO : LayS::UT_HI;
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_bf16(tmem + kA3, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id, 1u);
+      }
+      umma::commit(mbar);
+    }
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = false;
+    {
+      float acc[16];
+      umma::tmem_ld16(tl + kA4 + 16 * hf, acc);
+      const float a1 = vec[128 + c], a2 = vec[256 + c];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * acc[jj]);
+      if (c >= 64) {  // outputs of row t = c - 64
+        float o[16];
+        umma::tmem_ld16(tl + kA3 + 16 * hf, o);
+        const int t = c - 64;
+        if (t < n) {
+          float4 *dst = reinterpret_cast<float4 *>(
+              p.o + ((size_t)(tok0 + t) * H + h) * kD + col0 + 16 * hf);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+        }
+      }
+    }
+    const int P_end = p0 + e_loc;
+    if (p.ckpt_every > 0 && P_end % p.ckpt_every == 0 && p.ckpt_slots) {
+      const int mth = P_end / p.ckpt_every - p0 / p.ckpt_every - 1;
+      if (mth >= 0 && mth < p.max_ckpt) {
+        const int cs = p.ckpt_slots[(size_t)i * p.max_ckpt + mth];
+        if (cs >= p.P) {
+          if (tid == 0 && sl == 0) set_error(p.err, KDA_DERR_SLOT);
+        } else if (cs >= 0) {
+          float *dst = p.pool + ((size_t)cs * H + h) * kD * kD;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            dst[(size_t)(col0 + 16 * hf + jj) * kD + c] = S[jj];
+        }
+      }
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (q + 1 < nch) issue_g2(q + 1);  // K^^T and [T; M] are free
+  }
+  if (!ok) {
+    if (tid == 0) {
+      set_error(p.err, KDA_DERR_TIMEOUT);
+      if (mma_owed) umma::mbar_wait(mbar, phase, 1 << 26);
+    }
+  } else {
+    float *dst = p.pool + ((size_t)slot * H + h) * kD * kD;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) dst[(size_t)(col0 + 16 * hf + jj) * kD + c] = S[jj];
+  }
+  // no copy into shared memory outlives the CTA
+  if (tid == 0) {
+    if (owe1) umma::mbar_wait(g1bar, ph1, 1 << 26);
+    if (owe2) umma::mbar_wait(g2bar, ph2, 1 << 26);
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (tid < 32) umma::tmem_dealloc(tmem, 64);
+}
 }  // namespace
 
 namespace {
@@ -777,20 +1378,37 @@ cudaError_t beta_map(CUtensorMap *tm, const void *base, int N, int H) {
 
 }  // namespace
 
-// d_k = d_v = 128, chunk 64, bf16 inputs, H a multiple of 8; no workspace.
+// d_k = d_v = 128, chunk 64, bf16 inputs, H a multiple of 8: two passes
+// through the workspace when one is given, else the fused single pass.
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (p.B == 0 || p.N == 0) return cudaSuccess;
+  const bool two = p.ws != nullptr;
   InputMaps maps;
   cudaError_t e = input_map(&maps.q, p.q, p.N, p.H, kD);
   if (e == cudaSuccess) e = input_map(&maps.k, p.k, p.N, p.H, kD);
   if (e == cudaSuccess) e = input_map(&maps.a, p.alpha, p.N, p.H, kD);
-  if (e == cudaSuccess) e = input_map(&maps.v, p.v, p.N, p.H, kNC);
+  if (e == cudaSuccess) e = input_map(&maps.v, p.v, p.N, p.H, two ? kD : kNC);
   if (e == cudaSuccess) e = beta_map(&maps.b, p.beta, p.N, p.H);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)Lay::kBytes);
+  if (!two) {
+    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Lay::kBytes);
+    if (e != cudaSuccess) return e;
+    prefill_tc_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, Lay::kBytes, s>>>(p, maps);
+    return cudaGetLastError();
+  }
+  e = launch_chunk_table(p, kC, s);
   if (e != cudaSuccess) return e;
-  prefill_tc_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, Lay::kBytes, s>>>(p, maps);
+  e = cudaFuncSetAttribute(prefill_tc_chunk_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayP::kBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_tc_pass_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayS::kBytes);
+  if (e != cudaSuccess) return e;
+  prefill_tc_chunk_kernel<<<dim3(p.max_chunks, p.H), kThreads, LayP::kBytes, s>>>(p, maps);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prefill_tc_pass_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, LayS::kBytes, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -92,6 +92,35 @@ __device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global into shared memory, completing on `mbar`'s transaction count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
+}
+// Bulk copy from shared into global memory (same rules), in the issuing
+// thread's current bulk group.
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               :: "l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+// Close the issuing thread's bulk group, and wait until every group it
+// closed has finished reading shared memory.
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Hint: bring `bytes` (a multiple of 16) at `src` into L2.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes)
+               : "memory");
+}
+
 // Wait for phase `parity` of `mbar` to complete; gives up after `limit`
 // polls and returns false (the caller reports a device error).
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity,

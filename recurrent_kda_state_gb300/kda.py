@@ -175,10 +175,14 @@ def kda_prefill_workspace_size(num_tokens, num_seqs, H, d_k, d_v, chunk, dtype):
 
 def kda_prefill_chunked(tok, pool, state_slots, chunk, ckpt_every=0,
                         ckpt_slots=None, start_pos=None, workspace=None,
-                        stream=None):
-    """Chunked prefill; ckpt_slots [B][max_ckpt] int32 (device) or None."""
+                        stream=None, single_pass=False):
+    """Chunked prefill; ckpt_slots [B][max_ckpt] int32 (device) or None.
+    workspace None: one of the required size is allocated here;
+    single_pass: pass no workspace (the tensor-core shape's single pass)."""
     max_ckpt = 0 if ckpt_slots is None else int(ckpt_slots.shape[1])
-    if workspace is None:
+    if single_pass:
+        workspace = None
+    elif workspace is None:
         nbytes = kda_prefill_workspace_size(tok.c.num_tokens, tok.c.num_seqs,
                                             tok.c.num_heads, tok.c.d_k,
                                             tok.c.d_v, chunk, tok.c.dtype)

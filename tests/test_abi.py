@@ -108,9 +108,12 @@ def test_workspace_size_formula(L):
     entry = (4 * C * D + C * C + D + 63) // 64 * 64
     want = 256 + (N // C + 2 * B) * H * entry * 4
     assert L.kda_prefill_workspace_size(N, B, H, D, D, C, kda.KDA_F32) == want
-    # bf16 at d=128, chunk 64, heads a multiple of 8: the tensor-core kernel
-    # needs no workspace; other bf16 shapes follow the formula
-    assert L.kda_prefill_workspace_size(N, B, H, D, D, C, kda.KDA_BF16) == 0
+    # bf16 at d=128, chunk 64, heads a multiple of 8: the two-pass
+    # tensor-core path, table padded to 1 KiB + (N/C + 2B) x H entries of
+    # 165888 bytes (tile images, U', decay vectors); other bf16 shapes follow
+    # the formula above
+    assert L.kda_prefill_workspace_size(N, B, H, D, D, C, kda.KDA_BF16) == \
+        1024 + (N // C + 2 * B) * H * 165888
     assert L.kda_prefill_workspace_size(N, B, 4, D, D, C, kda.KDA_BF16) == \
         256 + (N // C + 2 * B) * 4 * entry * 4
     assert L.kda_prefill_workspace_size(N, B, H, D, D, 32, kda.KDA_BF16) > 0

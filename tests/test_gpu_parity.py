@@ -326,7 +326,7 @@ def test_slot_permutation_invariance():
 
 # ------------------------------------------------------------ prefill
 def _run_prefill(lengths, starts, H, d, C, ckpt_every, dtype, max_ckpt, hs,
-                 seed, s0_std=0.0, skip_ckpt=(), alpha=None):
+                 seed, s0_std=0.0, skip_ckpt=(), alpha=None, single_pass=False):
     rng = np.random.default_rng(seed)
     B = len(lengths)
     tok = ki.gen_tokens(rng, lengths, H, d)
@@ -343,7 +343,7 @@ def _run_prefill(lengths, starts, H, d, C, ckpt_every, dtype, max_ckpt, hs,
     tb = device_batch(tok, dtype)
     K.kda_prefill_chunked(tb, pool, i32(slots_np), chunk=C, ckpt_every=ckpt_every,
                           ckpt_slots=i32(ck) if max_ckpt else None,
-                          start_pos=i32(starts))
+                          start_pos=i32(starts), single_pass=single_pass)
     sess = oracle.OracleSession(P, len(hs), d, d, init=init[:, hs])
     o_ref, nck = sess.prefill(heads(tok, hs), slots_np, ckpt_every=ckpt_every,
                               ckpt_slots=ck if max_ckpt else None,
@@ -356,31 +356,38 @@ def _run_prefill(lengths, starts, H, d, C, ckpt_every, dtype, max_ckpt, hs,
     return tb, pool, nck
 
 
-def test_prefill_full_workload_sampled_heads():
+@pytest.mark.parametrize("single_pass", [False, True], ids=["two_pass", "single_pass"])
+def test_prefill_full_workload_sampled_heads(single_pass):
     """1 x 8192 tokens, 32 heads, d=128, bf16, chunk 64, checkpoints every
-    1024 tokens, S0 ~ N(0, 0.02^2); the oracle follows heads 0, 13 and 31."""
+    1024 tokens, S0 ~ N(0, 0.02^2); the oracle follows heads 0, 13 and 31.
+    Both tensor-core paths: two passes through a workspace, and one pass."""
     w = ki.PREFILL
     _, _, nck = _run_prefill([8192], [0], 32, 128, 64, 1024, "bf16", 8,
-                             [0, 13, 31], w.seed, s0_std=0.02)
+                             [0, 13, 31], w.seed, s0_std=0.02, single_pass=single_pass)
     assert nck[0] == 8
 
 
-@pytest.mark.parametrize("C,d", [(16, 64), (32, 64), (64, 64), (64, 128)])
-def test_prefill_ragged_and_offsets(C, d):
+@pytest.mark.parametrize("C,d,single_pass", [(16, 64, False), (32, 64, False),
+                                             (64, 64, False), (64, 128, False),
+                                             (64, 128, True)])
+def test_prefill_ragged_and_offsets(C, d, single_pass):
     lengths = [0, 1, C - 1, C, C + 1, 3 * C + 5, 100]
     starts = [0, 5, 0, 2 * C, C - 3, 7, 0]
-    H = 8 if d == 128 else 4  # d=128, chunk 64, 8 heads: the tensor-core kernel
+    H = 8 if d == 128 else 4  # d=128, chunk 64, 8 heads: the tensor-core kernels
     _run_prefill(lengths, starts, H, d, C, 2 * C, "bf16", 3, [0, 1, H // 2 + 1, H - 1],
-                 seed=900 + C + d, s0_std=0.1, skip_ckpt=[(5, 1)])
+                 seed=900 + C + d, s0_std=0.1, skip_ckpt=[(5, 1)],
+                 single_pass=single_pass)
 
 
-def test_prefill_slow_decay_carries_state():
+@pytest.mark.parametrize("single_pass", [False, True], ids=["two_pass", "single_pass"])
+def test_prefill_slow_decay_carries_state(single_pass):
     """alpha in [0.97, 1): the state carried across chunks dominates the
     outputs (with the default alpha ~ 0.5 it fades within a chunk), so the
     inter-chunk pass and the checkpoints are tested at full weight."""
     _run_prefill([1000, 333, 64], [0, 17, 64], 8, 128, 64, 128, "bf16", 8,
                  [0, 3, 7], seed=912, s0_std=0.5,
-                 alpha=lambda rng, shp: 1.0 - 0.03 * rng.random(shp))
+                 alpha=lambda rng, shp: 1.0 - 0.03 * rng.random(shp),
+                 single_pass=single_pass)
 
 
 def test_prefill_d128_chunk64_fallback_heads():

@@ -58,6 +58,9 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         (501, [200, 77], [0, 5], 8, 128, 64, 128, 2),
         (502, [130, 1, 64], [64, 3, 0], 2, 64, 32, 64, 3),
         (503, [200, 77], [0, 5], 4, 128, 64, 128, 2),  # d=128, 4 heads: scratch
+        # tensor-core shape whose two-pass workspace exceeds the scratch: the
+        # single pass, against the two-pass path of the workspace entry
+        (504, [3300], [0], 8, 128, 64, 1024, 3),
     ]
     for seed, lengths, starts, H, d, C, E, mc in cases:
         (o_ref, s_ref), (o_na, s_na) = _prefill_pair(seed, lengths, starts, H, d,
