@@ -760,8 +760,10 @@ struct LayP {                                  // pass 1
   static constexpr uint32_t MBAR = BST + 1024, SBAR = MBAR + 8, TSLOT = SBAR + 8;
   static constexpr uint32_t END = TSLOT + 8;
   static constexpr size_t kBytes = END + 1024;
-  // raw rows, consumed before E1 writes any tile over them
-  static constexpr uint32_t STG_Q = TM_HI, STG_K = TM_LO, STG_A = 65536, STG_V = 81920;
+  // raw rows of the next item, in regions free from the end of R2 (K^, A, X
+  // and the R2 B tile) and consumed before E1 writes any tile over them
+  static constexpr uint32_t STG_Q = 65536, STG_K = 81920, STG_A = B2_HI,
+                            STG_V = B2_HI + 16384;
 };
 static_assert(LayP::B2_LO % 1024 == 0 && LayP::KH_HI % 1024 == 0 &&
                   LayP::TM_HI % 1024 == 0 && LayP::KH_HI + 65536 == LayP::MISC,
@@ -772,17 +774,17 @@ static_assert(LayP::kBytes <= 232448, "pass-1 shared memory");
 struct LayS {                                  // pass 2
   static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
   static constexpr uint32_t KH_HI = 65536, KH_LO = 81920, TM_HI = 98304, TM_LO = 114688;
-  static constexpr uint32_t SB_HI = 131072, SB_LO = SB_HI + kNC * 256;
-  static constexpr uint32_t UT_HI = SB_LO + kNC * 256, UT_LO = UT_HI + kNC * 128;
+  // B operands with the hi and lo splits stacked along N (rows 0..31 hi,
+  // 32..63 lo): one N = 64 MMA takes both products with the A hi split
+  static constexpr uint32_t SB = 131072;       // S~^T: 64 x 128
+  static constexpr uint32_t UT = SB + 16384;   // U^T: 64 x 64
   // per chunk parity: U' slice [64][32] fp32, then the three vectors
-  static constexpr uint32_t SMALL = UT_LO + kNC * 128, SMALL_BYTES = 8192 + 1536;
+  static constexpr uint32_t SMALL = UT + 8192, SMALL_BYTES = 8192 + 1536;
   static constexpr uint32_t MBAR = SMALL + 2 * SMALL_BYTES, G1 = MBAR + 8, G2 = G1 + 8;
   static constexpr uint32_t TSLOT = G2 + 8, END = TSLOT + 8;
   static constexpr size_t kBytes = END + 1024;
 };
-static_assert(LayS::SB_HI % 1024 == 0 && LayS::SB_LO % 1024 == 0 &&
-                  LayS::UT_HI % 1024 == 0 && LayS::UT_LO % 1024 == 0,
-              "pass-2 tiles");
+static_assert(LayS::SB % 1024 == 0 && LayS::UT % 1024 == 0, "pass-2 tiles");
 static_assert(LayS::kBytes <= 232448, "pass-2 shared memory");
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -804,11 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *sbar_p = reinterpret_cast<uint64_t *>(sm + LayP::SBAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + LayP::TSLOT);
 
-  const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, H = p.H;
+  const int tid = threadIdx.x, H = p.H;
   const int c = tid & 127, hf = tid >> 7;
-  if (g >= reinterpret_cast<const int *>(p.ws)[p.B]) return;
-  const ChunkLoc cl = locate_chunk(p, g, kC);
-  const int n = cl.n, tok0 = cl.tok0, m = n >> 1;
+  // items (chunk g, head h), g-major; this CTA takes items blockIdx.x,
+  // blockIdx.x + gridDim.x, ...
+  const int total = reinterpret_cast<const int *>(p.ws)[p.B] * H;
+  int it = blockIdx.x;
+  if (it >= total) return;
 
   if (tid < 32) umma::tmem_alloc(tslot, 512);
   if (tid == 0) {
@@ -822,18 +826,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);
   uint32_t phase = 0, sphase = 0;
   const uint64_t dGA = umma::sdesc_sw128(sb);
-  if (tid == 0) {
-    const uint32_t sbar = sb + LayP::SBAR;
-    mbar_expect_tx(sbar, 4 * 64 * 2 * kD + 64 * 16);
-    tma_load3(sb + LayP::STG_Q, &maps.q, 0, h, tok0, sbar);
-    tma_load3(sb + LayP::STG_K, &maps.k, 0, h, tok0, sbar);
-    tma_load3(sb + LayP::STG_A, &maps.a, 0, h, tok0, sbar);
-    tma_load3(sb + LayP::STG_V, &maps.v, 0, h, tok0, sbar);
-    tma_load2(sb + LayP::BST, &maps.b, h & ~7, tok0, sbar);
-  }
-  bool ok = tc_wait(sbar_p, sphase, tid);
-  bool stage_owed = !ok, mma_owed = false;  // what a failed wait leaves in flight
-  if (ok) {
+  // TMA loads of item j's raw rows into the staging areas
+  auto stage = [&](int j) {
+    if (tid == 0) {
+      const int gj = j / H, hj = j - (j / H) * H;
+      const int t0 = locate_chunk(p, gj, kC).tok0;
+      const uint32_t sbar = sb + LayP::SBAR;
+      mbar_expect_tx(sbar, 4 * 64 * 2 * kD + 64 * 16);
+      tma_load3(sb + LayP::STG_Q, &maps.q, 0, hj, t0, sbar);
+      tma_load3(sb + LayP::STG_K, &maps.k, 0, hj, t0, sbar);
+      tma_load3(sb + LayP::STG_A, &maps.a, 0, hj, t0, sbar);
+      tma_load3(sb + LayP::STG_V, &maps.v, 0, hj, t0, sbar);
+      tma_load2(sb + LayP::BST, &maps.b, hj & ~7, t0, sbar);
+    }
+  };
+  stage(it);
+  bool ok = true, stage_owed = true, mma_owed = false;  // what is in flight
+  for (; it < total; it += gridDim.x) {
+    const int g = it / H, h = it - (it / H) * H;
+    const ChunkLoc cl = locate_chunk(p, g, kC);
+    const int n = cl.n, m = n >> 1;
+    if (!(ok = tc_wait(sbar_p, sphase, tid))) break;
+    stage_owed = false;
     // ---- E1 (as in the fused kernel; V^T over all 128 value columns)
     if (tid < kC) {
       const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + LayP::BST)[tid * 8 + (h & 7)];
@@ -875,7 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tot4[tq * 128 + c2] = la0[15];
     tot4[tq * 128 + c2 + 1] = la1[15];
-    __syncthreads();  // staging consumed; quarter sums visible
+    if (tid == 0) umma::bulk_wait_read();  // the last item's export has read its tiles
+    __syncthreads();  // staging consumed; quarter sums visible; tiles writable
     {
       float add0 = 0.f, add1 = 0.f;
       for (int w = 0; w < tq; ++w) {
@@ -975,10 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(mbar);
     }
-    ok = tc_wait(mbar, phase, tid);
-    mma_owed = !ok;
-  }
-  if (ok) {
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = false;
     {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> tile
       float gv[32];
       {
@@ -1046,11 +1060,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(mbar);
     }
-    ok = tc_wait(mbar, phase, tid);
-    mma_owed = !ok;
-  }
-  uint8_t *ent = p.ws + prefill_tc_entries_offset(p.B) + ((size_t)g * H + h) * kTcEntryBytes;
-  if (ok) {
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = false;
+    // R2 has read its operands: the next item's rows can land in the staging
+    // areas while this item's epilogue and export run
+    if (it + (int)gridDim.x < total) {
+      stage(it + gridDim.x);
+      stage_owed = true;
+    }
+    uint8_t *ent = p.ws + prefill_tc_entries_offset(p.B) + ((size_t)g * H + h) * kTcEntryBytes;
     if (c < 64) {  // W~ row t -> rows 0..63 of the [W~; Q~] tile; U' row t -> entry
       const int t = c;
 #pragma unroll
@@ -1090,13 +1109,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       vec[128 + tid] = egc[tid];
       vec[256 + tid] = ecm[tid];
     }
-    if (tid == 0) umma::bulk_wait_read();  // shared memory stays until read
-  } else if (tid == 0) {
+  }
+  if (!ok && tid == 0) {
     set_error(p.err, KDA_DERR_TIMEOUT);
     // one more bounded chance for what is still in flight
     if (mma_owed) umma::mbar_wait(mbar, phase, 1 << 26);
     if (stage_owed) umma::mbar_wait(sbar_p, sphase, 1 << 26);
   }
+  if (tid == 0) umma::bulk_wait_read();  // shared memory stays until read
   umma::fence_before_sync();
   __syncthreads();
   if (tid < 32) umma::tmem_dealloc(tmem, 512);
@@ -1128,7 +1148,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   const int g0 = table[i], nch = table[i + 1] - table[i];
   if (nch <= 0) return;
 
-  if (tid < 32) umma::tmem_alloc(tslot, 64);
+  if (tid < 32) umma::tmem_alloc(tslot, 128);
   if (tid == 0) {
     umma::mbar_init(mbar, 1);
     umma::mbar_init(g1bar, 1);
@@ -1139,7 +1159,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);
-  constexpr uint32_t kA3 = 0, kA4 = kNC;  // TMEM columns of the R3/R4 accumulators
+  // TMEM columns of the R3 / R4 accumulators, 64 each: columns 0..31 take
+  // the hi*hi and lo*hi products, 32..63 hi*lo; a result is their sum
+  constexpr uint32_t kA3 = 0, kA4 = 64;
   uint32_t phase = 0, ph1 = 0, ph2 = 0;
   bool owe1 = false, owe2 = false, mma_owed = false;
   const uint64_t dGA = umma::sdesc_sw128(sb);
@@ -1201,21 +1223,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       for (int jj = 0; jj < 16; ++jj) {
         uint16_t hi, lo;
         umma::split_bf16(egm * S[jj], hi, lo);
-        const uint32_t off = umma::sw128_off16(16 * hf + jj, c, kNC);
-        st_u16(sm, LayS::SB_HI + off, hi);
-        st_u16(sm, LayS::SB_LO + off, lo);
+        st_u16(sm, LayS::SB + umma::sw128_off16(16 * hf + jj, c, 64), hi);
+        st_u16(sm, LayS::SB + umma::sw128_off16(kNC + 16 * hf + jj, c, 64), lo);
       }
     }
     tiles_ready();
     // ---- R3: [W~; Q~] S~ -> W S (rows 0..63), Q S (rows 64..127)
-    if (tid == 0) {
-      const uint32_t id = umma::idesc_bf16(128, kNC);
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? LayS::GA + 32768 : LayS::GA;
-        const uint32_t b = ps == 2 ? LayS::SB_LO : LayS::SB_HI;
+    if (tid == 0) {  // A_hi [S~_hi | S~_lo] (N = 64), then A_lo S~_hi (N = 32)
+      for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t id = umma::idesc_bf16(128, ps ? kNC : 2 * kNC);
+        const uint32_t a = ps ? LayS::GA + 32768 : LayS::GA;
         for (int kk = 0; kk < 8; ++kk)
           umma::mma_bf16(tmem + kA3, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         dadd(dGA, b + (kk >> 2) * (kNC * 128) + (kk & 3) * 32), id,
+                         dadd(dGA, LayS::SB + (kk >> 2) * 8192 + (kk & 3) * 32), id,
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
@@ -1226,35 +1246,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     if (q + 1 < nch) issue_g1(q + 1);  // [W~; Q~] is free; the other parity too
     if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
       const int t = c;
-      float ws[16];
+      float ws[16], ws2[16];
       umma::tmem_ld16(tl + kA3 + 16 * hf, ws);
+      umma::tmem_ld16(tl + kA3 + kNC + 16 * hf, ws2);
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         uint16_t hi, lo;
-        umma::split_bf16(up[t * kNC + 16 * hf + jj] - ws[jj], hi, lo);
-        const uint32_t off = umma::sw128_off16(16 * hf + jj, t, kNC);
-        st_u16(sm, LayS::UT_HI + off, hi);
-        st_u16(sm, LayS::UT_LO + off, lo);
+        umma::split_bf16(up[t * kNC + 16 * hf + jj] - (ws[jj] + ws2[jj]), hi, lo);
+        st_u16(sm, LayS::UT + umma::sw128_off16(16 * hf + jj, t, 64), hi);
+        st_u16(sm, LayS::UT + umma::sw128_off16(kNC + 16 * hf + jj, t, 64), lo);
       }
     }
     if (!(ok = tc_wait(g2bar, ph2, tid))) break;
     owe2 = false;
     tiles_ready();
     // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
-    if (tid == 0) {
-      const uint32_t id = umma::idesc_bf16(128, kNC);
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? LayS::KH_LO : LayS::KH_HI;
-        const uint32_t b = ps == 2 ? LayS::UT_LO : LayS::UT_HI;
+    if (tid == 0) {  // as R3: the A hi split against [U_hi | U_lo], A lo against U_hi
+      for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t id = umma::idesc_bf16(128, ps ? kNC : 2 * kNC);
+        const uint32_t a = ps ? LayS::KH_LO : LayS::KH_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kA4, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
+          umma::mma_bf16(tmem + kA4, dadd(dGA, a + kk * 32), dadd(dGA, LayS::UT + kk * 32), id,
                          (uint32_t)(ps | kk));
       }
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? LayS::TM_LO : LayS::TM_HI;
-        const uint32_t b = ps == 2 ? LayS::UT_LO : LayS::UT_HI;
+      for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t id = umma::idesc_bf16(128, ps ? kNC : 2 * kNC);
+        const uint32_t a = ps ? LayS::TM_LO : LayS::TM_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kA3, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id, 1u);
+          umma::mma_bf16(tmem + kA3, dadd(dGA, a + kk * 32), dadd(dGA, LayS::UT + kk * 32), id,
+                         1u);
       }
       umma::commit(mbar);
     }
@@ -1262,21 +1282,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     if (!(ok = tc_wait(mbar, phase, tid))) break;
     mma_owed = false;
     {
-      float acc[16];
+      float acc[16], acc2[16];
       umma::tmem_ld16(tl + kA4 + 16 * hf, acc);
+      umma::tmem_ld16(tl + kA4 + kNC + 16 * hf, acc2);
       const float a1 = vec[128 + c], a2 = vec[256 + c];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * acc[jj]);
+      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * (acc[jj] + acc2[jj]));
       if (c >= 64) {  // outputs of row t = c - 64
-        float o[16];
+        float o[16], o2[16];
         umma::tmem_ld16(tl + kA3 + 16 * hf, o);
+        umma::tmem_ld16(tl + kA3 + kNC + 16 * hf, o2);
         const int t = c - 64;
         if (t < n) {
           float4 *dst = reinterpret_cast<float4 *>(
               p.o + ((size_t)(tok0 + t) * H + h) * kD + col0 + 16 * hf);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+            dst[e] = make_float4(o[4 * e] + o2[4 * e], o[4 * e + 1] + o2[4 * e + 1],
+                                 o[4 * e + 2] + o2[4 * e + 2], o[4 * e + 3] + o2[4 * e + 3]);
         }
       }
     }
@@ -1317,7 +1340,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   }
   umma::fence_before_sync();
   __syncthreads();
-  if (tid < 32) umma::tmem_dealloc(tmem, 64);
+  if (tid < 32) umma::tmem_dealloc(tmem, 128);
 }
 }  // namespace
 
@@ -1405,7 +1428,14 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   e = cudaFuncSetAttribute(prefill_tc_pass_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayS::kBytes);
   if (e != cudaSuccess) return e;
-  prefill_tc_chunk_kernel<<<dim3(p.max_chunks, p.H), kThreads, LayP::kBytes, s>>>(p, maps);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM walks the (chunk, head) items (the last ones exit at once)
+  const long long items = (long long)p.max_chunks * p.H;
+  const int grid1 = (int)(items < sms ? items : sms);
+  prefill_tc_chunk_kernel<<<grid1, kThreads, LayP::kBytes, s>>>(p, maps);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prefill_tc_pass_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, LayS::kBytes, s>>>(p);
