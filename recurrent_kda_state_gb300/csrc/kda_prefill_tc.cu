@@ -774,10 +774,10 @@ static_assert(LayP::kBytes <= 232448, "pass-1 shared memory");
 struct LayS {                                  // pass 2
   static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
   static constexpr uint32_t KH_HI = 65536, KH_LO = 81920, TM_HI = 98304, TM_LO = 114688;
-  // B operands with the hi and lo splits stacked along N (rows 0..31 hi,
-  // 32..63 lo): one N = 64 MMA takes both products with the A hi split
-  static constexpr uint32_t SB = 131072;       // S~^T: 64 x 128
-  static constexpr uint32_t UT = SB + 16384;   // U^T: 64 x 64
+  // B operands MN-major with the hi and lo splits stacked along N (n 0..31
+  // hi, 32..63 lo): one N = 64 MMA takes both products of an A split
+  static constexpr uint32_t SB = 131072;       // S~: K = 128 channels x 64
+  static constexpr uint32_t UT = SB + 16384;   // U: K = 64 tokens x 64
   // per chunk parity: U' slice [64][32] fp32, then the three vectors
   static constexpr uint32_t SMALL = UT + 8192, SMALL_BYTES = 8192 + 1536;
   static constexpr uint32_t MBAR = SMALL + 2 * SMALL_BYTES, G1 = MBAR + 8, G2 = G1 + 8;
@@ -786,6 +786,20 @@ struct LayS {                                  // pass 2
 };
 static_assert(LayS::SB % 1024 == 0 && LayS::UT % 1024 == 0, "pass-2 tiles");
 static_assert(LayS::kBytes <= 232448, "pass-2 shared memory");
+
+// Sixteen fp32 values x[0..15] of K-row k, MN positions n0 .. n0 + 15 (n0 a
+// multiple of 16, < 32) -> an MN-major tile holding the hi split at n and the
+// lo split at 32 + n: four 16-byte chunks.
+__device__ __forceinline__ void put16_mn(uint8_t *sm, uint32_t tile, int k, int n0,
+                                         const float *x) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) umma::split_bf16x2(x[2 * i], x[2 * i + 1], h[i], l[i]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, n0), h[0], h[1], h[2], h[3]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, n0 + 8), h[4], h[5], h[6], h[7]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0), l[0], l[1], l[2], l[3]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0 + 8), l[4], l[5], l[6], l[7]);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_chunk_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
@@ -1160,11 +1174,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);
   // TMEM columns of the R3 / R4 accumulators, 64 each: columns 0..31 take
-  // the hi*hi and lo*hi products, 32..63 hi*lo; a result is their sum
+  // the hi*hi and lo*hi products, 32..63 hi*lo and lo*lo; a result is their
+  // sum
   constexpr uint32_t kA3 = 0, kA4 = 64;
   uint32_t phase = 0, ph1 = 0, ph2 = 0;
   bool owe1 = false, owe2 = false, mma_owed = false;
   const uint64_t dGA = umma::sdesc_sw128(sb);
+  const uint64_t dSB = umma::sdesc_sw128_mn(sb + LayS::SB);
+  const uint64_t dUT = umma::sdesc_sw128_mn(sb + LayS::UT);
   const uint8_t *ent0 = p.ws + prefill_tc_entries_offset(p.B);
   auto entry = [&](int q) { return ent0 + ((size_t)(g0 + q) * H + h) * kTcEntryBytes; };
   // buffers: [W~; Q~] and the small parts (parity q & 1); K^^T and [T; M]
@@ -1219,24 +1236,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     owe1 = false;
     {  // S~ = Diag(e^{g_m}) S -> S~^T tile (row j, k = channel)
       const float egm = vec[c];
+      float x[16];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        uint16_t hi, lo;
-        umma::split_bf16(egm * S[jj], hi, lo);
-        st_u16(sm, LayS::SB + umma::sw128_off16(16 * hf + jj, c, 64), hi);
-        st_u16(sm, LayS::SB + umma::sw128_off16(kNC + 16 * hf + jj, c, 64), lo);
-      }
+      for (int jj = 0; jj < 16; ++jj) x[jj] = egm * S[jj];
+      put16_mn(sm, LayS::SB, c, 16 * hf, x);
     }
     tiles_ready();
     // ---- R3: [W~; Q~] S~ -> W S (rows 0..63), Q S (rows 64..127)
-    if (tid == 0) {  // A_hi [S~_hi | S~_lo] (N = 64), then A_lo S~_hi (N = 32)
+    if (tid == 0) {  // A_hi [S~_hi | S~_lo], then A_lo [S~_hi | S~_lo] (N = 64)
+      const uint32_t id = umma::idesc_bf16_bmn(128, 2 * kNC);
       for (int ps = 0; ps < 2; ++ps) {
-        const uint32_t id = umma::idesc_bf16(128, ps ? kNC : 2 * kNC);
         const uint32_t a = ps ? LayS::GA + 32768 : LayS::GA;
         for (int kk = 0; kk < 8; ++kk)
           umma::mma_bf16(tmem + kA3, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         dadd(dGA, LayS::SB + (kk >> 2) * 8192 + (kk & 3) * 32), id,
-                         (uint32_t)(ps | kk));
+                         dadd(dSB, kk * 2048), id, (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
     }
@@ -1249,32 +1262,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       float ws[16], ws2[16];
       umma::tmem_ld16(tl + kA3 + 16 * hf, ws);
       umma::tmem_ld16(tl + kA3 + kNC + 16 * hf, ws2);
+      const float4 *u4 = reinterpret_cast<const float4 *>(up + t * kNC + 16 * hf);
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        uint16_t hi, lo;
-        umma::split_bf16(up[t * kNC + 16 * hf + jj] - (ws[jj] + ws2[jj]), hi, lo);
-        st_u16(sm, LayS::UT + umma::sw128_off16(16 * hf + jj, t, 64), hi);
-        st_u16(sm, LayS::UT + umma::sw128_off16(kNC + 16 * hf + jj, t, 64), lo);
+      for (int e = 0; e < 4; ++e) {
+        const float4 uv = u4[e];
+        ws[4 * e] = uv.x - (ws[4 * e] + ws2[4 * e]);
+        ws[4 * e + 1] = uv.y - (ws[4 * e + 1] + ws2[4 * e + 1]);
+        ws[4 * e + 2] = uv.z - (ws[4 * e + 2] + ws2[4 * e + 2]);
+        ws[4 * e + 3] = uv.w - (ws[4 * e + 3] + ws2[4 * e + 3]);
       }
+      put16_mn(sm, LayS::UT, t, 16 * hf, ws);
     }
     if (!(ok = tc_wait(g2bar, ph2, tid))) break;
     owe2 = false;
     tiles_ready();
     // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
-    if (tid == 0) {  // as R3: the A hi split against [U_hi | U_lo], A lo against U_hi
+    if (tid == 0) {  // as R3: both A splits against [U_hi | U_lo]
+      const uint32_t id = umma::idesc_bf16_bmn(128, 2 * kNC);
       for (int ps = 0; ps < 2; ++ps) {
-        const uint32_t id = umma::idesc_bf16(128, ps ? kNC : 2 * kNC);
         const uint32_t a = ps ? LayS::KH_LO : LayS::KH_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kA4, dadd(dGA, a + kk * 32), dadd(dGA, LayS::UT + kk * 32), id,
+          umma::mma_bf16(tmem + kA4, dadd(dGA, a + kk * 32), dadd(dUT, kk * 2048), id,
                          (uint32_t)(ps | kk));
       }
       for (int ps = 0; ps < 2; ++ps) {
-        const uint32_t id = umma::idesc_bf16(128, ps ? kNC : 2 * kNC);
         const uint32_t a = ps ? LayS::TM_LO : LayS::TM_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kA3, dadd(dGA, a + kk * 32), dadd(dGA, LayS::UT + kk * 32), id,
-                         1u);
+          umma::mma_bf16(tmem + kA3, dadd(dGA, a + kk * 32), dadd(dUT, kk * 2048), id, 1u);
       }
       umma::commit(mbar);
     }

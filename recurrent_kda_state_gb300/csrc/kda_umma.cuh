@@ -32,6 +32,27 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return d;
 }
 
+// Descriptor of an MN-major operand with the 128-byte swizzle whose MN extent
+// is one 64-element atom (128 bytes): K-rows of 128 bytes, 8-row groups 1024
+// bytes apart (both stride fields 1024: with one MN atom only the K-group
+// stride is used).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(1024 >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Byte offset of element (k, n) of such an MN-major tile (n < 64): K-row k
+// holds n = 0..63 contiguous, 16-byte chunks swizzled by k % 8.
+__host__ __device__ __forceinline__ uint32_t sw128_mn_off16(int k, int n) {
+  return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((n >> 3) ^ (k & 7))) << 4) +
+                    (n & 7) * 2);
+}
+
 // Byte offset of element (row, k) of a K-major SW128 tile of 16-bit elements
 // with `rows` rows: K/64 blocks of rows x 128 bytes, 8 elements per 16-byte
 // chunk, swizzled as above.
@@ -48,6 +69,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_off16(int row, int k, int row
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+// The same with B MN-major (bit 16: B transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) {
+  return idesc_bf16(M, N) | (1u << 16);
 }
 
 // D (TMEM) (+)= A * B^T for one K = 16 step; A is M x 16, B is N x 16 (bf16).
