@@ -746,33 +746,32 @@ struct Entry {                                 // byte offsets in an entry
 static_assert(Entry::END <= kTcEntryBytes && kTcEntryBytes % 1024 == 0, "entry");
 
 struct LayP {                                  // pass 1
-  static constexpr uint32_t GA_HI = 0, GA_LO = 32768;
-  static constexpr uint32_t GB_HI = 65536, GB_LO = 81920;  // K^ (R1)
-  static constexpr uint32_t AF = 65536, XF = 82944;         // after R1
-  static constexpr uint32_t B2_HI = 101376;    // [K~^T; V^T]: 256 x 64
-  static constexpr uint32_t B2_LO = B2_HI + 256 * 128;      // K~^T lo
-  static constexpr uint32_t KH_HI = B2_LO + 16384, KH_LO = KH_HI + 16384;
-  static constexpr uint32_t TM_HI = KH_LO + 16384, TM_LO = TM_HI + 16384;
-  static constexpr uint32_t MISC = TM_LO + 16384;
+  static constexpr uint32_t GA_HI = 0, GA_LO = 32768;       // [K~; Q~] -> [W~; Q~]
+  static constexpr uint32_t GB_HI = 65536, GB_LO = 81920;   // K^ (R1 B; exported)
+  static constexpr uint32_t TM_HI = 98304, TM_LO = 114688;  // [T; M] (exported)
+  static constexpr uint32_t VT = 131072;       // V, MN-major (TMA, 128B swizzle)
+  static constexpr uint32_t AF = 147456, XF = AF + 64 * 68 * 4;  // after R1
+  static constexpr uint32_t MISC = XF + 64 * 68 * 4;
   static constexpr uint32_t BET = MISC, GM = BET + 256, GC = GM + 512;
   static constexpr uint32_t EGC = GC + 512, ECM = EGC + 512, EGM = ECM + 512;
   static constexpr uint32_t PT = EGM + 512, TOT4 = PT + 3072, BST = TOT4 + 2048;
   static constexpr uint32_t MBAR = BST + 1024, SBAR = MBAR + 8, TSLOT = SBAR + 8;
-  static constexpr uint32_t END = TSLOT + 8;
+  static constexpr uint32_t STG_A = (TSLOT + 8 + 1023) & ~1023u;
+  static constexpr uint32_t END = STG_A + 16384;
   static constexpr size_t kBytes = END + 1024;
-  // raw rows of the next item, in regions free from the end of R2 (K^, A, X
-  // and the R2 B tile) and consumed before E1 writes any tile over them
-  static constexpr uint32_t STG_Q = 65536, STG_K = 81920, STG_A = B2_HI,
-                            STG_V = B2_HI + 16384;
+  // raw q, k rows of the next item in the A and X arrays (free from the end of
+  // R2), alpha in its own area, V straight into VT; all consumed (or, for V,
+  // read by R2) before anything is written over them
+  static constexpr uint32_t STG_Q = AF, STG_K = AF + 16384;
 };
-static_assert(LayP::B2_LO % 1024 == 0 && LayP::KH_HI % 1024 == 0 &&
-                  LayP::TM_HI % 1024 == 0 && LayP::KH_HI + 65536 == LayP::MISC,
-              "pass-1 tiles");
-static_assert(LayP::XF + 64 * 68 * 4 <= LayP::B2_HI, "A and X before the R2 B tile");
+static_assert(LayP::GB_HI + 65536 == LayP::VT && LayP::VT % 1024 == 0,
+              "K^ and [T; M] contiguous (one export); V tile aligned");
+static_assert(LayP::STG_K + 16384 <= LayP::MISC, "q, k staging in A and X");
 static_assert(LayP::kBytes <= 232448, "pass-1 shared memory");
 
 struct LayS {                                  // pass 2
   static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
+  // K^ (read MN-major as K^^T) hi, lo; [T; M] hi, lo
   static constexpr uint32_t KH_HI = 65536, KH_LO = 81920, TM_HI = 98304, TM_LO = 114688;
   // B operands MN-major with the hi and lo splits stacked along N (n 0..31
   // hi, 32..63 lo): one N = 64 MMA takes both products of an A split
@@ -850,7 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load3(sb + LayP::STG_Q, &maps.q, 0, hj, t0, sbar);
       tma_load3(sb + LayP::STG_K, &maps.k, 0, hj, t0, sbar);
       tma_load3(sb + LayP::STG_A, &maps.a, 0, hj, t0, sbar);
-      tma_load3(sb + LayP::STG_V, &maps.v, 0, hj, t0, sbar);
+      tma_load3(sb + LayP::VT, &maps.v, 0, hj, t0, sbar);  // two 64-channel atoms
+      tma_load3(sb + LayP::VT + 8192, &maps.v, 64, hj, t0, sbar);
       tma_load2(sb + LayP::BST, &maps.b, hj & ~7, t0, sbar);
     }
   };
@@ -882,18 +882,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         qr[u] = t < n ? sq[t * 64 + cp] : 0u;
         la0[u] = t < n ? __logf(__uint_as_float(aw << 16)) : 0.f;
         la1[u] = t < n ? __logf(__uint_as_float(aw & 0xffff0000u)) : 0.f;
-      }
-    }
-    // V^T: thread (column j, token half vh) packs tokens 32 vh .. 32 vh + 31
-    uint32_t vw[16];
-    const int vj = tid & 127, vh = tid >> 7;
-    {
-      const uint16_t *vs = reinterpret_cast<const uint16_t *>(sm + LayP::STG_V);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int ta = 32 * vh + 2 * e;
-        vw[e] = (ta < n ? (uint32_t)vs[ta * kD + vj] : 0u) |
-                (ta + 1 < n ? (uint32_t)vs[(ta + 1) * kD + vj] << 16 : 0u);
       }
     }
 #pragma unroll
@@ -940,7 +928,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         egmv[c2] = __expf(gm0);
         egmv[c2 + 1] = __expf(gm1);
       }
-      uint32_t ktH[8], ktL[8], khH[8], khL[8];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
         const int t = tb0 + u;
@@ -950,45 +937,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float k1 = __uint_as_float(kr[u] & 0xffff0000u);
         const float q0 = __uint_as_float(qr[u] << 16);
         const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
+        // K~ and Q~ rows of [K~; Q~] and the K^ rows: K-major for R1, and the
+        // same bytes serve R2 (K~) and the chunk walk's R4 (K^) as MN-major
+        // operands, so no transposed copy is written
         uint32_t hi, lo;
         uint32_t off = umma::sw128_off16(t, c2, 128);
-        umma::split_bf16x2(f0 * k0, f1 * k1, ktH[u & 7], ktL[u & 7]);
-        *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = ktH[u & 7];
-        *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = ktL[u & 7];
+        umma::split_bf16x2(f0 * k0, f1 * k1, hi, lo);
+        *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = hi;
+        *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = lo;
         off = umma::sw128_off16(64 + t, c2, 128);
         umma::split_bf16x2(f0 * q0, f1 * q1, hi, lo);
         *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = hi;
         *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = lo;
         off = umma::sw128_off16(t, c2, 64);
-        umma::split_bf16x2(fi0 * k0, fi1 * k1, khH[u & 7], khL[u & 7]);
-        *reinterpret_cast<uint32_t *>(sm + LayP::GB_HI + off) = khH[u & 7];
-        *reinterpret_cast<uint32_t *>(sm + LayP::GB_LO + off) = khL[u & 7];
-        if ((u & 7) == 7) {
-          const int tb = t - 7;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const uint32_t sel = e ? 0x7632u : 0x5410u;
-            const int row = c2 + e;
-            st_v4(sm, LayP::B2_HI + umma::sw128_off16(row, tb, 256),
-                  __byte_perm(ktH[0], ktH[1], sel), __byte_perm(ktH[2], ktH[3], sel),
-                  __byte_perm(ktH[4], ktH[5], sel), __byte_perm(ktH[6], ktH[7], sel));
-            st_v4(sm, LayP::B2_LO + umma::sw128_off16(row, tb, 128),
-                  __byte_perm(ktL[0], ktL[1], sel), __byte_perm(ktL[2], ktL[3], sel),
-                  __byte_perm(ktL[4], ktL[5], sel), __byte_perm(ktL[6], ktL[7], sel));
-            st_v4(sm, LayP::KH_HI + umma::sw128_off16(row, tb, 128),
-                  __byte_perm(khH[0], khH[1], sel), __byte_perm(khH[2], khH[3], sel),
-                  __byte_perm(khH[4], khH[5], sel), __byte_perm(khH[6], khH[7], sel));
-            st_v4(sm, LayP::KH_LO + umma::sw128_off16(row, tb, 128),
-                  __byte_perm(khL[0], khL[1], sel), __byte_perm(khL[2], khL[3], sel),
-                  __byte_perm(khL[4], khL[5], sel), __byte_perm(khL[6], khL[7], sel));
-          }
-        }
+        umma::split_bf16x2(fi0 * k0, fi1 * k1, hi, lo);
+        *reinterpret_cast<uint32_t *>(sm + LayP::GB_HI + off) = hi;
+        *reinterpret_cast<uint32_t *>(sm + LayP::GB_LO + off) = lo;
       }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)  // V^T rows of the R2 B tile: exact bf16, hi only
-      st_v4(sm, LayP::B2_HI + umma::sw128_off16(128 + vj, 32 * vh + 8 * e, 256),
-            vw[4 * e], vw[4 * e + 1], vw[4 * e + 2], vw[4 * e + 3]);
     tiles_ready();
 
     // ---- R1: G = [K~; Q~] K^^T
@@ -1062,14 +1028,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tiles_ready();
 
-    // ---- R2: [T; M] [K~^T; V^T]^T -> rows 0..63: W~ (cols 0..127), U' (128..255)
+    // ---- R2: [T; M] K~ -> rows 0..63: W~ (cols 0..127);  [T; M] V -> U'
+    // (cols 128..255).  K~ (rows 0..63 of [K~; Q~], 64-key atoms 16 KB apart)
+    // and V (two 64-channel atoms) are MN-major B operands.
     if (tid == 0) {
+      const uint32_t id = umma::idesc_bf16_bmn(128, 128);
+      const uint64_t dKh = umma::sdesc_sw128_mn(sb + LayP::GA_HI, 16384);
+      const uint64_t dKl = umma::sdesc_sw128_mn(sb + LayP::GA_LO, 16384);
+      const uint64_t dV = umma::sdesc_sw128_mn(sb + LayP::VT, 8192);
       for (int ps = 0; ps < 3; ++ps) {
         const uint32_t a = ps == 1 ? LayP::TM_LO : LayP::TM_HI;
-        const uint32_t b = ps == 2 ? LayP::B2_LO : LayP::B2_HI;
-        const uint32_t id = umma::idesc_bf16(128, ps == 2 ? 128 : 256);
+        const uint64_t b = ps == 2 ? dKl : dKh;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc2, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
+          umma::mma_bf16(tmem + kAcc2, dadd(dGA, a + kk * 32), dadd(b, kk * 2048), id,
+                         (uint32_t)(ps | kk));
+      }
+      for (int ps = 0; ps < 2; ++ps) {  // V is an exact bf16 input: two passes
+        const uint32_t a = ps ? LayP::TM_LO : LayP::TM_HI;
+        for (int kk = 0; kk < 4; ++kk)
+          umma::mma_bf16(tmem + kAcc2 + 128, dadd(dGA, a + kk * 32), dadd(dV, kk * 2048), id,
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
@@ -1113,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         umma::bulk_s2g(ent + Entry::GA + 16384 * k, sb + LayP::GA_HI + 16384 * k, 16384);
-        umma::bulk_s2g(ent + Entry::KT + 16384 * k, sb + LayP::KH_HI + 16384 * k, 16384);
+        umma::bulk_s2g(ent + Entry::KT + 16384 * k, sb + LayP::GB_HI + 16384 * k, 16384);
       }
       umma::bulk_commit();
     }
@@ -1277,12 +1254,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     owe2 = false;
     tiles_ready();
     // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
-    if (tid == 0) {  // as R3: both A splits against [U_hi | U_lo]
+    if (tid == 0) {  // as R3: both A splits against [U_hi | U_lo]; K^^T is the
+                     // K^ tile read MN-major (64-key atoms 8 KB apart)
+      const uint32_t idk = umma::idesc_bf16_abmn(128, 2 * kNC);
       const uint32_t id = umma::idesc_bf16_bmn(128, 2 * kNC);
       for (int ps = 0; ps < 2; ++ps) {
-        const uint32_t a = ps ? LayS::KH_LO : LayS::KH_HI;
+        const uint64_t a = umma::sdesc_sw128_mn(sb + (ps ? LayS::KH_LO : LayS::KH_HI), 8192);
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kA4, dadd(dGA, a + kk * 32), dadd(dUT, kk * 2048), id,
+          umma::mma_bf16(tmem + kA4, dadd(a, kk * 2048), dadd(dUT, kk * 2048), idk,
                          (uint32_t)(ps | kk));
       }
       for (int ps = 0; ps < 2; ++ps) {
@@ -1382,8 +1361,10 @@ EncodeTiledFn encode_tiled() {
 }
 
 // [N][H][D] bf16 as a 3-D tensor map with boxes of `box_x` channels x 1 head
-// x 64 tokens, no swizzle, zero fill past N.
-cudaError_t input_map(CUtensorMap *tm, const void *base, int N, int H, int box_x) {
+// x 64 tokens, zero fill past N; no swizzle, or (box_x = 64) the 128-byte
+// swizzle of an MN-major MMA operand (one 64-channel atom per box).
+cudaError_t input_map(CUtensorMap *tm, const void *base, int N, int H, int box_x,
+                      bool swizzle128 = false) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t gdim[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)N};
@@ -1392,8 +1373,8 @@ cudaError_t input_map(CUtensorMap *tm, const void *base, int N, int H, int box_x
   const cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
                          gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1424,7 +1405,8 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   cudaError_t e = input_map(&maps.q, p.q, p.N, p.H, kD);
   if (e == cudaSuccess) e = input_map(&maps.k, p.k, p.N, p.H, kD);
   if (e == cudaSuccess) e = input_map(&maps.a, p.alpha, p.N, p.H, kD);
-  if (e == cudaSuccess) e = input_map(&maps.v, p.v, p.N, p.H, two ? kD : kNC);
+  if (e == cudaSuccess)
+    e = two ? input_map(&maps.v, p.v, p.N, p.H, 64, true) : input_map(&maps.v, p.v, p.N, p.H, kNC);
   if (e == cudaSuccess) e = beta_map(&maps.b, p.beta, p.N, p.H);
   if (e != cudaSuccess) return e;
   if (!two) {

@@ -32,14 +32,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return d;
 }
 
-// Descriptor of an MN-major operand with the 128-byte swizzle whose MN extent
-// is one 64-element atom (128 bytes): K-rows of 128 bytes, 8-row groups 1024
-// bytes apart (both stride fields 1024: with one MN atom only the K-group
-// stride is used).
-__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr) {
+// Descriptor of an MN-major operand with the 128-byte swizzle: K-rows of
+// 128 bytes (64 MN elements, one atom), 8-row groups 1024 bytes apart, and
+// atoms along MN `atom_stride` bytes apart (the leading byte offset; unused
+// when the operand's MN extent is a single atom).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t atom_stride = 1024) {
   uint64_t d = 0;
   d |= (uint64_t)((addr & 0x3FFFF) >> 4);
-  d |= (uint64_t)(1024 >> 4) << 16;
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFF) << 16;
   d |= (uint64_t)(1024 >> 4) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
@@ -70,9 +70,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
-// The same with B MN-major (bit 16: B transposed).
+// The same with B MN-major (bit 16: B transposed), and with A and B MN-major
+// (bit 15: A transposed).
 __host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) {
   return idesc_bf16(M, N) | (1u << 16);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_abmn(int M, int N) {
+  return idesc_bf16(M, N) | (1u << 15) | (1u << 16);
 }
 
 // D (TMEM) (+)= A * B^T for one K = 16 step; A is M x 16, B is N x 16 (bf16).
