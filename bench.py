@@ -17,7 +17,8 @@ oracle on the host cores, bounded sample), `e2e` (same metric with every
 step's inputs copied from pinned host memory and its outputs copied back
 inside the timed region, the copies of neighbouring steps overlapping the
 compute on their own streams), `prefill` (chunked prefill with in-pass checkpoints,
-1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region),
+1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region: the
+two-pass path through the workspace, and the single pass beside it),
 `clocks` (nvidia-smi samples during the timed region),
 `ablation_direct_snapshots` (the design ReplaySSM replaces -- the state
 stored at every drafted position, the accepted one copied at commit -- on the
@@ -85,10 +86,19 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_hash(unit):
+    """First 16 hex digits of the SHA-256 of a kernel's translation unit and
+    the two headers it includes: a committed profile is used only when it was
+    taken on the same source."""
+    h = hashlib.sha256()
+    for name in (unit, "kda_umma.cuh", "kda_internal.cuh"):
+        with open(os.path.join(ROOT, "recurrent_kda_state_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def verify_source_hash():
-    src = os.path.join(ROOT, "recurrent_kda_state_gb300", "csrc", "kda_verify.cu")
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    return source_hash("kda_verify.cu")
 
 
 def ncu_traffic():
@@ -282,21 +292,19 @@ def build_inputs(torch, rng, NL, dev):
 
 
 def prefill_tensor_profile():
-    """Tensor-pipe utilisation of the prefill kernel from the committed ncu
+    """Tensor-pipe utilisation of the two prefill passes from the committed ncu
     summary, when it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "prefill_tc_tensor.json")
-    src = os.path.join(ROOT, "recurrent_kda_state_gb300", "csrc", "kda_prefill_tc.cu")
     try:
         with open(path) as f:
             prof = json.load(f)
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        sha = source_hash("kda_prefill_tc.cu")
     except OSError:
         return None
     if prof.get("kernel_source_sha256_16") != sha:
         return None
     return {k: prof[k] for k in ("sm__pipe_tensor_cycles_active_pct",
-                                 "dram_bytes_per_launch", "source")
+                                 "dram_bytes_per_call", "kernels", "source")
             if k in prof}
 
 
