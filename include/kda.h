@@ -225,6 +225,35 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
                const int32_t *is_spec, kda_stream_t stream);
 
 /*
+ * kda_forward_mixed -- one KDA layer over a packed batch that holds prefill
+ * segments beside speculative and ordinary decode segments, read in place
+ * with outputs written in place ("Small tensor copies leave the hot path":
+ * contiguous zero-copy slices and direct output writes; "KDA checkpoints stay
+ * inside the prefill").
+ *
+ * Sequences 0 .. num_prefill-1 of tok are prefill segments and occupy token
+ * rows [0, prefill_tokens) (prefill_tokens = cu_seqlens[num_prefill], passed
+ * on the host); they follow kda_prefill_chunked with state_slots[i],
+ * ckpt_slots [num_prefill][max_ckpt], start_pos [num_prefill] (or NULL) and
+ * the workspace (sized by kda_prefill_workspace_size(prefill_tokens,
+ * num_prefill, ...); NULL allowed where kda_prefill_chunked allows it).
+ * Sequences num_prefill .. num_seqs-1 follow kda_verify with
+ * state_slots[num_prefill + j], is_spec[num_prefill + j] (is_spec indexed
+ * over the whole batch, or NULL) and ring.  The parts must use distinct slots.
+ * Results are those of the two separate calls, bit for bit.
+ * With side_stream non-NULL (and not `stream`) the prefill part runs on
+ * side_stream, forked from `stream` and joined back by events, beside the
+ * verify part on `stream`; the call returns with `stream` ordered after both.
+ */
+int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefill_tokens,
+                      kda_state_pool *pool, const int32_t *state_slots,
+                      const int32_t *ckpt_slots, int32_t max_ckpt, int32_t ckpt_every,
+                      int32_t chunk, const int32_t *start_pos, void *workspace,
+                      size_t workspace_bytes, int32_t max_T, kda_replay_ring *ring,
+                      const int32_t *is_spec, kda_stream_t stream,
+                      kda_stream_t side_stream);
+
+/*
  * kda_commit -- record how many drafted tokens each sequence accepted.
  * ("Rejecting a draft only moves the buffer pointer.")
  *

@@ -40,7 +40,7 @@ int check_pool(const kda_state_pool *pool) {
   return KDA_OK;
 }
 
-int check_tokens(const kda_tokens *t, const kda_state_pool *pool) {
+int check_tokens(const kda_tokens *t, const kda_state_pool *pool, bool cu_aligned = true) {
   if (!t) return KDA_EINVAL;
   if (t->dtype != KDA_F32 && t->dtype != KDA_BF16) return KDA_EDTYPE;
   if (t->num_seqs < 0 || t->num_tokens < 0) return KDA_EINVAL;
@@ -56,7 +56,7 @@ int check_tokens(const kda_tokens *t, const kda_state_pool *pool) {
       if (!aligned16(p)) return KDA_EALIGN;
     }
   }
-  if (!aligned16(t->cu_seqlens)) return KDA_EALIGN;
+  if (cu_aligned && !aligned16(t->cu_seqlens)) return KDA_EALIGN;
   return KDA_OK;
 }
 
@@ -126,14 +126,17 @@ size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
   return kda::prefill_workspace_bytes(num_tokens, num_seqs, num_heads, d_k, chunk);
 }
 
-int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
-                        const int32_t *state_slots, const int32_t *ckpt_slots,
-                        int32_t max_ckpt, int32_t ckpt_every, int32_t chunk,
-                        const int32_t *start_pos, void *workspace,
-                        size_t workspace_bytes, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *state_slots,
+                 const int32_t *ckpt_slots, int32_t max_ckpt, int32_t ckpt_every,
+                 int32_t chunk, const int32_t *start_pos, void *workspace,
+                 size_t workspace_bytes, kda_stream_t stream, bool cu_aligned) {
   int st = check_pool(pool);
   if (st) return st;
-  if ((st = check_tokens(tok, pool))) return st;
+  if ((st = check_tokens(tok, pool, cu_aligned))) return st;
   if (chunk != 16 && chunk != 32 && chunk != 64) return KDA_EINVAL;
   if (ckpt_every < 0 || max_ckpt < 0) return KDA_EINVAL;
   if (ckpt_every > 0 && ckpt_every % chunk != 0) return KDA_EINVAL;
@@ -182,12 +185,12 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
-               const int32_t *state_slots, kda_replay_ring *ring,
-               const int32_t *is_spec, kda_stream_t stream) {
+int verify_impl(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
+                const int32_t *state_slots, kda_replay_ring *ring, const int32_t *is_spec,
+                kda_stream_t stream, bool cu_aligned) {
   int st = check_pool(pool);
   if (st) return st;
-  if ((st = check_tokens(tok, pool))) return st;
+  if ((st = check_tokens(tok, pool, cu_aligned))) return st;
   if ((st = check_ring(ring, tok->dtype, true))) return st;
   if (max_T < 0) return KDA_EINVAL;
   if (!is_spec && max_T > ring->depth) return KDA_EPROTO;
@@ -211,6 +214,90 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
   p.mode = 0;
   return cuda_status(kda::launch_verify(p, tok->dtype, tok->d_k,
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
+                        const int32_t *state_slots, const int32_t *ckpt_slots,
+                        int32_t max_ckpt, int32_t ckpt_every, int32_t chunk,
+                        const int32_t *start_pos, void *workspace,
+                        size_t workspace_bytes, kda_stream_t stream) {
+  return prefill_impl(tok, pool, state_slots, ckpt_slots, max_ckpt, ckpt_every, chunk,
+                      start_pos, workspace, workspace_bytes, stream, true);
+}
+
+int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
+               const int32_t *state_slots, kda_replay_ring *ring,
+               const int32_t *is_spec, kda_stream_t stream) {
+  return verify_impl(tok, max_T, pool, state_slots, ring, is_spec, stream, true);
+}
+
+int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefill_tokens,
+                      kda_state_pool *pool, const int32_t *state_slots,
+                      const int32_t *ckpt_slots, int32_t max_ckpt, int32_t ckpt_every,
+                      int32_t chunk, const int32_t *start_pos, void *workspace,
+                      size_t workspace_bytes, int32_t max_T, kda_replay_ring *ring,
+                      const int32_t *is_spec, kda_stream_t stream,
+                      kda_stream_t side_stream) {
+  int st = check_pool(pool);
+  if (st) return st;
+  if ((st = check_tokens(tok, pool))) return st;
+  if (num_prefill < 0 || num_prefill > tok->num_seqs) return KDA_EINVAL;
+  if (prefill_tokens < 0 || prefill_tokens > tok->num_tokens) return KDA_EINVAL;
+  if (num_prefill == 0 && prefill_tokens != 0) return KDA_EINVAL;
+  if (tok->num_seqs > 0 && !state_slots) return KDA_EINVAL;
+  // the two parts: zero-copy views of the same packed tensors
+  kda_tokens tp = *tok, tv = *tok;
+  tp.num_seqs = num_prefill;
+  tp.num_tokens = prefill_tokens;
+  tv.num_seqs = tok->num_seqs - num_prefill;
+  tv.cu_seqlens = tok->cu_seqlens ? tok->cu_seqlens + num_prefill : nullptr;
+  if (tv.num_seqs > 0) {  // validate the verify part before anything is launched
+    if ((st = check_ring(ring, tok->dtype, true))) return st;
+    if (max_T < 0) return KDA_EINVAL;
+    if (!is_spec && max_T > ring->depth) return KDA_EPROTO;
+    if (kda::verify_smem_bytes(tok->d_k, ring->depth, max_T, tok->dtype) > kMaxSmem)
+      return KDA_EINVAL;
+  }
+  const bool fork = side_stream != nullptr && side_stream != stream && num_prefill > 0 &&
+                    tv.num_seqs > 0;
+  cudaStream_t main_s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t side_s = reinterpret_cast<cudaStream_t>(side_stream);
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  if (fork) {
+    if (cudaEventCreateWithFlags(&ev[0], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev[1], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventRecord(ev[0], main_s) != cudaSuccess ||
+        cudaStreamWaitEvent(side_s, ev[0], 0) != cudaSuccess) {
+      for (cudaEvent_t e : ev)
+        if (e) cudaEventDestroy(e);
+      return KDA_ECUDA;
+    }
+  }
+  bool join = false;
+  if (num_prefill > 0) {
+    st = prefill_impl(&tp, pool, state_slots, ckpt_slots, max_ckpt, ckpt_every, chunk,
+                      start_pos, workspace, workspace_bytes, fork ? side_stream : stream,
+                      true);
+    if (fork) {
+      if (cudaEventRecord(ev[1], side_s) == cudaSuccess) join = true;
+      else if (st == KDA_OK) st = KDA_ECUDA;
+    }
+  }
+  if (st == KDA_OK && tv.num_seqs > 0)
+    st = verify_impl(&tv, max_T, pool, state_slots + num_prefill, ring,
+                     is_spec ? is_spec + num_prefill : nullptr, stream, false);
+  if (fork) {
+    // the caller's stream waits for whatever the side stream took (the join)
+    if (join && cudaStreamWaitEvent(main_s, ev[1], 0) != cudaSuccess && st == KDA_OK)
+      st = KDA_ECUDA;
+    cudaEventDestroy(ev[0]);
+    cudaEventDestroy(ev[1]);
+  }
+  return st;
 }
 
 int kda_commit(const int32_t *accepted_len, const int32_t *state_slots,

@@ -45,7 +45,7 @@ EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_noalloc",
            "kda_prefill_workspace_size", "kda_verify",
            "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
            "kda_gather_states", "kda_copy_slots", "kda_verify_snapshot",
-           "kda_commit_snapshot", "kda_get_device_error",
+           "kda_commit_snapshot", "kda_forward_mixed", "kda_get_device_error",
            "kda_status_string", "kda_version")
 
 _lib = None
@@ -75,6 +75,8 @@ def lib():
         L.kda_gather_states.argtypes = [pp, _P, _I32, _P, _P]
         L.kda_copy_slots.argtypes = [pp, _P, _P, _I32, _P]
         L.kda_verify_snapshot.argtypes = [tp, _I32, pp, _P, _P, _P]
+        L.kda_forward_mixed.argtypes = [tp, _I32, _I32, pp, _P, _P, _I32, _I32, _I32,
+                                        _P, _P, ctypes.c_size_t, _I32, rp, _P, _P, _P]
         L.kda_commit_snapshot.argtypes = [_P, _P, _I32, pp, _P, _I32, _P]
         L.kda_get_device_error.argtypes = [ctypes.POINTER(_I32), _P]
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -214,6 +216,33 @@ def kda_verify(tok, max_T, pool, state_slots, ring, is_spec=None, stream=None):
     _check(lib().kda_verify(ctypes.byref(tok.c), max_T, ctypes.byref(pool.c),
                             _ptr(state_slots), ctypes.byref(ring.c),
                             _ptr(is_spec), _stream(stream)), "kda_verify")
+
+
+def kda_forward_mixed(tok, num_prefill, prefill_tokens, pool, state_slots, chunk,
+                      max_T, ring, ckpt_every=0, ckpt_slots=None, start_pos=None,
+                      is_spec=None, workspace=None, single_pass=False, stream=None,
+                      side_stream=None):
+    """Prefill segments (the first num_prefill sequences, token rows
+    [0, prefill_tokens)) and verify/decode segments of one packed batch in one
+    call; side_stream: run the prefill part there, forked and joined."""
+    max_ckpt = 0 if ckpt_slots is None else int(ckpt_slots.shape[1])
+    if single_pass or num_prefill == 0:
+        workspace = None
+    elif workspace is None:
+        nbytes = kda_prefill_workspace_size(prefill_tokens, num_prefill,
+                                            tok.c.num_heads, tok.c.d_k, tok.c.d_v,
+                                            chunk, tok.c.dtype)
+        if nbytes > 0:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=tok.k.device)
+    side = None if side_stream is None else ctypes.c_void_p(side_stream.cuda_stream)
+    _check(lib().kda_forward_mixed(
+        ctypes.byref(tok.c), num_prefill, prefill_tokens, ctypes.byref(pool.c),
+        _ptr(state_slots), _ptr(ckpt_slots), max_ckpt, ckpt_every, chunk,
+        _ptr(start_pos), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), max_T,
+        ctypes.byref(ring.c), _ptr(is_spec), _stream(stream), side),
+        "kda_forward_mixed")
+    return workspace
 
 
 def kda_commit(accepted_len, state_slots, pool, ring, stream=None):

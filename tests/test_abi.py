@@ -163,3 +163,27 @@ def test_snapshot_validation(L):
     assert L.kda_commit_snapshot(s, s, 1, by(pool), ctypes.c_void_p(0x60008), 4,
                                  None) == kda.KDA_EALIGN
     assert L.kda_commit_snapshot(s, s, 0, by(pool), snap, 4, None) == kda.KDA_OK
+
+
+def test_forward_mixed_validation(L):
+    """The mixed prefill + verify call checks its split on the host."""
+    pool, tok, ring = _pool(), _tokens(B=2, N=8), _ring()
+    by = ctypes.byref
+    s = ctypes.c_void_p(0x40000)
+
+    def call(npf, ptok, slots=s, ring_=ring, max_T=4, chunk=16):
+        return L.kda_forward_mixed(by(tok), npf, ptok, by(pool), slots, None, 0, 0,
+                                   chunk, None, None, 0, max_T,
+                                   by(ring_) if ring_ is not None else None,
+                                   None, None, None)
+    assert call(3, 0) == kda.KDA_EINVAL          # more prefill rows than sequences
+    assert call(-1, 0) == kda.KDA_EINVAL
+    assert call(1, 9) == kda.KDA_EINVAL          # beyond the batch's tokens
+    assert call(0, 4) == kda.KDA_EINVAL          # prefill tokens without sequences
+    assert call(1, 4, slots=None) == kda.KDA_EINVAL
+    assert call(1, 4, ring_=None) == kda.KDA_EINVAL   # the verify part needs a ring
+    assert call(1, 4, max_T=5) == kda.KDA_EPROTO      # drafts longer than the ring
+    assert call(1, 4, chunk=24) == kda.KDA_EINVAL     # prefill chunk size
+    none = _tokens(B=0, N=0)
+    assert L.kda_forward_mixed(by(none), 0, 0, by(pool), None, None, 0, 0, 16, None,
+                               None, 0, 4, by(ring), None, None, None) == kda.KDA_OK

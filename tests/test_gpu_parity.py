@@ -575,3 +575,64 @@ def test_determinism():
     p1 = _run_spec(steps=3, hs=[0])
     p2 = _run_spec(steps=3, hs=[0])
     assert torch.equal(p1.data, p2.data)
+
+
+# ------------------------------------------- prefill beside verify, one call
+@pytest.mark.parametrize("use_side", [False, True], ids=["one_stream", "side_stream"])
+def test_forward_mixed_prefill_and_verify_segments(use_side):
+    """One packed batch: two prefill segments (checkpoints, a start offset)
+    followed by speculative and ordinary rows, run by kda_forward_mixed as
+    zero-copy views; equals the two separate calls on separate tensors bit for
+    bit (outputs, states, ring), and the oracle, also after the commit."""
+    rng = np.random.default_rng(71)
+    H, d, C, T, P = 8, 128, 64, 8, 24
+    spec_mask = [1, 0, 1, 0, 0, 1]
+    lens = [200, 77] + [T if m else 1 for m in spec_mask]
+    npf, starts = 2, [0, 64]
+    tok = ki.round_to(ki.gen_tokens(rng, lens, H, d), "bf16")
+    ptok = int(tok["cu_seqlens"][npf])
+    slots_np = np.array([0, 1, 5, 6, 7, 8, 9, 10], np.int32)
+    ck = np.array([[2, 3], [4, -1]], np.int32)
+    init = ki.initial_states(rng, P, H, d, d, 0.1)
+    is_spec = np.array([0] * npf + spec_mask, np.int32)
+
+    poolA = K.StatePool(to_gpu_states(init).cuda())
+    ringA = K.ReplayRing(P, H, d, T, torch.bfloat16)
+    tbA = device_batch(tok, "bf16")
+    side = torch.cuda.Stream() if use_side else None
+    K.kda_forward_mixed(tbA, npf, ptok, poolA, i32(slots_np), C, T, ringA,
+                        ckpt_every=128, ckpt_slots=i32(ck), start_pos=i32(starts),
+                        is_spec=i32(is_spec), side_stream=side)
+
+    names = ("q", "k", "v", "alpha", "beta")
+    pre = {n: tok[n][:ptok] for n in names}
+    pre["cu_seqlens"] = tok["cu_seqlens"][:npf + 1]
+    rest = {n: tok[n][ptok:] for n in names}
+    rest["cu_seqlens"] = (tok["cu_seqlens"][npf:] - ptok).astype(np.int32)
+    poolB = K.StatePool(to_gpu_states(init).cuda())
+    ringB = K.ReplayRing(P, H, d, T, torch.bfloat16)
+    tbP, tbR = device_batch(pre, "bf16"), device_batch(rest, "bf16")
+    K.kda_prefill_chunked(tbP, poolB, i32(slots_np[:npf]), chunk=C, ckpt_every=128,
+                          ckpt_slots=i32(ck), start_pos=i32(starts))
+    K.kda_verify(tbR, T, poolB, i32(slots_np[npf:]), ringB, is_spec=i32(spec_mask))
+    torch.cuda.synchronize()
+    assert torch.equal(tbA.o[:ptok], tbP.o) and torch.equal(tbA.o[ptok:], tbR.o)
+    assert torch.equal(poolA.data, poolB.data)
+    for n in ("k", "v", "alpha", "beta", "ctrl"):
+        assert torch.equal(getattr(ringA, n), getattr(ringB, n))
+
+    sess = oracle.OracleSession(P, H, d, d, init=init)
+    o_pre, nck = sess.prefill(pre, slots_np[:npf], ckpt_every=128, ckpt_slots=ck,
+                              start_pos=np.asarray(starts, np.int32))
+    o_rest = sess.verify(rest, slots_np[npf:], is_spec=spec_mask)
+    assert list(nck) == [1, 1]
+    assert_outputs(tbA.o[:ptok].cpu().numpy(), o_pre)
+    assert_outputs(tbA.o[ptok:].cpu().numpy(), o_rest)
+    a = np.array([rng.integers(0, T + 1) if m else 0 for m in spec_mask], np.int32)
+    K.kda_commit(i32(a), i32(slots_np[npf:]), poolA, ringA)
+    sess.commit(a, slots_np[npf:])
+    K.kda_materialize(i32(slots_np[npf:]), poolA, ringA)
+    got = from_gpu_states(poolA.data)
+    for s in range(P):
+        assert_states(got[s], sess.pool[s])
+    assert K.kda_get_device_error() == 0
