@@ -20,6 +20,10 @@ compute on their own streams), `prefill` (chunked prefill with in-pass checkpoin
 1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region: the
 two-pass path through the workspace, and the single pass beside it),
 `clocks` (nvidia-smi samples during the timed region),
+`mixed` (the mixed-batch workload: 64 rows, 8 speculative + 56 ordinary, in
+256 shuffled slots, own timed region with its HBM roofline; and the same
+batch with a 2048-token prefill segment in front through kda_forward_mixed,
+one stream and with a side stream),
 `ablation_direct_snapshots` (the design ReplaySSM replaces -- the state
 stored at every drafted position, the accepted one copied at commit -- on the
 same workload, its own timed region; with both designs' algorithmic bytes
@@ -368,6 +372,132 @@ def run_prefill(torch, K, dev):
     }
 
 
+def decode_unit_bytes(d=D):
+    """Algorithmic bytes of an ordinary (one-token, committed at once) row's
+    (sequence, head) unit: state read and write, the token's inputs and
+    output, ctrl word and slot."""
+    return 2 * d * d * 4 + (4 * d * 2 + 2) + d * 4 + 8 + 4
+
+
+def run_mixed(torch, K, dev, steps=32, warmup=4, NL=4, prefill_len=2048):
+    """The mixed-batch workload: 64 sequences in 256 shuffled slots, 8
+    speculative (T = 8, accepted ~ U{0..8}) at seeded random positions among
+    56 ordinary one-token rows, one packed batch per step (kda_verify over all
+    64, then the commit); NL layer pools rotate so the state touched per step
+    (NL x 128 MiB) exceeds the L2.  Then the same batch with a 2048-token
+    prefill segment in front (checkpoint every 1024), one layer, through
+    kda_forward_mixed on one stream and with the prefill on a side stream."""
+    w = ki.MIXED
+    rng = np.random.default_rng(w.seed)
+    Bm, Pm, nspec, Tm = w.num_seqs, w.extra["num_slots"], w.extra["num_spec"], w.extra["T"]
+    slots_np = ki.slot_table(rng, Bm, Pm)
+    is_spec_np = np.zeros(Bm, np.int32)
+    is_spec_np[rng.choice(Bm, nspec, replace=False)] = 1
+    lens = [Tm if x else 1 for x in is_spec_np]
+    N = sum(lens)
+    slots = torch.as_tensor(slots_np, device=dev)
+    is_spec = torch.as_tensor(is_spec_np, device=dev)
+    pools = [K.StatePool.zeros(Pm + 3, H, D, device=dev) for _ in range(NL)]
+    rings = [K.ReplayRing(Pm + 3, H, D, Tm, torch.bfloat16, device=dev) for _ in range(NL)]
+
+    def batch(lengths):
+        tok = ki.gen_tokens(rng, lengths, H, D)
+        t = {n: torch.from_numpy(tok[n]).to(device=dev, dtype=torch.bfloat16)
+             for n in ("q", "k", "v", "alpha", "beta")}
+        cu = torch.as_tensor(tok["cu_seqlens"], device=dev)
+        return K.TokenBatch(t["q"], t["k"], t["v"], t["alpha"], t["beta"], cu)
+
+    G = 4
+    sets = [[batch(lens) for _ in range(NL)] for _ in range(G)]
+    A = 64
+    acc_np = np.where(is_spec_np[None, :] == 1,
+                      ki.accepted_uniform(rng, A * Bm, Tm).reshape(A, Bm), 0).astype(np.int32)
+    acc = torch.as_tensor(acc_np, device=dev)
+    stream = torch.cuda.current_stream()
+    evs = []
+    for s in range(warmup + steps):
+        rec = s >= warmup
+        for l in range(NL):
+            e0 = e1 = None
+            if rec:
+                e0, e1 = (torch.cuda.Event(enable_timing=True),
+                          torch.cuda.Event(enable_timing=True))
+                e0.record(stream)
+            K.kda_verify(sets[s % G][l], Tm, pools[l], slots, rings[l], is_spec=is_spec)
+            if rec:
+                e1.record(stream)
+                evs.append((e0, e1, s))
+        K.kda_commit_layers(acc[s % A], slots, pools[0], rings)
+        if s == warmup - 1:
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    durs = [a.elapsed_time(b) for a, b, _ in evs]
+    byts = []
+    for _, _, s in evs:
+        prev = acc_np[(s - 1) % A]
+        byts.append(float(sum(unit_bytes(int(prev[i])) if is_spec_np[i] else decode_unit_bytes()
+                              for i in range(Bm)) * H))
+    mean_us = float(np.mean(durs)) * 1e3
+    achieved = float(np.mean(byts)) / (mean_us * 1e-6) / 1e9
+    peak, _ = load_peaks()
+    bits = K.kda_get_device_error()
+
+    # the same decode batch with a prefill segment in front, one layer
+    mixed = batch([prefill_len] + lens)
+    pslots = torch.as_tensor(np.concatenate([[Pm], slots_np]).astype(np.int32), device=dev)
+    pspec = torch.as_tensor(np.concatenate([[0], is_spec_np]).astype(np.int32), device=dev)
+    ck = torch.tensor([[Pm + 1, Pm + 2]], dtype=torch.int32, device=dev)
+    sp = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = None
+    side = torch.cuda.Stream(device=dev)
+    acc_m = torch.as_tensor(np.concatenate([np.zeros((A, 1), np.int32), acc_np], 1), device=dev)
+
+    def mixed_ms(use_side, n=16):
+        nonlocal ws
+        out = []
+        for s in range(3 + n):
+            e0, e1 = (torch.cuda.Event(enable_timing=True),
+                      torch.cuda.Event(enable_timing=True))
+            e0.record(stream)
+            ws = K.kda_forward_mixed(mixed, 1, prefill_len, pools[0], pslots, 64, Tm, rings[0],
+                                     ckpt_every=1024, ckpt_slots=ck, start_pos=sp,
+                                     is_spec=pspec, workspace=ws,
+                                     side_stream=side if use_side else None)
+            K.kda_commit(acc_m[s % A], pslots, pools[0], rings[0])
+            e1.record(stream)
+            if s >= 3:
+                out.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in out]))
+
+    one = mixed_ms(False)
+    two = mixed_ms(True)
+    bits |= K.kda_get_device_error()
+    del pools, rings, sets, ws
+    torch.cuda.empty_cache()
+    return {
+        "workload": w.name, "kda_layers": NL, "steps": steps,
+        "tokens_per_step": N, "value": N * steps * NL / (ms * 1e-3), "unit": "tokens/s",
+        "ms_per_step": ms / steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "kernel": "verify_kernel<128, bf16> (64 rows)",
+                     "mean_launch_us": mean_us, "alg_bytes_per_launch": float(np.mean(byts))},
+        "with_prefill_segment": {
+            "prefill_tokens": prefill_len, "decode_tokens": N,
+            "ms_one_stream": one, "ms_side_stream": two,
+            "note": "kda_forward_mixed + commit, one layer: the prefill segment "
+                    "(two passes through the workspace) and the 64 decode rows "
+                    "of one packed batch, serial on one stream or with the "
+                    "prefill part forked onto a side stream"},
+        "device_error_bits": bits,
+    }
+
+
 CACHE_BUDGET_GIB = 46.48   # the pages' KV/state cache budget for the comparison
 
 
@@ -617,6 +747,7 @@ def run_kda(args, rank, world, local_rank):
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dist, dev)
 
     prefill = run_prefill(torch, K, dev)
+    mixed = run_mixed(torch, K, dev)
     direct = run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np,
                                    G, A)
     cache = state_cache_bytes()
@@ -667,6 +798,7 @@ def run_kda(args, rank, world, local_rank):
         "clocks": clocks.summary(w0, w1),
         "device_error_bits": bits,
         "prefill": prefill,
+        "mixed": mixed,
         "ablation_direct_snapshots": direct,
     }
     print(json.dumps(line), flush=True)
