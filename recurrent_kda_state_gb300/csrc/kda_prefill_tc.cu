@@ -739,7 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct Entry {                                 // byte offsets in an entry
   static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
   static constexpr uint32_t KT = 65536;        // K^^T hi, lo, [T; M] hi, lo
-  static constexpr uint32_t UP = 131072;       // U' [4 slices][64][32] fp32
+  static constexpr uint32_t UP = 131072;       // U' [4 slices][64][32] fp32, the
+                                               // 16-byte chunks of row t rotated by t
   static constexpr uint32_t VEC = 163840;      // e^{g_m}, e^{g_C}, e^{g_C-g_m}
   static constexpr uint32_t END = VEC + 3 * 128 * 4;
 };
@@ -1078,11 +1079,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float u[16];
         const int j0 = 64 * hf + 16 * blk;
         umma::tmem_ld16(tl + kAcc2 + 128 + j0, u);
-        float4 *dst = reinterpret_cast<float4 *>(
-            ent + Entry::UP + (((j0 >> 5) * 64 + t) * 32 + (j0 & 31)) * 4);
+        float4 *row = reinterpret_cast<float4 *>(ent + Entry::UP) + ((j0 >> 5) * 64 + t) * 8;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          dst[e] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+        for (int e = 0; e < 4; ++e)  // chunk (j mod 32) / 4 at position (chunk + t) mod 8
+          row[((((j0 & 31) >> 2) + e) + t) & 7] =
+              make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
       }
     }
     tiles_ready();
@@ -1203,14 +1204,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     const float *up = reinterpret_cast<const float *>(sm + LayS::SMALL +
                                                       (q & 1) * LayS::SMALL_BYTES);
     const float *vec = up + 64 * kNC;
-    if (tid == 0 && q + 2 < nch) {  // two chunks ahead: into L2
+    if (!(ok = tc_wait(g1bar, ph1, tid))) break;
+    owe1 = false;
+    if (tid == 32 && q + 2 < nch) {  // two chunks ahead: into L2 (not the MMA warp)
       const uint8_t *e = entry(q + 2);
       umma::prefetch_l2(e + Entry::GA, 131072);
       umma::prefetch_l2(e + Entry::UP + sl * 8192, 8192);
       umma::prefetch_l2(e + Entry::VEC, 1536);
     }
-    if (!(ok = tc_wait(g1bar, ph1, tid))) break;
-    owe1 = false;
     {  // S~ = Diag(e^{g_m}) S -> S~^T tile (row j, k = channel)
       const float egm = vec[c];
       float x[16];
@@ -1239,10 +1240,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       float ws[16], ws2[16];
       umma::tmem_ld16(tl + kA3 + 16 * hf, ws);
       umma::tmem_ld16(tl + kA3 + kNC + 16 * hf, ws2);
-      const float4 *u4 = reinterpret_cast<const float4 *>(up + t * kNC + 16 * hf);
+      const float4 *u4 = reinterpret_cast<const float4 *>(up + t * kNC);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 uv = u4[e];
+      for (int e = 0; e < 4; ++e) {  // rotated chunks: 8 rows hit 8 bank groups
+        const float4 uv = u4[(4 * hf + e + t) & 7];
         ws[4 * e] = uv.x - (ws[4 * e] + ws2[4 * e]);
         ws[4 * e + 1] = uv.y - (ws[4 * e + 1] + ws2[4 * e + 1]);
         ws[4 * e + 2] = uv.z - (ws[4 * e + 2] + ws2[4 * e + 2]);
@@ -1274,6 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     mma_owed = true;
     if (!(ok = tc_wait(mbar, phase, tid))) break;
     mma_owed = false;
+    if (q + 1 < nch) issue_g2(q + 1);  // K^ and [T; M] are free
     {
       float acc[16], acc2[16];
       umma::tmem_ld16(tl + kA4 + 16 * hf, acc);
@@ -1314,7 +1316,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
-    if (q + 1 < nch) issue_g2(q + 1);  // K^^T and [T; M] are free
   }
   if (!ok) {
     if (tid == 0) {
