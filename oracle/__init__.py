@@ -8,6 +8,7 @@ from .kda_oracle import (  # noqa: F401
     OracleSession,
     num_threads,
     prefill,
+    prep_inputs,
     set_num_threads,
     step,
     verify,

@@ -158,6 +158,21 @@ def commit(cu_seqlens, q, k, v, alpha, beta, accepted_len, S):
     return S
 
 
+def prep_inputs(q, k_raw, z_alpha, z_beta):
+    """The input-side preparation in front of the path, in fp64: the pages do
+    not define it, so it follows the input generator's formulas for the
+    synthetic workloads -- each key L2-normalised over d_k per (token, head),
+    alpha = exp(-softplus(z_alpha)) per key channel, beta = sigmoid(z_beta)
+    per (token, head); q is used as given.  Returns (q, k, alpha, beta)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k_raw, dtype=np.float64)
+    nrm = np.sqrt((k * k).sum(-1, keepdims=True))
+    k = k / np.maximum(nrm, 1e-12)
+    alpha = np.exp(-np.logaddexp(0.0, np.asarray(z_alpha, dtype=np.float64)))
+    beta = 1.0 / (1.0 + np.exp(-np.asarray(z_beta, dtype=np.float64)))
+    return q, k, alpha, beta
+
+
 class OracleSession:
     """Paged state pool plus the speculative protocol, evaluated eagerly.
 

@@ -285,3 +285,44 @@ def test_capped_geometric_reading():
     assert abs(a.mean() - 4.70) < 0.03
     assert abs((a == 0).mean() - (1 - rho)) < 0.01
     assert abs((a == 8).mean() - rho ** 8) < 0.01
+
+
+# ------------------------------------------------------------ input prep
+def test_prep_inputs_closed_forms():
+    """The input prep (the generator's formulas) against values fixed by the
+    mathematics: softplus(0) = ln 2, so z = 0 gives alpha = 1/2 exactly;
+    sigmoid(0) = 1/2; alpha -> e^{-z} for large z and -> 1 for very negative
+    z; sigmoid is odd about 1/2; a 3-4-5 key normalises to (0.6, 0.8); a zero
+    key stays zero; q passes through."""
+    q = np.array([[[1.5, -2.0]]])
+    k = np.array([[[3.0, 4.0]]])
+    z = np.array([[[0.0, 40.0]]])
+    b = np.array([[0.0]])
+    q2, k2, a2, b2 = oracle.prep_inputs(q, k, z, b)
+    assert np.array_equal(q2, q)
+    assert np.allclose(k2, [[[0.6, 0.8]]], rtol=0, atol=1e-15)
+    assert a2[0, 0, 0] == 0.5
+    assert abs(a2[0, 0, 1] / np.exp(-40.0) - 1.0) < 1e-12
+    assert b2[0, 0] == 0.5
+    _, _, a3, b3 = oracle.prep_inputs(q, k, np.array([[[-40.0, 3.0]]]),
+                                      np.array([[2.5]]))
+    assert abs(a3[0, 0, 0] - 1.0) < 1e-15
+    assert abs(a3[0, 0, 1] - 1.0 / (1.0 + np.exp(3.0))) < 1e-15  # exp(-softplus(z)) = sigmoid(-z)
+    _, _, _, b4 = oracle.prep_inputs(q, k, z, np.array([[-2.5]]))
+    assert abs(b3[0, 0] + b4[0, 0] - 1.0) < 1e-15
+    _, k5, _, _ = oracle.prep_inputs(q, np.zeros((1, 1, 2)), z, b)
+    assert np.array_equal(k5, np.zeros((1, 1, 2)))
+
+
+def test_prep_inputs_matches_generator():
+    """Random projections: unit-norm keys parallel to the raw keys, and
+    alpha, beta as the generator draws them from the same normal values."""
+    rng = np.random.default_rng(8)
+    kr = rng.standard_normal((5, 3, 16)) * 3.0
+    z = rng.standard_normal((5, 3, 16))
+    b = rng.standard_normal((5, 3))
+    _, k, a, bb = oracle.prep_inputs(np.zeros_like(kr), kr, z, b)
+    assert np.allclose(np.linalg.norm(k, axis=-1), 1.0, atol=1e-14)
+    assert np.allclose(k * np.linalg.norm(kr, axis=-1, keepdims=True), kr, atol=1e-12)
+    assert np.allclose(a, 1.0 / (1.0 + np.exp(z)), atol=1e-15)
+    assert np.allclose(bb, 1.0 / (1.0 + np.exp(-b)), atol=1e-15)
