@@ -348,7 +348,25 @@ def run_prefill(torch, K, dev):
 
     ms = timed(False)
     ms_single = timed(True)
-    del ws
+    # the same prefill on projection-space inputs, prep fused into the kernels
+    rtok = ki.gen_raw_tokens(rng, [L], H, D)
+    rt = {n: torch.from_numpy(rtok[n]).to(device=dev, dtype=torch.bfloat16)
+          for n in ("q", "k", "v", "alpha", "beta")}
+    rtb = K.TokenBatch(rt["q"], rt["k"], rt["v"], rt["alpha"], rt["beta"], cu)
+    for _ in range(3):
+        K.kda_prefill_chunked(rtb, pool, slots, C, E, ck, workspace=ws, raw=True)
+    revs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(reps)]
+    torch.cuda.synchronize()
+    for e0, e1 in revs:
+        e0.record(stream)
+        K.kda_prefill_chunked(rtb, pool, slots, C, E, ck, workspace=ws, raw=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_raw = float(np.mean([a.elapsed_time(b) for a, b in revs]))
+    # a separate prep pass would read the raw k, alpha, beta and write them back
+    prep_bytes = 2 * (L * H * (2 * D) * 2 + L * H * 2)
+    del ws, rt, rtb
     torch.cuda.empty_cache()
     alg_bytes = (L * H * (4 * D * 2 + 2) + L * H * D * 4
                  + (2 + L // E) * H * D * D * 4)
@@ -361,6 +379,10 @@ def run_prefill(torch, K, dev):
         "workspace_bytes": ws_bytes,
         "single_pass_ms": ms_single,
         "single_pass_tokens_per_s": L / (ms_single * 1e-3),
+        "raw_inputs_fused_prep_ms": ms_raw,
+        "raw_inputs_note": "kda_prefill_chunked_raw (two passes): raw keys, decay "
+                           "and beta logits, prep fused into the kernels; a "
+                           "separate prep pass would move %d bytes" % prep_bytes,
         "note": "two tcgen05 passes through the workspace: every (chunk, head) "
                 "computes its state-independent operands at once (tile images, "
                 "U', decay vectors), then one CTA per (32-column value slice, "

@@ -160,6 +160,27 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
                         const int32_t *start_pos, void *workspace,
                         size_t workspace_bytes, kda_stream_t stream);
 
+/*
+ * kda_prefill_chunked_raw -- kda_prefill_chunked on projection-space inputs,
+ * with the input-side preparation fused into the kernels instead of a
+ * separate pass over the tokens (the pages leave the preparation open; it
+ * follows the formulas the synthetic workloads are drawn with):
+ *   k     : raw keys, L2-normalised over d_k per (token, head) in-kernel;
+ *   alpha : decay logits z, alpha = exp(-softplus(z)) per key channel;
+ *   beta  : logits b, beta = sigmoid(b) per (token, head);
+ *   q, v  : used as given.
+ * The prep runs in fp32 on the values as given (nothing is rounded to the
+ * input dtype in between).  Only the tensor-core shape (bf16 inputs,
+ * d_k = d_v = 128, chunk 64, heads a multiple of 8) is supported; other
+ * shapes return KDA_ESHAPE.  Arguments and outputs otherwise as
+ * kda_prefill_chunked (workspace optional at that shape).
+ */
+int kda_prefill_chunked_raw(const kda_tokens *tok, kda_state_pool *pool,
+                            const int32_t *state_slots, const int32_t *ckpt_slots,
+                            int32_t max_ckpt, int32_t ckpt_every, int32_t chunk,
+                            const int32_t *start_pos, void *workspace,
+                            size_t workspace_bytes, kda_stream_t stream);
+
 /* Bytes of workspace kda_prefill_chunked needs for these sizes and input
  * dtype (at the tensor-core shape: for the two-pass path, about 162 KiB per
  * (chunk of 64 tokens, head)), and 0 on bad arguments (which the prefill call

@@ -80,6 +80,24 @@ def gen_tokens(rng, lengths, H, dk, dv=None):
                 alpha=alpha.astype(f), beta=beta.astype(f), cu_seqlens=cu)
 
 
+def gen_raw_tokens(rng, lengths, H, dk, dv=None):
+    """Projection-space tokens for the fused-prep prefill (fp32 numpy): the
+    draws gen_tokens prepares -- raw keys k ~ N(0, 1) (not normalised), decay
+    logits alpha ~ N(0, 1), logits beta ~ N(0, 1), q, v ~ N(0, 1).  The
+    preparation itself belongs to the path under test and to the oracle."""
+    dv = dk if dv is None else dv
+    lengths = np.asarray(lengths, dtype=np.int64)
+    N = int(lengths.sum())
+    cu = np.zeros(len(lengths) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lengths)
+    f = np.float32
+    return dict(q=rng.standard_normal((N, H, dk)).astype(f),
+                k=rng.standard_normal((N, H, dk)).astype(f),
+                v=rng.standard_normal((N, H, dv)).astype(f),
+                alpha=rng.standard_normal((N, H, dk)).astype(f),
+                beta=rng.standard_normal((N, H)).astype(f), cu_seqlens=cu)
+
+
 def round_to(tok, dtype):
     """Round the float tensors of ``tok`` to ``dtype`` ("f32" or "bf16").
 

@@ -133,7 +133,8 @@ namespace {
 int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *state_slots,
                  const int32_t *ckpt_slots, int32_t max_ckpt, int32_t ckpt_every,
                  int32_t chunk, const int32_t *start_pos, void *workspace,
-                 size_t workspace_bytes, kda_stream_t stream, bool cu_aligned) {
+                 size_t workspace_bytes, kda_stream_t stream, bool cu_aligned,
+                 bool raw = false) {
   int st = check_pool(pool);
   if (st) return st;
   if ((st = check_tokens(tok, pool, cu_aligned))) return st;
@@ -144,6 +145,7 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
   if (tok->num_seqs == 0) return KDA_OK;
   if (!state_slots) return KDA_EINVAL;
   const bool tc = kda::prefill_uses_tc(tok->dtype, tok->num_heads, tok->d_k, tok->d_v, chunk);
+  if (raw && !tc) return KDA_ESHAPE;  // the prep is fused into the tensor-core kernels
   // the CUDA-core kernels and the two-pass tensor-core kernels work in the
   // caller's workspace; at the tensor-core shape a NULL workspace selects the
   // single pass
@@ -181,6 +183,7 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
   p.max_ckpt = max_ckpt;
   p.ckpt_every = ckpt_every;
   p.max_chunks = kda::prefill_max_chunks(tok->num_tokens, tok->num_seqs, chunk);
+  p.raw = raw ? 1 : 0;
   return cuda_status(kda::launch_prefill(p, tok->dtype, tok->d_k, chunk,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -227,6 +230,15 @@ int kda_prefill_chunked(const kda_tokens *tok, kda_state_pool *pool,
                         size_t workspace_bytes, kda_stream_t stream) {
   return prefill_impl(tok, pool, state_slots, ckpt_slots, max_ckpt, ckpt_every, chunk,
                       start_pos, workspace, workspace_bytes, stream, true);
+}
+
+int kda_prefill_chunked_raw(const kda_tokens *tok, kda_state_pool *pool,
+                            const int32_t *state_slots, const int32_t *ckpt_slots,
+                            int32_t max_ckpt, int32_t ckpt_every, int32_t chunk,
+                            const int32_t *start_pos, void *workspace,
+                            size_t workspace_bytes, kda_stream_t stream) {
+  return prefill_impl(tok, pool, state_slots, ckpt_slots, max_ckpt, ckpt_every, chunk,
+                      start_pos, workspace, workspace_bytes, stream, true, true);
 }
 
 int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,

@@ -119,6 +119,7 @@ struct PrefillParams {
   unsigned char *ws;          // workspace (chunk table + per-chunk operands)
   unsigned int *err;
   int B, N, H, P, max_ckpt, ckpt_every, max_chunks;
+  int raw;  // inputs are projections: k unnormalised, alpha and beta logits
 };
 
 // Workspace geometry of the chunked prefill (shared with the size query):

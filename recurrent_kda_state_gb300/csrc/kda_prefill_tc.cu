@@ -224,6 +224,39 @@ __device__ void unit_lower_inverse(const float *A, float *X, float *P, int tid) 
   __syncthreads();
 }
 
+// Input prep for projection-space inputs (the generator's formulas; the
+// pages leave it open): log alpha = -softplus(z), beta = sigmoid(b), and the
+// key's inverse L2 norm over the 128 channels of one (token, head).
+__device__ __forceinline__ float neg_softplus(float z) {
+  return -(fmaxf(z, 0.f) + __logf(1.f + __expf(-fabsf(z))));
+}
+__device__ __forceinline__ float sigmoid_f(float b) {
+  return __fdividef(1.f, 1.f + __expf(-b));
+}
+// E1 thread (channel pair cp, token quarter tq) holding bf16 key pairs kr[u]
+// of tokens 16 tq + u: per-token sums of squares over the 64 channel pairs
+// (two warps per quarter) -> scr[warp][u]; after a barrier, norm_finish
+// turns them into inverse norms nrm[t] (threads cp == 0).
+__device__ __forceinline__ void norm_partials(const uint32_t (&kr)[16], float *scr, int tid) {
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float k0 = __uint_as_float(kr[u] << 16), k1 = __uint_as_float(kr[u] & 0xffff0000u);
+    float x = fmaf(k0, k0, k1 * k1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if ((tid & 31) == 0) scr[(tid >> 5) * 16 + u] = x;
+  }
+}
+__device__ __forceinline__ void norm_finish(const float *scr, float *nrm, int tid) {
+  if ((tid & 63) == 0) {
+    const int tq = tid >> 6;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      nrm[16 * tq + u] = rsqrtf(fmaxf(scr[(2 * tq) * 16 + u] + scr[(2 * tq + 1) * 16 + u],
+                                      1e-24f));
+  }
+}
+
 // Descriptor of a tile `off` bytes past the one `d` describes (the start
 // address field counts 16-byte units).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t off) {
@@ -284,6 +317,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
 }
 
 
+template <bool RAW>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
   extern __shared__ float4 smem4[];
@@ -376,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     stage_owed = false;
     if (tid < kC) {
       const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + Lay::BST)[tid * 8 + (h & 7)];
-      bet[tid] = tid < n ? __uint_as_float((uint32_t)bw << 16) : 0.f;
+      const float bv = __uint_as_float((uint32_t)bw << 16);
+      bet[tid] = tid < n ? (RAW ? sigmoid_f(bv) : bv) : 0.f;
     }
     const int cp = tid & 63, tq = tid >> 6, c2 = 2 * cp, tb0 = 16 * tq;
     float la0[16], la1[16];
@@ -391,10 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aw = sa[t * 64 + cp];
         kr[u] = t < n ? sk[t * 64 + cp] : 0u;
         qr[u] = t < n ? sq[t * 64 + cp] : 0u;
-        la0[u] = t < n ? __logf(__uint_as_float(aw << 16)) : 0.f;
-        la1[u] = t < n ? __logf(__uint_as_float(aw & 0xffff0000u)) : 0.f;
+        const float a0 = __uint_as_float(aw << 16), a1 = __uint_as_float(aw & 0xffff0000u);
+        la0[u] = t < n ? (RAW ? neg_softplus(a0) : __logf(a0)) : 0.f;
+        la1[u] = t < n ? (RAW ? neg_softplus(a1) : __logf(a1)) : 0.f;
       }
     }
+    float *nscr = reinterpret_cast<float *>(sm + Lay::PT);   // key norms (raw inputs)
+    float *nrm = nscr + 128;
+    if (RAW) norm_partials(kr, nscr, tid);
     uint32_t vw[4];
     {
       const int j = tid & 31, tg = tid >> 5;
@@ -434,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sgc[c2 + 1] = la1[15];
       }
     }
+    if (RAW) norm_finish(nscr, nrm, tid);
     __syncthreads();
     {
       const float gm0 = sgm[c2], gm1 = sgm[c2 + 1];
@@ -455,8 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tb0 + u;
         const float f0 = __expf(la0[u] - gm0), fi0 = __expf(gm0 - la0[u]);
         const float f1 = __expf(la1[u] - gm1), fi1 = __expf(gm1 - la1[u]);
-        const float k0 = __uint_as_float(kr[u] << 16);
-        const float k1 = __uint_as_float(kr[u] & 0xffff0000u);
+        const float kn = RAW ? nrm[t] : 1.f;
+        const float k0 = __uint_as_float(kr[u] << 16) * kn;
+        const float k1 = __uint_as_float(kr[u] & 0xffff0000u) * kn;
         const float q0 = __uint_as_float(qr[u] << 16);
         const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
         uint32_t hi, lo;
@@ -801,6 +842,7 @@ __device__ __forceinline__ void put16_mn(uint8_t *sm, uint32_t tile, int k, int 
   st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0 + 8), l[4], l[5], l[6], l[7]);
 }
 
+template <bool RAW>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_chunk_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
   extern __shared__ float4 smem4[];
@@ -866,7 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- E1 (as in the fused kernel; V^T over all 128 value columns)
     if (tid < kC) {
       const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + LayP::BST)[tid * 8 + (h & 7)];
-      bet[tid] = tid < n ? __uint_as_float((uint32_t)bw << 16) : 0.f;
+      const float bv = __uint_as_float((uint32_t)bw << 16);
+      bet[tid] = tid < n ? (RAW ? sigmoid_f(bv) : bv) : 0.f;
     }
     const int cp = tid & 63, tq = tid >> 6, c2 = 2 * cp, tb0 = 16 * tq;
     float la0[16], la1[16];
@@ -881,10 +924,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aw = sa[t * 64 + cp];
         kr[u] = t < n ? sk[t * 64 + cp] : 0u;
         qr[u] = t < n ? sq[t * 64 + cp] : 0u;
-        la0[u] = t < n ? __logf(__uint_as_float(aw << 16)) : 0.f;
-        la1[u] = t < n ? __logf(__uint_as_float(aw & 0xffff0000u)) : 0.f;
+        const float a0 = __uint_as_float(aw << 16), a1 = __uint_as_float(aw & 0xffff0000u);
+        la0[u] = t < n ? (RAW ? neg_softplus(a0) : __logf(a0)) : 0.f;
+        la1[u] = t < n ? (RAW ? neg_softplus(a1) : __logf(a1)) : 0.f;
       }
     }
+    float *nscr = reinterpret_cast<float *>(sm + LayP::PT);   // key norms (raw inputs)
+    float *nrm = nscr + 128;
+    if (RAW) norm_partials(kr, nscr, tid);
 #pragma unroll
     for (int u = 1; u < 16; ++u) {
       la0[u] += la0[u - 1];
@@ -914,6 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sgc[c2 + 1] = la1[15];
       }
     }
+    if (RAW) norm_finish(nscr, nrm, tid);
     __syncthreads();
     {
       const float gm0 = sgm[c2], gm1 = sgm[c2 + 1];
@@ -934,8 +982,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tb0 + u;
         const float f0 = __expf(la0[u] - gm0), fi0 = __expf(gm0 - la0[u]);
         const float f1 = __expf(la1[u] - gm1), fi1 = __expf(gm1 - la1[u]);
-        const float k0 = __uint_as_float(kr[u] << 16);
-        const float k1 = __uint_as_float(kr[u] & 0xffff0000u);
+        const float kn = RAW ? nrm[t] : 1.f;
+        const float k0 = __uint_as_float(kr[u] << 16) * kn;
+        const float k1 = __uint_as_float(kr[u] & 0xffff0000u) * kn;
         const float q0 = __uint_as_float(qr[u] << 16);
         const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
         // K~ and Q~ rows of [K~; Q~] and the K^ rows: K-major for R1, and the
@@ -1411,16 +1460,16 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (e == cudaSuccess) e = beta_map(&maps.b, p.beta, p.N, p.H);
   if (e != cudaSuccess) return e;
   if (!two) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Lay::kBytes);
+    auto k1 = p.raw ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, Lay::kBytes, s>>>(p, maps);
+    k1<<<dim3(kD / kNC, p.H, p.B), kThreads, Lay::kBytes, s>>>(p, maps);
     return cudaGetLastError();
   }
   e = launch_chunk_table(p, kC, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_tc_chunk_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayP::kBytes);
+  auto kp1 = p.raw ? prefill_tc_chunk_kernel<true> : prefill_tc_chunk_kernel<false>;
+  e = cudaFuncSetAttribute(kp1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayP::kBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(prefill_tc_pass_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayS::kBytes);
@@ -1432,7 +1481,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   // one CTA per SM walks the (chunk, head) items (the last ones exit at once)
   const long long items = (long long)p.max_chunks * p.H;
   const int grid1 = (int)(items < sms ? items : sms);
-  prefill_tc_chunk_kernel<<<grid1, kThreads, LayP::kBytes, s>>>(p, maps);
+  kp1<<<grid1, kThreads, LayP::kBytes, s>>>(p, maps);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prefill_tc_pass_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, LayS::kBytes, s>>>(p);

@@ -41,7 +41,7 @@ class kda_replay_ring(ctypes.Structure):
                 ("ctrl", _P), ("depth", _I32), ("dtype", ctypes.c_int)]
 
 
-EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_noalloc",
+EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_raw", "kda_prefill_chunked_noalloc",
            "kda_prefill_workspace_size", "kda_verify",
            "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
            "kda_gather_states", "kda_copy_slots", "kda_verify_snapshot",
@@ -63,6 +63,8 @@ def lib():
                       ctypes.POINTER(kda_replay_ring))
         L.kda_prefill_chunked.argtypes = [tp, pp, _P, _P, _I32, _I32, _I32, _P,
                                           _P, ctypes.c_size_t, _P]
+        L.kda_prefill_chunked_raw.argtypes = [tp, pp, _P, _P, _I32, _I32, _I32, _P,
+                                              _P, ctypes.c_size_t, _P]
         L.kda_prefill_chunked_noalloc.argtypes = [tp, pp, _P, _P, _I32, _I32,
                                                   _I32, _P, _P]
         L.kda_prefill_workspace_size.argtypes = [_I32] * 6 + [ctypes.c_int]
@@ -177,10 +179,11 @@ def kda_prefill_workspace_size(num_tokens, num_seqs, H, d_k, d_v, chunk, dtype):
 
 def kda_prefill_chunked(tok, pool, state_slots, chunk, ckpt_every=0,
                         ckpt_slots=None, start_pos=None, workspace=None,
-                        stream=None, single_pass=False):
+                        stream=None, single_pass=False, raw=False):
     """Chunked prefill; ckpt_slots [B][max_ckpt] int32 (device) or None.
     workspace None: one of the required size is allocated here;
-    single_pass: pass no workspace (the tensor-core shape's single pass)."""
+    single_pass: pass no workspace (the tensor-core shape's single pass);
+    raw: projection-space inputs, prep fused (kda_prefill_chunked_raw)."""
     max_ckpt = 0 if ckpt_slots is None else int(ckpt_slots.shape[1])
     if single_pass:
         workspace = None
@@ -190,11 +193,13 @@ def kda_prefill_chunked(tok, pool, state_slots, chunk, ckpt_every=0,
                                             tok.c.d_v, chunk, tok.c.dtype)
         if nbytes > 0:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=tok.k.device)
-    _check(lib().kda_prefill_chunked(
+    fn, name = ((lib().kda_prefill_chunked_raw, "kda_prefill_chunked_raw") if raw
+                else (lib().kda_prefill_chunked, "kda_prefill_chunked"))
+    _check(fn(
         ctypes.byref(tok.c), ctypes.byref(pool.c), _ptr(state_slots),
         _ptr(ckpt_slots), max_ckpt, ckpt_every, chunk, _ptr(start_pos),
         _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        _stream(stream)), "kda_prefill_chunked")
+        _stream(stream)), name)
     return workspace
 
 

@@ -187,3 +187,12 @@ def test_forward_mixed_validation(L):
     none = _tokens(B=0, N=0)
     assert L.kda_forward_mixed(by(none), 0, 0, by(pool), None, None, 0, 0, 16, None,
                                None, 0, 4, by(ring), None, None, None) == kda.KDA_OK
+
+
+def test_prefill_raw_needs_the_tensor_core_shape(L):
+    """The fused-prep prefill exists only where the prep is fused."""
+    pool, tok = _pool(), _tokens()
+    s = ctypes.c_void_p(0x40000)
+    ws = ctypes.c_void_p(0x80000)
+    assert L.kda_prefill_chunked_raw(ctypes.byref(tok), ctypes.byref(pool), s, None, 0, 0,
+                                     16, None, ws, 1 << 20, None) == kda.KDA_ESHAPE

@@ -636,3 +636,41 @@ def test_forward_mixed_prefill_and_verify_segments(use_side):
     for s in range(P):
         assert_states(got[s], sess.pool[s])
     assert K.kda_get_device_error() == 0
+
+
+# ------------------------------------------------ fused input preparation
+@pytest.mark.parametrize("single_pass", [False, True], ids=["two_pass", "single_pass"])
+@pytest.mark.parametrize("case", ["ragged", "full"])
+def test_prefill_raw_inputs_fused_prep(single_pass, case):
+    """kda_prefill_chunked_raw: projection-space inputs (raw keys, decay and
+    beta logits) with the prep fused into the tensor-core kernels, against
+    the oracle's fp64 prep followed by its prefill; ragged lengths and start
+    offsets at 8 heads, and the full 8192-token workload (heads sampled)."""
+    if case == "full":
+        lengths, starts, H, E, mc, hs, seed = [8192], [0], 32, 1024, 8, [0, 17, 31], 931
+    else:
+        lengths, starts = [0, 1, 63, 64, 65, 197, 100], [0, 5, 0, 128, 61, 7, 0]
+        H, E, mc, hs, seed = 8, 128, 3, [0, 3, 4, 7], 932
+    d, C = 128, 64
+    rng = np.random.default_rng(seed)
+    raw = ki.round_to(ki.gen_raw_tokens(rng, lengths, H, d), "bf16")
+    B = len(lengths)
+    P = B * (1 + mc) + 1
+    init = ki.initial_states(rng, P, H, d, d, 0.05)
+    pool = K.StatePool(to_gpu_states(init).cuda())
+    slots_np = np.arange(B, dtype=np.int32)
+    ck = (B + np.arange(B * mc, dtype=np.int32)).reshape(B, mc)
+    tb = device_batch(raw, "bf16")
+    K.kda_prefill_chunked(tb, pool, i32(slots_np), chunk=C, ckpt_every=E, ckpt_slots=i32(ck),
+                          start_pos=i32(starts), single_pass=single_pass, raw=True)
+    q, k, a, b = oracle.prep_inputs(raw["q"], raw["k"], raw["alpha"], raw["beta"])
+    prep = dict(q=q, k=k, v=raw["v"].astype(np.float64), alpha=a, beta=b,
+                cu_seqlens=raw["cu_seqlens"])
+    sess = oracle.OracleSession(P, len(hs), d, d, init=init[:, hs])
+    o_ref, _ = sess.prefill(heads(prep, hs), slots_np, ckpt_every=E, ckpt_slots=ck,
+                            start_pos=np.asarray(starts, np.int32))
+    assert_outputs(tb.o[:, hs].cpu().numpy(), o_ref)
+    got = from_gpu_states(pool.data[:, hs])
+    for s in range(P):
+        assert_states(got[s], sess.pool[s])
+    assert K.kda_get_device_error() == 0
