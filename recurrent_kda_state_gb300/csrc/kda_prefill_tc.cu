@@ -2,9 +2,7 @@
 // d_k = d_v = 128, chunk 64, bf16 inputs, heads a multiple of 8, with the in-pass checkpoints of
 // "KDA checkpoints stay inside the prefill" (vLLM Kimi K3 optimisation page).
 //
-// One CTA per (value-column slice of NC columns, head, sequence) walks the
-// sequence's chunks in order; nothing goes through a workspace.  Per chunk of
-// C tokens with g_t = sum_{s<=t} log alpha_s (per key channel) and a
+// Per chunk of C tokens with g_t = sum_{s<=t} log alpha_s (per key channel) and a
 // reference row m in the middle of the chunk (every factor below stays within
 // e^{+-80}, checked), with K~ = e^{g-g_m} K, Q~ = e^{g-g_m} Q, K^ = e^{-(g-g_m)} K
 // and S~ = Diag(e^{g_m}) S (S the chunk-start state slice):
@@ -20,12 +18,25 @@
 // This is the chunk (WY/UT) form of the gated delta rule with the factor
 // pairs re-referenced to row m; the triangles of A and M keep it exact.
 //
+// Two ways to run it:
+//   - prefill_tc_kernel, no workspace: one CTA per (value-column slice of NC
+//     columns, head, sequence) walks the sequence's chunks and does all of
+//     the above per chunk;
+//   - with a workspace, prefill_tc_chunk_kernel first does everything up to
+//     R2 for every (chunk, head) at once and writes the chunk's operands as
+//     shared-memory images, then prefill_tc_pass_kernel walks the chunks with
+//     R3, R4 and the state only (see the comment above those kernels).
+// With projection-space inputs (RAW) E1 also prepares them: keys L2-
+// normalised, log alpha = -softplus(z), beta = sigmoid(b).
+//
 // Precision: every operand that is not an exact bf16 input is split into
 // bf16 hi + lo and each product runs as hi*hi + lo*hi + hi*lo (three
-// kind::f16 MMAs into one fp32 accumulator, ~2^-16 relative per product); V
-// is an exact bf16 input and takes two.  The state stays fp32 in registers.
+// kind::f16 MMAs into one fp32 accumulator, ~2^-16 relative per product; the
+// chunk walk's stacked form adds lo*lo); V is an exact bf16 input and takes
+// two.  The state stays fp32 in registers.
 //
-// Shared-memory operand tiles are K-major with the 128-byte swizzle (see
+// Shared-memory operand tiles are 128-byte swizzled, K-major or, where the
+// same bytes serve a second product transposed, read MN-major (see
 // kda_umma.cuh); the TMEM accumulators sit at fixed columns.
 #include <cuda.h>
 
