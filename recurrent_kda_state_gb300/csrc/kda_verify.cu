@@ -491,10 +491,7 @@ __global__ void __launch_bounds__(2 * D, 2)
     if (tid == 0) set_error(p.err, (unsigned)bad);
     return;
   }
-  // speculative rows with drafts take their tensor-memory columns now, while
-  // the loads below are in flight
   const bool drafts = spec && T > 0;
-  if (drafts && tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)(4 * TP));
 
   // Round trip 2, all independent: the state (16-byte loads, 4 lanes per 64
   // contiguous bytes of a column), the ring control word, every ring entry
@@ -513,6 +510,10 @@ __global__ void __launch_bounds__(2 * D, 2)
       S[1][2 * f] = y.x; S[1][2 * f + 1] = y.y;
     }
   }
+  // speculative rows with drafts take their tensor-memory columns now, while
+  // the state's loads are in flight (an allocation costs the warp about as
+  // long as a DRAM round trip)
+  if (drafts && tid < 32) umma::tmem_alloc(&s_tmem, (uint32_t)(4 * TP));
   if (tid == 0) {
     const int32_t *c = p.ctrl + unit * 2;
     const int pend = c[0], acc = c[1];
