@@ -767,6 +767,11 @@ def run_kda(args, rank, world, local_rank):
     f1.record(d2h_s)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dist, dev)
+    # the graphs' timing events were recorded again by this pass: the verify
+    # launches' duration while the copies ran beside them
+    e2e_launch_us = float(np.mean([events[s][l][0].elapsed_time(events[s][l][1])
+                                   for s in range(args.warmup, total_steps)
+                                   for l in range(NL)])) * 1e3
 
     prefill = run_prefill(torch, K, dev)
     mixed = run_mixed(torch, K, dev)
@@ -815,7 +820,9 @@ def run_kda(args, rank, world, local_rank):
                      "alg_bytes_per_launch": float(np.mean(abytes))},
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e / args.steps,
+                "verify_launch_us_during_copies": e2e_launch_us},
         "gpu_launches": (NL + 1) * args.steps,
         "clocks": clocks.summary(w0, w1),
         "device_error_bits": bits,
