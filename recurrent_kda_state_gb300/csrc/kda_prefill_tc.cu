@@ -60,7 +60,7 @@ struct Lay {
   static constexpr uint32_t GB_LO = 81920;
   static constexpr uint32_t AF = 65536;      // after R1: A fp32 64 x 68
   static constexpr uint32_t XF = 82944;      //           X fp32 64 x 68
-  static constexpr uint32_t UT_HI = 65536;   // after the solve: U^T NC x 64
+  static constexpr uint32_t UT_HI = 65536;   // after the solve: U, MN-major 64 x [hi|lo]
   static constexpr uint32_t UT_LO = UT_HI + kNC * 128;
   static constexpr uint32_t B2_HI = 101376;  // [K~^T; V^T]: (128 + NC) x 64
   static constexpr uint32_t B2_LO = B2_HI + (128 + kNC) * 128;  // K~^T lo
@@ -68,7 +68,7 @@ struct Lay {
   static constexpr uint32_t KH_LO = KH_HI + 16384;
   static constexpr uint32_t TM_HI = KH_LO + 16384;  // [T; M]: 128 x 64
   static constexpr uint32_t TM_LO = TM_HI + 16384;
-  static constexpr uint32_t SB_HI = TM_LO + 16384;  // S~^T: NC x 128
+  static constexpr uint32_t SB_HI = TM_LO + 16384;  // S~: MN-major 128 x [hi|lo]
   static constexpr uint32_t SB_LO = SB_HI + kNC * 256;
   static constexpr uint32_t MISC = SB_LO + kNC * 256;
   // misc (floats unless noted)
@@ -102,18 +102,18 @@ static_assert(kStgV + 64 * kNC * 2 <= Lay::XF, "V staging");
 static_assert(Lay::kBytes <= 232448, "shared memory per CTA");
 
 // TMEM columns of the accumulators (512 allocated).
+// R3 and R4 take the hi and lo splits of their B operand stacked along N
+// (N = 64): columns 0..31 of kAcc3 / kAcc4 hold hi*hi + lo*hi, 32..63 hi*lo +
+// lo*lo, and a result is their sum.
 constexpr uint32_t kAccG = 0, kAcc2 = 64, kAcc3 = 64 + 128 + kNC,
-                   kAcc4 = kAcc3 + kNC;
-static_assert(kAcc4 + kNC <= 512, "TMEM columns");
+                   kAcc4 = kAcc3 + 2 * kNC;
+static_assert(kAcc4 + 2 * kNC <= 512, "TMEM columns");
 
 // Index of element (r, c) of a 64 x 64 fp32 array with rows 68 floats apart:
 // rows stay 16-byte aligned and a column's 8 consecutive rows fall in
 // distinct banks.
 __device__ __forceinline__ int fo(int r, int c) { return r * 68 + c; }
 
-__device__ __forceinline__ void st_u16(uint8_t *base, uint32_t off, uint16_t v) {
-  *reinterpret_cast<uint16_t *>(base + off) = v;
-}
 __device__ __forceinline__ void st_v4(uint8_t *base, uint32_t off, uint32_t a,
                                       uint32_t b, uint32_t c, uint32_t d) {
   *reinterpret_cast<uint4 *>(base + off) = make_uint4(a, b, c, d);
@@ -127,6 +127,20 @@ __device__ __forceinline__ void put8(uint8_t *sm, uint32_t hi_off, uint32_t lo_o
   for (int i = 0; i < 4; ++i) umma::split_bf16x2(x[2 * i], x[2 * i + 1], h[i], l[i]);
   st_v4(sm, hi_off, h[0], h[1], h[2], h[3]);
   st_v4(sm, lo_off, l[0], l[1], l[2], l[3]);
+}
+
+// Sixteen fp32 values x[0..15] of K-row k, MN positions n0 .. n0 + 15 (n0 a
+// multiple of 16, < 32) -> an MN-major tile holding the hi split at n and the
+// lo split at 32 + n: four 16-byte chunks.
+__device__ __forceinline__ void put16_mn(uint8_t *sm, uint32_t tile, int k, int n0,
+                                         const float *x) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) umma::split_bf16x2(x[2 * i], x[2 * i + 1], h[i], l[i]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, n0), h[0], h[1], h[2], h[3]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, n0 + 8), h[4], h[5], h[6], h[7]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0), l[0], l[1], l[2], l[3]);
+  st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0 + 8), l[4], l[5], l[6], l[7]);
 }
 
 // Four consecutive entries (r, c..c+3) of a swizzled 64 x 64 fp32 array
@@ -548,14 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     {
       const float egm = __expf(sgm[c]);
+      float x[16];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        uint16_t hi, lo;
-        umma::split_bf16(egm * S[jj], hi, lo);
-        const uint32_t off = umma::sw128_off16(16 * hf + jj, c, kNC);
-        st_u16(sm, Lay::SB_HI + off, hi);
-        st_u16(sm, Lay::SB_LO + off, lo);
-      }
+      for (int jj = 0; jj < 16; ++jj) x[jj] = egm * S[jj];
+      put16_mn(sm, Lay::SB_HI, c, 16 * hf, x);  // MN-major, hi and lo stacked
     }
     {  // V^T rows of the R2 B tile: exact bf16, hi part only
       const int j = tid & 31, tg = tid >> 5;
@@ -665,69 +675,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     tiles_ready();
 
     // ---- R3: [W~; Q~] S~ -> W S (rows 0..63), Q S (rows 64..127)
-    if (tid == 0) {
-      const uint32_t id = umma::idesc_bf16(128, kNC);
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? Lay::GA_LO : Lay::GA_HI;
-        const uint32_t b = ps == 2 ? Lay::SB_LO : Lay::SB_HI;
+    if (tid == 0) {  // A_hi [S~_hi | S~_lo], then A_lo [S~_hi | S~_lo] (N = 64)
+      const uint32_t id = umma::idesc_bf16_bmn(128, 2 * kNC);
+      const uint64_t dSB = umma::sdesc_sw128_mn(sb + Lay::SB_HI);
+      for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t a = ps ? Lay::GA_LO : Lay::GA_HI;
         for (int kk = 0; kk < 8; ++kk)
           umma::mma_bf16(tmem + kAcc3, dadd(dGA, a + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         dadd(dGA, b + (kk >> 2) * (kNC * 128) + (kk & 3) * 32), id,
-                         (uint32_t)(ps | kk));
+                         dadd(dSB, kk * 2048), id, (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
     }
     if (!(ok = tc_wait(mbar, phase, tid))) break;
     if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
       const int t = c;
-      float ws[16];
+      float ws[16], ws2[16];
       umma::tmem_ld16(tl + kAcc3 + 16 * hf, ws);
+      umma::tmem_ld16(tl + kAcc3 + kNC + 16 * hf, ws2);
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        uint16_t hi, lo;
-        umma::split_bf16(up[jj] - ws[jj], hi, lo);
-        const uint32_t off = umma::sw128_off16(16 * hf + jj, t, kNC);
-        st_u16(sm, Lay::UT_HI + off, hi);
-        st_u16(sm, Lay::UT_LO + off, lo);
-      }
+      for (int jj = 0; jj < 16; ++jj) ws[jj] = up[jj] - (ws[jj] + ws2[jj]);
+      put16_mn(sm, Lay::UT_HI, t, 16 * hf, ws);  // MN-major, hi and lo stacked
     }
     tiles_ready();
 
     // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
-    if (tid == 0) {
-      const uint32_t id = umma::idesc_bf16(128, kNC);
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? Lay::KH_LO : Lay::KH_HI;
-        const uint32_t b = ps == 2 ? Lay::UT_LO : Lay::UT_HI;
+    if (tid == 0) {  // both A splits against [U_hi | U_lo] (N = 64)
+      const uint32_t id = umma::idesc_bf16_bmn(128, 2 * kNC);
+      const uint64_t dUT = umma::sdesc_sw128_mn(sb + Lay::UT_HI);
+      for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t a = ps ? Lay::KH_LO : Lay::KH_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc4, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id,
+          umma::mma_bf16(tmem + kAcc4, dadd(dGA, a + kk * 32), dadd(dUT, kk * 2048), id,
                          (uint32_t)(ps | kk));
       }
-      for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? Lay::TM_LO : Lay::TM_HI;
-        const uint32_t b = ps == 2 ? Lay::UT_LO : Lay::UT_HI;
+      for (int ps = 0; ps < 2; ++ps) {
+        const uint32_t a = ps ? Lay::TM_LO : Lay::TM_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc3, dadd(dGA, a + kk * 32), dadd(dGA, b + kk * 32), id, 1u);
+          umma::mma_bf16(tmem + kAcc3, dadd(dGA, a + kk * 32), dadd(dUT, kk * 2048), id, 1u);
       }
       umma::commit(mbar);
     }
     if (!(ok = tc_wait(mbar, phase, tid))) break;
     {
-      float acc[16];
+      float acc[16], acc2[16];
       umma::tmem_ld16(tl + kAcc4 + 16 * hf, acc);
+      umma::tmem_ld16(tl + kAcc4 + kNC + 16 * hf, acc2);
       const float a1 = egc[c], a2 = ecm[c];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * acc[jj]);
+      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * (acc[jj] + acc2[jj]));
       if (c >= 64) {  // outputs of row t = c - 64
-        float o[16];
+        float o[16], o2[16];
         umma::tmem_ld16(tl + kAcc3 + 16 * hf, o);
+        umma::tmem_ld16(tl + kAcc3 + kNC + 16 * hf, o2);
         const int t = c - 64;
         if (t < n) {
           float4 *dst = reinterpret_cast<float4 *>(
               p.o + ((size_t)(tok0 + t) * H + h) * kD + col0 + 16 * hf);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+            dst[e] = make_float4(o[4 * e] + o2[4 * e], o[4 * e + 1] + o2[4 * e + 1],
+                                 o[4 * e + 2] + o2[4 * e + 2], o[4 * e + 3] + o2[4 * e + 3]);
         }
       }
     }
@@ -838,20 +845,6 @@ struct LayS {                                  // pass 2
 };
 static_assert(LayS::SB % 1024 == 0 && LayS::UT % 1024 == 0, "pass-2 tiles");
 static_assert(LayS::kBytes <= 232448, "pass-2 shared memory");
-
-// Sixteen fp32 values x[0..15] of K-row k, MN positions n0 .. n0 + 15 (n0 a
-// multiple of 16, < 32) -> an MN-major tile holding the hi split at n and the
-// lo split at 32 + n: four 16-byte chunks.
-__device__ __forceinline__ void put16_mn(uint8_t *sm, uint32_t tile, int k, int n0,
-                                         const float *x) {
-  uint32_t h[8], l[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) umma::split_bf16x2(x[2 * i], x[2 * i + 1], h[i], l[i]);
-  st_v4(sm, tile + umma::sw128_mn_off16(k, n0), h[0], h[1], h[2], h[3]);
-  st_v4(sm, tile + umma::sw128_mn_off16(k, n0 + 8), h[4], h[5], h[6], h[7]);
-  st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0), l[0], l[1], l[2], l[3]);
-  st_v4(sm, tile + umma::sw128_mn_off16(k, kNC + n0 + 8), l[4], l[5], l[6], l[7]);
-}
 
 template <bool RAW>
 __global__ void __launch_bounds__(kThreads, 1)
