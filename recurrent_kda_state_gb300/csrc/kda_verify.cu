@@ -24,6 +24,8 @@
 //   delta_t = beta_t (v_tj - (S^T kt_t)_j - sum_{s<t} A_ts delta_s)
 //   o_tj    = (S^T qt_t)_j + sum_{s<=t} B_ts delta_s
 // which is the recurrence unrolled over the drafted tokens.
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_umma.cuh"
 
@@ -896,28 +898,57 @@ int resident_ctas(const void *kern, int threads, size_t dyn_smem) {
   return n;
 }
 
-template <int D, typename Tin>
-cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
-  const size_t smem = verify_smem_bytes(D, p.depth, p.max_T,
-                                       sizeof(Tin) == 2 ? KDA_BF16 : KDA_F32);
-  auto kern = p.max_T <= 8 ? verify_kernel<D, Tin, 8> : verify_kernel<D, Tin, 16>;
+// Launch set-up of one (device, kernel, shared-memory size): the attributes
+// are set once and the first wave's size (CTAs that fit at once on all SMs)
+// is computed once; later launches reuse it without querying the driver.
+struct VerifySetup {
+  int dev;
+  const void *kern;
+  size_t smem;
+  int first_wave;
+};
+
+cudaError_t verify_setup(const void *kern, int threads, size_t smem, int *first_wave) {
+  static std::mutex mu;
+  static VerifySetup cache[64];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int k = 0; k < used; ++k)
+    if (cache[k].dev == dev && cache[k].kern == kern && cache[k].smem == smem) {
+      *first_wave = cache[k].first_wave;
+      return cudaSuccess;
+    }
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
   }
   // all of the unified L1 as shared memory: two CTAs per SM at d = 128
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                         (int)cudaSharedmemCarveoutMaxShared);
   if (ce != cudaSuccess) return ce;
+  const int per_sm = resident_ctas(kern, threads, smem);
+  int sms = 0;
+  *first_wave = per_sm > 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount,
+                                                     dev) == cudaSuccess
+                    ? per_sm * sms
+                    : 0;
+  if (used < 64) cache[used++] = VerifySetup{dev, kern, smem, *first_wave};
+  return cudaSuccess;
+}
+
+template <int D, typename Tin>
+cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
+  const size_t smem = verify_smem_bytes(D, p.depth, p.max_T,
+                                       sizeof(Tin) == 2 ? KDA_BF16 : KDA_F32);
+  auto kern = p.max_T <= 8 ? verify_kernel<D, Tin, 8> : verify_kernel<D, Tin, 16>;
   // CTAs resident in the first wave: they prefetch the later waves' states.
-  const int per_sm = resident_ctas(reinterpret_cast<const void *>(kern), 2 * D, smem);
-  int dev = 0, sms = 0;
-  if (per_sm > 0 && cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-    p.prefetch_stride = per_sm * sms;
-  else
-    p.prefetch_stride = 0;
+  int first_wave = 0;
+  cudaError_t e = verify_setup(reinterpret_cast<const void *>(kern), 2 * D, smem, &first_wave);
+  if (e != cudaSuccess) return e;
+  p.prefetch_stride = first_wave;
   dim3 grid(p.H, p.B);
   kern<<<grid, 2 * D, smem, s>>>(p);
   return cudaGetLastError();
