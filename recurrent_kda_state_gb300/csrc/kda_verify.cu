@@ -920,11 +920,15 @@ cudaError_t verify_setup(const void *kern, int threads, size_t smem, int *first_
       *first_wave = cache[k].first_wave;
       return cudaSuccess;
     }
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  // the kernel's dynamic shared-memory limit is one attribute for every
+  // launch of it: raise it to the device's opt-in maximum (never lower it to
+  // this launch's size, which would break a cached larger configuration)
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if ((size_t)optin < smem) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e != cudaSuccess) return e;
   // all of the unified L1 as shared memory: two CTAs per SM at d = 128
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                         (int)cudaSharedmemCarveoutMaxShared);

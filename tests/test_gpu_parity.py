@@ -674,3 +674,33 @@ def test_prefill_raw_inputs_fused_prep(single_pass, case):
     for s in range(P):
         assert_states(got[s], sess.pool[s])
     assert K.kda_get_device_error() == 0
+
+
+def test_verify_launch_configurations_interleave():
+    """Launches of the verify kernel with different shared-memory sizes
+    (ring depth 16 with 16-token drafts, depth 8, materialize with no tokens)
+    interleave in any order: the launch set-up is cached per configuration and
+    one configuration must not invalidate another."""
+    rng = np.random.default_rng(95)
+    B, H, d, P = 3, 8, 128, 8
+    slots_np = ki.slot_table(rng, B, P)
+    slots = i32(slots_np)
+    pool8, pool16 = K.StatePool.zeros(P, H, d), K.StatePool.zeros(P, H, d)
+    ring8 = K.ReplayRing(P, H, d, 8, torch.bfloat16)
+    ring16 = K.ReplayRing(P, H, d, 16, torch.bfloat16)
+    sess8, sess16 = oracle.OracleSession(P, H, d, d), oracle.OracleSession(P, H, d, d)
+    for step in range(3):
+        for T, pool, ring, sess in ((16, pool16, ring16, sess16), (8, pool8, ring8, sess8)):
+            tok = _spec_tokens(rng, B, H, d, T, "bf16")
+            tb = device_batch(tok, "bf16")
+            K.kda_verify(tb, T, pool, slots, ring)
+            a = ki.accepted_uniform(rng, B, T)
+            K.kda_commit(i32(a), slots, pool, ring)
+            assert_outputs(tb.o.cpu().numpy(), sess.verify(tok, slots_np))
+            sess.commit(a, slots_np)
+            K.kda_materialize(slots, pool, ring)
+    for pool, sess in ((pool8, sess8), (pool16, sess16)):
+        got = from_gpu_states(pool.data)
+        for s_ in slots_np:
+            assert_states(got[s_], sess.pool[s_])
+    assert K.kda_get_device_error() == 0
