@@ -923,11 +923,15 @@ cudaError_t verify_setup(const void *kern, int threads, size_t smem, int *first_
   // the kernel's dynamic shared-memory limit is one attribute for every
   // launch of it: raise it to the device's opt-in maximum (never lower it to
   // this launch's size, which would break a cached larger configuration)
+  // (the opt-in maximum less the kernel's static shared memory)
   int optin = 0;
+  cudaFuncAttributes fa;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
-  if ((size_t)optin < smem) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  const int dyn_max = optin - (int)fa.sharedSizeBytes;
+  if (dyn_max < 0 || (size_t)dyn_max < smem) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
   if (e != cudaSuccess) return e;
   // all of the unified L1 as shared memory: two CTAs per SM at d = 128
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
