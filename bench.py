@@ -10,7 +10,8 @@ recording the step's accepted lengths in every layer's ring.  NL layers have the
 pools, so the state touched per step is NL x 32 MiB, at least 4x the L2.  The
 value is drafted tokens verified through one KDA layer per second,
 B * T * NL * steps / time.  Each step is one CUDA graph captured from the
-public API calls, with timing events around every verify launch.
+public API calls, with a timing event pair around its NL verify launches
+(the verify launch duration is that block's time / NL).
 
 Extra keys: `roofline` (verify kernel vs HBM), `cpu_baseline` (the fp64
 oracle on the host cores, bounded sample), `e2e` (same metric with every
@@ -24,6 +25,10 @@ two-pass path through the workspace, and the single pass beside it),
 256 shuffled slots, own timed region with its HBM roofline; and the same
 batch with a 2048-token prefill segment in front through kda_forward_mixed,
 one stream and with a side stream),
+`serving` (16 sequences x 8192-token prefill with checkpoints every 1024,
+then T = 8 verify + commit with capped-geometric acceptance until 1024 tokens
+are committed per sequence, on the same NL layers: prefill, verified and
+committed tokens/s and the KDA-layer time),
 `ablation_direct_snapshots` (the design ReplaySSM replaces -- the state
 stored at every drafted position, the accepted one copied at commit -- on the
 same workload, its own timed region; with both designs' algorithmic bytes
@@ -406,7 +411,8 @@ def run_mixed(torch, K, dev, steps=32, warmup=4, NL=4, prefill_len=2048):
     speculative (T = 8, accepted ~ U{0..8}) at seeded random positions among
     56 ordinary one-token rows, one packed batch per step (kda_verify over all
     64, then the commit); NL layer pools rotate so the state touched per step
-    (NL x 128 MiB) exceeds the L2.  Then the same batch with a 2048-token
+    (NL x 128 MiB) exceeds the L2; one CUDA graph per step, an event pair
+    around its NL verify launches.  Then the same batch with a 2048-token
     prefill segment in front (checkpoint every 1024), one layer, through
     kda_forward_mixed on one stream and with the prefill on a side stream."""
     w = ki.MIXED
@@ -435,35 +441,49 @@ def run_mixed(torch, K, dev, steps=32, warmup=4, NL=4, prefill_len=2048):
     acc_np = np.where(is_spec_np[None, :] == 1,
                       ki.accepted_uniform(rng, A * Bm, Tm).reshape(A, Bm), 0).astype(np.int32)
     acc = torch.as_tensor(acc_np, device=dev)
-    stream = torch.cuda.current_stream()
-    evs = []
-    for s in range(warmup + steps):
-        rec = s >= warmup
-        for l in range(NL):
-            e0 = e1 = None
-            if rec:
-                e0, e1 = (torch.cuda.Event(enable_timing=True),
-                          torch.cuda.Event(enable_timing=True))
-                e0.record(stream)
-            K.kda_verify(sets[s % G][l], Tm, pools[l], slots, rings[l], is_spec=is_spec)
-            if rec:
-                e1.record(stream)
-                evs.append((e0, e1, s))
-        K.kda_commit_layers(acc[s % A], slots, pools[0], rings)
-        if s == warmup - 1:
-            torch.cuda.synchronize()
-            t0 = torch.cuda.Event(enable_timing=True)
-            t0.record(stream)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t1.record(stream)
+    # one CUDA graph per step (NL verify launches between one event pair,
+    # then the commit), as in the main line
+    gstream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(gstream):
+        for s in range(warmup + steps):
+            g = torch.cuda.CUDAGraph()
+            ev = (torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True)) \
+                if s >= warmup else None
+            g.capture_begin()
+            if ev:
+                ev[0].record(gstream)
+            for l in range(NL):
+                K.kda_verify(sets[s % G][l], Tm, pools[l], slots, rings[l],
+                             is_spec=is_spec, stream=gstream)
+            if ev:
+                ev[1].record(gstream)
+            K.kda_commit_layers(acc[s % A], slots, pools[0], rings, stream=gstream)
+            g.capture_end()
+            graphs.append((g, ev))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(gstream):
+        for g, _ in graphs[:warmup]:
+            g.replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(gstream)
+        for g, _ in graphs[warmup:]:
+            g.replay()
+        t1.record(gstream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    durs = [a.elapsed_time(b) for a, b, _ in evs]
-    byts = []
-    for _, _, s in evs:
+    durs, byts = [], []
+    for s in range(warmup, warmup + steps):
+        ev = graphs[s][1]
+        durs.append(ev[0].elapsed_time(ev[1]) / NL)
         prev = acc_np[(s - 1) % A]
         byts.append(float(sum(unit_bytes(int(prev[i])) if is_spec_np[i] else decode_unit_bytes()
                               for i in range(Bm)) * H))
+    del graphs
+    stream = torch.cuda.current_stream()
     mean_us = float(np.mean(durs)) * 1e3
     achieved = float(np.mean(byts)) / (mean_us * 1e-6) / 1e9
     peak, _ = load_peaks()
@@ -547,7 +567,8 @@ def run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np, G, A,
     """The direct per-position snapshot design on the same workload: per step
     kda_verify_snapshot on each of NL layers, then kda_commit_snapshot of the
     step's accepted lengths on each layer.  Own pools (zero), own timed
-    region, CUDA events around every launch."""
+    region, one CUDA event pair around each step's NL verify launches and
+    one around its NL commits (launch durations = block time / NL)."""
     pools = [K.StatePool.zeros(P, H, D, device=dev) for _ in range(NL)]
     snaps = [K.snapshot_buffer(B, T, pools[l]) for l in range(NL)]
     stream = torch.cuda.Stream(device=dev)
@@ -555,23 +576,23 @@ def run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np, G, A,
     with torch.cuda.stream(stream):
         for s in range(warmup + steps):
             g = torch.cuda.CUDAGraph()
-            ev = [[torch.cuda.Event(enable_timing=True, external=True)
-                   for _ in range(4)] for _ in range(NL)] if s >= warmup else None
+            # event pairs around the NL verify launches and the NL commits
+            ev = [torch.cuda.Event(enable_timing=True, external=True)
+                  for _ in range(4)] if s >= warmup else None
             g.capture_begin()
+            if ev:
+                ev[0].record(stream)
             for l in range(NL):
-                if ev:
-                    ev[l][0].record(stream)
                 K.kda_verify_snapshot(batches[s % G][l], T, pools[l], slots,
                                       snaps[l], stream=stream)
-                if ev:
-                    ev[l][1].record(stream)
+            if ev:
+                ev[1].record(stream)
+                ev[2].record(stream)
             for l in range(NL):
-                if ev:
-                    ev[l][2].record(stream)
                 K.kda_commit_snapshot(acc[s % A], slots, pools[l], snaps[l],
                                       stream=stream)
-                if ev:
-                    ev[l][3].record(stream)
+            if ev:
+                ev[3].record(stream)
             g.capture_end()
             graphs.append(g)
             events.append(ev)
@@ -593,14 +614,11 @@ def run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np, G, A,
     v_us, c_us, v_bytes, c_bytes = [], [], [], []
     for s in range(warmup, warmup + steps):
         per = [snapshot_unit_bytes(int(x)) for x in acc_np[s % A]]
-        vb = float(sum(p[0] for p in per) * H)
-        cb = float(sum(p[1] for p in per) * H)
-        for l in range(NL):
-            ev = events[s][l]
-            v_us.append(ev[0].elapsed_time(ev[1]) * 1e3)
-            c_us.append(ev[2].elapsed_time(ev[3]) * 1e3)
-            v_bytes.append(vb)
-            c_bytes.append(cb)
+        v_bytes.append(float(sum(p[0] for p in per) * H))
+        c_bytes.append(float(sum(p[1] for p in per) * H))
+        ev = events[s]
+        v_us.append(ev[0].elapsed_time(ev[1]) * 1e3 / NL)
+        c_us.append(ev[2].elapsed_time(ev[3]) * 1e3 / NL)
     del graphs, snaps, pools
     torch.cuda.empty_cache()
     v_mean, c_mean = float(np.mean(v_us)), float(np.mean(c_us))
@@ -616,6 +634,144 @@ def run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np, G, A,
         "note": "direct design: T state snapshots written per (sequence, head) "
                 "per step, the accepted one copied into the pool; same inputs, "
                 "slots and accepted lengths as the main line",
+    }
+
+
+def serving_schedule(rng, n, decode_tokens, rho, t=T):
+    """Decode steps of the serving-shaped load: each step every live sequence
+    verifies t drafts and commits a capped-geometric accepted count, the last
+    one clipped so that a sequence stops at exactly ``decode_tokens``
+    committed.  Returns [(live sequence indices, accepted counts)]."""
+    committed = np.zeros(n, dtype=np.int64)
+    steps = []
+    while committed.min() < decode_tokens:
+        live = np.nonzero(committed < decode_tokens)[0].astype(np.int32)
+        a = ki.accepted_capped_geometric(rng, len(live), rho, t)
+        a = np.minimum(a, decode_tokens - committed[live]).astype(np.int32)
+        committed[live] += a
+        steps.append((live, a))
+    return steps
+
+
+def serving_verify_bytes(steps, h=H):
+    """Algorithmic bytes of the decode phase's verify launches (one layer):
+    per live (sequence, head) unit the spec-verify bytes, with the replay of
+    that sequence's previous accepted count."""
+    prev = {}
+    total = 0
+    for live, a in steps:
+        total += sum(unit_bytes(prev.get(int(i), 0)) for i in live) * h
+        prev.update({int(i): int(x) for i, x in zip(live, a)})
+    return total
+
+
+def run_serving(torch, K, dev, NL, G=4):
+    """Serving-shaped load on NL KDA layers (own pools and rings per layer):
+    16 sequences prefilled in passes of at most 16384 tokens (chunk 64, a
+    checkpoint every 1024 tokens into its own slot), their rings reset, then
+    T = 8 verify + ReplaySSM commit steps with capped-geometric accepted
+    counts until every sequence has 1024 tokens committed, and a final
+    materialize.  The decode steps are CUDA graphs captured from the public
+    calls (their live slot tables and accepted counts on the device before
+    timing); one warm run, then one timed run, events at the phase
+    boundaries."""
+    w = ki.SERVING
+    x = w.extra
+    Bs, L, C, E = w.num_seqs, x["prefill_len"], x["chunk"], x["ckpt_every"]
+    rng = np.random.default_rng(w.seed)
+    per_pass = max(1, 16384 // L)
+    n_ck = L // E
+    Ps = Bs * (1 + n_ck)
+    perm = rng.permutation(Ps).astype(np.int32)
+    seq_slot = perm[:Bs]
+    ck_np = perm[Bs:].reshape(Bs, n_ck)
+    pools = [K.StatePool.zeros(Ps, H, D, device=dev) for _ in range(NL)]
+    rings = [K.ReplayRing(Ps, H, D, x["depth"], torch.bfloat16, device=dev)
+             for _ in range(NL)]
+    tok = ki.gen_tokens(rng, [L] * per_pass, H, D)
+    pt = {n: torch.from_numpy(tok[n]).to(device=dev, dtype=torch.bfloat16)
+          for n in ("q", "k", "v", "alpha", "beta")}
+    del tok
+    cu_p = torch.arange(0, (per_pass + 1) * L, L, dtype=torch.int32, device=dev)
+    ptb = K.TokenBatch(pt["q"], pt["k"], pt["v"], pt["alpha"], pt["beta"], cu_p)
+    ws_bytes = K.kda_prefill_workspace_size(per_pass * L, per_pass, H, D, D, C,
+                                            K.KDA_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    passes = [(torch.as_tensor(seq_slot[i:i + per_pass], device=dev),
+               torch.as_tensor(ck_np[i:i + per_pass].copy(), device=dev))
+              for i in range(0, Bs, per_pass)]
+    all_slots = torch.as_tensor(seq_slot, device=dev)
+
+    steps = serving_schedule(rng, Bs, x["decode_tokens"], x["rho"], x["T"])
+    sets = [build_inputs(torch, rng, NL, dev) for _ in range(G)]
+    cu_d = torch.arange(0, (Bs + 1) * T, T, dtype=torch.int32, device=dev)
+    outs = torch.empty(G, NL, Bs * T, H, D, dtype=torch.float32, device=dev)
+    live_slots = [torch.as_tensor(seq_slot[live], device=dev) for live, _ in steps]
+    accs = [torch.as_tensor(a, device=dev) for _, a in steps]
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for s, (live, _) in enumerate(steps):
+            n = len(live)
+            g = torch.cuda.CUDAGraph()
+            g.capture_begin()
+            for l in range(NL):
+                v = sets[s % G][1][l]
+                tb = K.TokenBatch(v["q"][:n * T], v["k"][:n * T], v["v"][:n * T],
+                                  v["alpha"][:n * T], v["beta"][:n * T],
+                                  cu_d[:n + 1], o=outs[s % G, l, :n * T])
+                K.kda_verify(tb, T, pools[l], live_slots[s], rings[l],
+                             stream=stream)
+            K.kda_commit_layers(accs[s], live_slots[s], pools[0], rings,
+                                stream=stream)
+            g.capture_end()
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    def flow():
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for l in range(NL):
+                for slots_p, ck_p in passes:
+                    K.kda_prefill_chunked(ptb, pools[l], slots_p, C, E, ck_p,
+                                          workspace=ws, stream=stream)
+                K.kda_ring_reset(all_slots, pools[l], rings[l], stream=stream)
+            ev[1].record(stream)
+            for g in graphs:
+                g.replay()
+            for l in range(NL):
+                K.kda_materialize(all_slots, pools[l], rings[l], stream=stream)
+            ev[2].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+
+    K.kda_get_device_error()
+    flow()
+    prefill_ms, decode_ms = flow()
+    bits = K.kda_get_device_error()
+    del graphs, ws, pools, rings, sets, outs, pt, ptb
+    torch.cuda.empty_cache()
+    verified = sum(len(live) for live, _ in steps) * T
+    committed = sum(int(a.sum()) for _, a in steps)
+    vbytes = serving_verify_bytes(steps) * NL
+    return {
+        "workload": w.name, "kda_layers": NL,
+        "prefill_passes_per_layer": len(passes),
+        "prefill_tokens_per_s": Bs * L * NL / (prefill_ms * 1e-3),
+        "prefill_ms_per_layer": prefill_ms / NL,
+        "decode_steps": len(steps),
+        "verified_tokens_per_s": verified * NL / (decode_ms * 1e-3),
+        "committed_tokens_per_s": committed * NL / (decode_ms * 1e-3),
+        "mean_accepted": committed / sum(len(live) for live, _ in steps),
+        "decode_ms_per_layer": decode_ms / NL,
+        "kda_layer_ms": (prefill_ms + decode_ms) / NL,
+        "decode_verify_alg_gbs": vbytes / (decode_ms * 1e-3) / 1e9,
+        "device_error_bits": bits,
+        "note": "per-layer figures = totals over the NL layers / NL; the "
+                "decode phase's GB/s counts the verify launches' algorithmic "
+                "bytes over the whole phase (commit and materialize launches "
+                "included in the time)",
     }
 
 
@@ -655,17 +811,19 @@ def run_kda(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for s in range(total_steps):
             g = torch.cuda.CUDAGraph()
-            evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                    torch.cuda.Event(enable_timing=True, external=True))
-                   for _ in range(NL)] if s >= args.warmup else None
+            # one event pair around the step's NL verify launches: a pair
+            # around every launch delays each launch by several microseconds
+            evs = (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True)) \
+                if s >= args.warmup else None
             g.capture_begin()
+            if evs:
+                evs[0].record(stream)
             for l in range(NL):
-                if evs:
-                    evs[l][0].record(stream)
                 K.kda_verify(batches[s % G][l], T, pools[l], slots, rings[l],
                              stream=stream)
-                if evs:
-                    evs[l][1].record(stream)
+            if evs:
+                evs[1].record(stream)
             # the sampler's accepted lengths, recorded in every layer's ring
             K.kda_commit_layers(acc[s % A], slots, pools[0], rings, stream=stream)
             g.capture_end()
@@ -704,15 +862,14 @@ def run_kda(args, rank, world, local_rank):
     clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     bits = K.kda_get_device_error()
-    # per-launch verify durations over the timed region
+    # average verify launch duration over the timed region: each step's block
+    # of NL back-to-back launches / NL (the gaps between launches included)
     durs, abytes = [], []
     for s in range(args.warmup, total_steps):
         a_prev = acc_np[(s - 1) % A]
-        b = float(sum(unit_bytes(int(x)) for x in a_prev) * H)
-        for l in range(NL):
-            ev0, ev1 = events[s][l]
-            durs.append(ev0.elapsed_time(ev1))
-            abytes.append(b)
+        abytes.append(float(sum(unit_bytes(int(x)) for x in a_prev) * H))
+        ev0, ev1 = events[s]
+        durs.append(ev0.elapsed_time(ev1) / NL)
     mean_dur_s = float(np.mean(durs)) * 1e-3
     achieved = float(np.mean(abytes)) / mean_dur_s / 1e9
     peak, peak_kind = load_peaks()
@@ -769,14 +926,14 @@ def run_kda(args, rank, world, local_rank):
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), dist, dev)
     # the graphs' timing events were recorded again by this pass: the verify
     # launches' duration while the copies ran beside them
-    e2e_launch_us = float(np.mean([events[s][l][0].elapsed_time(events[s][l][1])
-                                   for s in range(args.warmup, total_steps)
-                                   for l in range(NL)])) * 1e3
+    e2e_launch_us = float(np.mean([events[s][0].elapsed_time(events[s][1]) / NL
+                                   for s in range(args.warmup, total_steps)])) * 1e3
 
     prefill = run_prefill(torch, K, dev)
     mixed = run_mixed(torch, K, dev)
     direct = run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np,
                                    G, A)
+    serving = run_serving(torch, K, dev, NL)
     cache = state_cache_bytes()
     budget = CACHE_BUDGET_GIB * 2 ** 30
     replay_step_bytes = float(np.mean(abytes)) + B * H * 8
@@ -817,6 +974,8 @@ def run_kda(args, rank, world, local_rank):
                      "traffic": ncu_traffic(), "kernel": "verify_kernel<128, bf16>",
                      "peak_source": peak_kind,
                      "mean_launch_us": mean_dur_s * 1e6,
+                     "launch_timing": "one CUDA event pair around each step's "
+                                      "%d back-to-back verify launches, / %d" % (NL, NL),
                      "alg_bytes_per_launch": float(np.mean(abytes))},
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
@@ -828,6 +987,7 @@ def run_kda(args, rank, world, local_rank):
         "device_error_bits": bits,
         "prefill": prefill,
         "mixed": mixed,
+        "serving": serving,
         "ablation_direct_snapshots": direct,
     }
     print(json.dumps(line), flush=True)

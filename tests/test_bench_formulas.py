@@ -28,3 +28,28 @@ def test_state_cache_bytes_per_sequence_layer():
     assert c["direct_snapshots"] == 9 * 32 * 65536                  # 18 874 368
     assert int(46.48 * 2 ** 30 // c["replay_ssm"]) == 21750
     assert int(46.48 * 2 ** 30 // c["direct_snapshots"]) == 2644
+
+
+def test_serving_schedule_commits_exactly_the_decode_budget():
+    import numpy as np
+    steps = bench.serving_schedule(np.random.default_rng(0), 5, 40, 0.8802, 8)
+    total = np.zeros(5, dtype=np.int64)
+    left = set(range(5))
+    for live, a in steps:
+        assert set(live.tolist()) == left          # every unfinished one, no other
+        assert ((a >= 0) & (a <= 8)).all()
+        total[live] += a
+        left = {int(i) for i in np.nonzero(total < 40)[0]}
+    assert (total == 40).all() and not left
+
+
+def test_serving_verify_bytes_by_hand():
+    import numpy as np
+    # step 1: both sequences replay nothing; step 2: sequence 0 replays 3,
+    # sequence 1 nothing; step 3: sequence 1 alone replays 2
+    steps = [(np.array([0, 1]), np.array([3, 0])),
+             (np.array([0, 1]), np.array([8, 2])),
+             (np.array([1]), np.array([5]))]
+    u0, u3, u2 = 84008, 84008 + 65536 + 3 * 770, 84008 + 65536 + 2 * 770
+    assert bench.serving_verify_bytes(steps) == (2 * u0 + u3 + u0 + u2) * 32
+    assert bench.serving_verify_bytes(steps) == 17758784
