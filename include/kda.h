@@ -240,6 +240,10 @@ int kda_prefill_chunked_noalloc(const kda_tokens *tok, kda_state_pool *pool,
  *      ctrl becomes {0, 0}.
  * A verify that follows another verify with no kda_commit between them
  * treats the earlier drafts as all rejected.
+ * The kernel is launched as a programmatic dependent of the previous work on
+ * the stream: it may start while that work finishes, but it only prefetches
+ * into L2 until that work has completed, so stream order holds for every
+ * value it reads.  kda_materialize launches the same way.
  */
 int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
                const int32_t *state_slots, kda_replay_ring *ring,

@@ -472,6 +472,38 @@ __global__ void __launch_bounds__(2 * D, 2)
   const int rg = tid & 3;
   const int j0 = 2 * (tid >> 2);
 
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream, this CTA may start while that kernel's last CTAs still run.
+  // Until griddepcontrol.wait returns it only issues L2 prefetch hints for
+  // this unit's state and ring entries, at the slot the table holds when
+  // read: a relaxed read that the previous kernel may still be writing, so
+  // a stale value costs only a useless hint, and L2 is the point where the
+  // previous kernel's writes become visible, so no stale data is ever used.
+  if (tid == 0) {
+    int s0;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];"
+                 : "=r"(s0) : "l"(p.state_slots + i) : "memory");
+    if (s0 >= 0 && s0 < p.P) {
+      const size_t u0 = (size_t)s0 * H + h;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                   :: "l"(p.pool + u0 * D * D), "r"(D * D * 4) : "memory");
+      const uint32_t rbytes = (uint32_t)(p.depth * D * sizeof(Tin));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                   :: "l"(reinterpret_cast<const Tin *>(p.rk) + u0 * p.depth * D),
+                      "r"(rbytes) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                   :: "l"(reinterpret_cast<const Tin *>(p.ra) + u0 * p.depth * D),
+                      "r"(rbytes) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                   :: "l"(reinterpret_cast<const Tin *>(p.rv) + u0 * p.depth * D),
+                      "r"(rbytes) : "memory");
+    }
+  }
+  // the previous kernel has completed and its writes are visible; the next
+  // kernel may be scheduled once every CTA of this one has passed here
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // Round trip 1 (all threads, same addresses): slot, segment, row kind.
   const int slot = p.state_slots[i];
   int tok0 = 0, T = 0, spec = 0, bad = 0;
@@ -957,9 +989,19 @@ cudaError_t launch_verify_t(VerifyParams p, cudaStream_t s) {
   cudaError_t e = verify_setup(reinterpret_cast<const void *>(kern), 2 * D, smem, &first_wave);
   if (e != cudaSuccess) return e;
   p.prefetch_stride = first_wave;
-  dim3 grid(p.H, p.B);
-  kern<<<grid, 2 * D, smem, s>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel on the stream: the
+  // kernel prefetches into L2 before it waits for that kernel to complete
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.H, p.B);
+  cfg.blockDim = dim3(2 * D);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
