@@ -29,6 +29,8 @@ one stream and with a side stream),
 then T = 8 verify + commit with capped-geometric acceptance until 1024 tokens
 are committed per sequence, on the same NL layers: prefill, verified and
 committed tokens/s and the KDA-layer time),
+`tiny` (latency of the tiny correctness workload: 1 sequence, 2 heads,
+d = 16, fp32, a 64-token prefill then 8 verify + commit steps with T = 4),
 `ablation_direct_snapshots` (the design ReplaySSM replaces -- the state
 stored at every drafted position, the accepted one copied at commit -- on the
 same workload, its own timed region; with both designs' algorithmic bytes
@@ -775,6 +777,80 @@ def run_serving(torch, K, dev, NL, G=4):
     }
 
 
+def run_tiny(torch, K, dev, reps=50, warmup=5):
+    """Latency of the tiny workload (a correctness workload: no roofline).
+    One sequence, 2 heads, d = 16, fp32 inputs, state from zero: a 64-token
+    prefill (chunk 16, checkpoints after tokens 32 and 64), the ring reset,
+    then 8 steps of verify T = 4 + commit with accepted ~ U{0..4}.  Eager
+    calls on one stream; CUDA events at the phase boundaries and the host
+    wall time of a whole flow (synchronized at its end), over ``reps`` flows
+    after ``warmup``."""
+    w = ki.TINY
+    x = w.extra
+    rng = np.random.default_rng(w.seed)
+    Hn, d, L, Tn, n = w.num_heads, w.d, x["prefill_len"], x["T"], x["steps"]
+    C, E = x["chunk"], x["ckpt_every"]
+
+    def batch(tok):
+        t = {k: torch.from_numpy(tok[k]).to(device=dev, dtype=torch.float32)
+             for k in ("q", "k", "v", "alpha", "beta")}
+        cu = torch.as_tensor(np.asarray(tok["cu_seqlens"], dtype=np.int32),
+                             device=dev)
+        return K.TokenBatch(t["q"], t["k"], t["v"], t["alpha"], t["beta"], cu)
+
+    prompt = batch(ki.gen_tokens(rng, [L], Hn, d))
+    drafts = [batch(ki.gen_tokens(rng, [Tn], Hn, d)) for _ in range(n)]
+    acc = [torch.as_tensor(ki.accepted_uniform(rng, 1, Tn), device=dev)
+           for _ in range(n)]
+    n_ck = L // E
+    pool = K.StatePool.zeros(1 + n_ck, Hn, d, device=dev)
+    ring = K.ReplayRing(1 + n_ck, Hn, d, Tn, torch.float32, device=dev)
+    slots = torch.zeros(1, dtype=torch.int32, device=dev)
+    ck = torch.arange(1, 1 + n_ck, dtype=torch.int32, device=dev).view(1, -1)
+    ws_bytes = K.kda_prefill_workspace_size(L, 1, Hn, d, d, C, K.KDA_F32)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    stream = torch.cuda.current_stream()
+
+    def flow(ev=None):
+        if ev:
+            ev[0].record(stream)
+        K.kda_prefill_chunked(prompt, pool, slots, C, E, ck, workspace=ws)
+        K.kda_ring_reset(slots, pool, ring)
+        if ev:
+            ev[1].record(stream)
+        for s in range(n):
+            K.kda_verify(drafts[s], Tn, pool, slots, ring)
+            K.kda_commit(acc[s], slots, pool, ring)
+        if ev:
+            ev[2].record(stream)
+
+    K.kda_get_device_error()
+    pre, dec, wall = [], [], []
+    for r in range(warmup + reps):
+        pool.data.zero_()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t0 = time.perf_counter()
+        flow(ev)
+        torch.cuda.synchronize()
+        if r >= warmup:
+            wall.append(time.perf_counter() - t0)
+            pre.append(ev[0].elapsed_time(ev[1]))
+            dec.append(ev[1].elapsed_time(ev[2]))
+    bits = K.kda_get_device_error()
+    return {
+        "workload": w.name, "reps": reps,
+        "prefill_us": float(np.median(pre)) * 1e3,
+        "verify_commit_us_per_step": float(np.median(dec)) * 1e3 / n,
+        "flow_wall_us": float(np.median(wall)) * 1e6,
+        "device_error_bits": bits,
+        "note": "medians; device times from CUDA events around the eager "
+                "calls (prefill + ring reset; the 8 verify + commit steps), "
+                "wall time of the whole flow on the host including the "
+                "binding's call overhead; launch-bound at this size",
+    }
+
+
 def run_kda(args, rank, world, local_rank):
     import torch
     from recurrent_kda_state_gb300 import kda as K
@@ -934,6 +1010,7 @@ def run_kda(args, rank, world, local_rank):
     direct = run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np,
                                    G, A)
     serving = run_serving(torch, K, dev, NL)
+    tiny = run_tiny(torch, K, dev)
     cache = state_cache_bytes()
     budget = CACHE_BUDGET_GIB * 2 ** 30
     replay_step_bytes = float(np.mean(abytes)) + B * H * 8
@@ -988,6 +1065,7 @@ def run_kda(args, rank, world, local_rank):
         "prefill": prefill,
         "mixed": mixed,
         "serving": serving,
+        "tiny": tiny,
         "ablation_direct_snapshots": direct,
     }
     print(json.dumps(line), flush=True)
