@@ -97,19 +97,21 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash(unit):
+def source_hash(unit, extra=()):
     """First 16 hex digits of the SHA-256 of a kernel's translation unit and
-    the two headers it includes: a committed profile is used only when it was
+    the headers it includes: a committed profile is used only when it was
     taken on the same source."""
     h = hashlib.sha256()
-    for name in (unit, "kda_umma.cuh", "kda_internal.cuh"):
+    for name in (unit,) + tuple(extra) + ("kda_umma.cuh", "kda_internal.cuh"):
         with open(os.path.join(ROOT, "recurrent_kda_state_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def verify_source_hash():
-    return source_hash("kda_verify.cu")
+    """The pipelined verify kernel (the spec-decode and mixed workloads' shape)
+    and the single-token step it shares with the per-unit kernel."""
+    return source_hash("kda_verify_pipe.cu", ("kda_step.cuh",))
 
 
 def ncu_traffic():
@@ -529,7 +531,7 @@ def run_mixed(torch, K, dev, steps=32, warmup=4, NL=4, prefill_len=2048):
         "tokens_per_step": N, "value": N * steps * NL / (ms * 1e-3), "unit": "tokens/s",
         "ms_per_step": ms / steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "kernel": "verify_kernel<128, bf16> (64 rows)",
+                     "frac": achieved / peak, "kernel": "verify_pipe_kernel (d=128, bf16; 64 rows)",
                      "mean_launch_us": mean_us, "alg_bytes_per_launch": float(np.mean(byts))},
         "with_prefill_segment": {
             "prefill_tokens": prefill_len, "decode_tokens": N,
@@ -1048,7 +1050,7 @@ def run_kda(args, rank, world, local_rank):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic(), "kernel": "verify_kernel<128, bf16>",
+                     "traffic": ncu_traffic(), "kernel": "verify_pipe_kernel (d=128, bf16)",
                      "peak_source": peak_kind,
                      "mean_launch_us": mean_dur_s * 1e6,
                      "launch_timing": "one CUDA event pair around each step's "

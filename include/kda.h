@@ -85,8 +85,18 @@ enum {
   KDA_DERR_RANGE = 32,   /* prefill: cumulative log-decay across half a
                             chunk below -80 in some channel (fp32 factor
                             range); outputs of that chunk are unreliable   */
-  KDA_DERR_TIMEOUT = 64  /* a bounded wait on the tensor cores gave up; the
-                            affected outputs were not written             */
+  KDA_DERR_TIMEOUT = 64, /* a bounded wait (tensor cores, copy engine, a
+                            pipeline stage) gave up; the kernel stopped
+                            taking work: what it had not finished (outputs,
+                            states, rings of those units) is left as it was
+                            or unspecified, never half-written silently   */
+  KDA_DERR_UNSAFE = 128  /* after a timeout, the second bounded wait for
+                            work still in flight (tensor cores or copies)
+                            also gave up before the kernel released its
+                            tensor memory or shared memory; once
+                            kda_get_device_error has seen this bit, every
+                            later launching call on that device returns
+                            KDA_EDEVICE for the rest of the process      */
 };
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -210,6 +220,9 @@ size_t kda_prefill_workspace_size(int32_t num_tokens, int32_t num_seqs,
  *     runs the single pass without touching the array.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset it is stale (as is the device error word's), so do
+ *     not call into the library again on a device that was reset.
  *   - Every call shares the one array and it keeps the last call's contents
  *     (no part of it needs to start at zero: each call writes what it reads).
  *     Calls whose work overlaps on the GPU (different streams, or different
@@ -280,7 +293,8 @@ int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefil
 
 /*
  * kda_commit -- record how many drafted tokens each sequence accepted.
- * ("Rejecting a draft only moves the buffer pointer.")
+ * ("ReplaySSM shrinks rollback state", vLLM Kimi K3 optimisation page: a
+ * rejection records a count and writes no state.)
  *
  * accepted_len[i] (device, 0 <= a <= pending) is recorded in ctrl of every
  * head of slot state_slots[i]; the replay itself is folded into the next
@@ -307,25 +321,32 @@ int kda_commit_layers(const int32_t *accepted_len, const int32_t *state_slots,
  * kda_materialize -- apply every recorded commit now: replay the accepted
  * ring entries of each listed slot onto its state, write the state, and
  * clear ctrl to {0, 0}.  Call before reading a state any other way (gather,
- * copy, prefill from it) after a commit.
+ * copy, prefill from it) after a commit.  ("ReplaySSM shrinks rollback
+ * state": the accepted state is rebuilt from the kept inputs; this is that
+ * rebuild on demand, for a state about to be read outside a verify.)
  */
 int kda_materialize(const int32_t *state_slots, int32_t num_seqs,
                     kda_state_pool *pool, kda_replay_ring *ring,
                     kda_stream_t stream);
 
 /* kda_ring_reset -- set ctrl of every head of the listed slots to {0, 0}
- * (a fresh slot, or drafts to discard). */
+ * (a fresh slot, or drafts to discard: "ReplaySSM shrinks rollback state",
+ * where discarding drafts is a pointer move, not a state write). */
 int kda_ring_reset(const int32_t *slots, int32_t n, const kda_state_pool *pool,
                    kda_replay_ring *ring, kda_stream_t stream);
 
 /* kda_gather_states -- out[i] = pool[slots[i]] for i < n; out is fp32
- * [n][H][d_v][d_k] on the device.  Reads committed-and-materialized state. */
+ * [n][H][d_v][d_k] on the device.  Reads committed-and-materialized state.
+ * (Paged per-sequence state addressed through a slot table: the hybrid
+ * cache of the daily.dev Kimi K3 summary, and "KDA checkpoints stay inside
+ * the prefill", whose checkpoints are read back by slot.) */
 int kda_gather_states(const kda_state_pool *pool, const int32_t *slots,
                       int32_t n, float *out, kda_stream_t stream);
 
 /* kda_copy_slots -- pool[dst[i]] = pool[src[i]] for i < n (prefix-cache
- * fork of a checkpoint into a live slot).  The src and dst sets must be
- * disjoint. */
+ * fork of a checkpoint into a live slot: "KDA checkpoints stay inside the
+ * prefill", where a partial prefix hit resumes from a block-boundary
+ * checkpoint).  The src and dst sets must be disjoint. */
 int kda_copy_slots(kda_state_pool *pool, const int32_t *src,
                    const int32_t *dst, int32_t n, kda_stream_t stream);
 
@@ -366,6 +387,17 @@ int kda_commit_snapshot(const int32_t *accepted_len, const int32_t *state_slots,
  * of the current device into *host_bits (host pointer), clear it, and return
  * KDA_EDEVICE if any bit was set, else KDA_OK. */
 int kda_get_device_error(int32_t *host_bits, kda_stream_t stream);
+
+/* kda_set_wait_limit -- testing hook for the failure path: every bounded
+ * device wait of later launches (tensor-core completions, pipeline stages,
+ * copy arrivals) gives up after `polls` polls instead of the default
+ * (about 4 M polls), and reports KDA_DERR_TIMEOUT; a negative value restores
+ * the default.  With polls = 0 a kernel's first wait gives up at once: the
+ * pipelined verify then writes nothing (no output, state, ring or ctrl
+ * word) and still lets its own copies land before it exits.  The second,
+ * drain-before-exit waits keep their own fixed limit.  Library-wide, not
+ * per stream; meant for tests, not for serving. */
+int kda_set_wait_limit(int32_t polls);
 
 /* Human-readable name of a status code (static string). */
 const char *kda_status_string(int status);

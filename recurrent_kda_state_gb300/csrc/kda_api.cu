@@ -1,6 +1,7 @@
 // Public C ABI of libkda.so: argument validation on the host, then launches on
 // the caller's stream.  Nothing is allocated here; every buffer belongs to the
 // caller.  The only library-owned device object is one error word per device.
+#include <atomic>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -23,6 +24,19 @@ unsigned int *device_error_word() {
     cache[dev] = static_cast<unsigned int *>(p);
   }
   return cache[dev];
+}
+
+// Polls of a bounded device wait (kda_set_wait_limit; negative = default).
+std::atomic<int> g_wait_limit{-1};
+
+// Devices on which a kernel reported KDA_DERR_UNSAFE (seen by
+// kda_get_device_error): the library refuses further launches there.
+std::atomic<unsigned long long> g_unsafe_devices{0};
+
+bool device_unsafe() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  return (g_unsafe_devices.load() >> dev) & 1ull;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -90,14 +104,27 @@ kda::VerifyParams verify_params(const kda_state_pool *pool,
   p.H = pool->num_heads;
   p.P = pool->num_slots;
   p.depth = ring->depth;
+  p.spin_limit = kda::wait_limit_polls();
   return p;
 }
 
 }  // namespace
 
+namespace kda {
+int wait_limit_polls() {
+  const int v = g_wait_limit.load();
+  return v < 0 ? kDefaultWaitPolls : v;
+}
+}  // namespace kda
+
 extern "C" {
 
 int kda_version(void) { return 1; }
+
+int kda_set_wait_limit(int32_t polls) {
+  g_wait_limit.store(polls < 0 ? -1 : polls);
+  return KDA_OK;
+}
 
 const char *kda_status_string(int status) {
   switch (status) {
@@ -134,7 +161,7 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
                  const int32_t *ckpt_slots, int32_t max_ckpt, int32_t ckpt_every,
                  int32_t chunk, const int32_t *start_pos, void *workspace,
                  size_t workspace_bytes, kda_stream_t stream, bool cu_aligned,
-                 bool raw = false) {
+                 bool raw = false, bool check_only = false) {
   int st = check_pool(pool);
   if (st) return st;
   if ((st = check_tokens(tok, pool, cu_aligned))) return st;
@@ -146,6 +173,7 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
   if (!state_slots) return KDA_EINVAL;
   const bool tc = kda::prefill_uses_tc(tok->dtype, tok->num_heads, tok->d_k, tok->d_v, chunk);
   if (raw && !tc) return KDA_ESHAPE;  // the prep is fused into the tensor-core kernels
+  if (check_only) return KDA_OK;
   // the CUDA-core kernels and the two-pass tensor-core kernels work in the
   // caller's workspace; at the tensor-core shape a NULL workspace selects the
   // single pass
@@ -160,6 +188,7 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
   }
   if ((long long)tok->num_tokens / chunk + 2LL * tok->num_seqs > 0x7fffffffLL)
     return KDA_ESHAPE;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::PrefillParams p = {};
@@ -184,6 +213,7 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
   p.ckpt_every = ckpt_every;
   p.max_chunks = kda::prefill_max_chunks(tok->num_tokens, tok->num_seqs, chunk);
   p.raw = raw ? 1 : 0;
+  p.spin_limit = kda::wait_limit_polls();
   return cuda_status(kda::launch_prefill(p, tok->dtype, tok->d_k, chunk,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -201,6 +231,7 @@ int verify_impl(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
     return KDA_EINVAL;
   if (tok->num_seqs == 0) return KDA_OK;
   if (!state_slots) return KDA_EINVAL;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::VerifyParams p = verify_params(pool, ring, state_slots, tok->num_seqs, err);
@@ -220,6 +251,15 @@ int verify_impl(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
 }
 
 }  // namespace
+
+namespace kda {
+int prefill_check_args(const kda_tokens *tok, kda_state_pool *pool,
+                       const int32_t *state_slots, const int32_t *ckpt_slots,
+                       int32_t max_ckpt, int32_t ckpt_every, int32_t chunk) {
+  return prefill_impl(tok, pool, state_slots, ckpt_slots, max_ckpt, ckpt_every, chunk,
+                      nullptr, nullptr, 0, nullptr, true, false, true);
+}
+}  // namespace kda
 
 extern "C" {
 
@@ -321,6 +361,7 @@ int kda_commit(const int32_t *accepted_len, const int32_t *state_slots,
   if (num_seqs < 0) return KDA_EINVAL;
   if (num_seqs == 0) return KDA_OK;
   if (!accepted_len || !state_slots) return KDA_EINVAL;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::CommitParams p = {accepted_len, state_slots, ring->ctrl, err, num_seqs,
@@ -343,6 +384,7 @@ int kda_commit_layers(const int32_t *accepted_len, const int32_t *state_slots,
     if ((st = check_ring(&rings[l], KDA_F32, false))) return st;
     p.ctrl[l] = rings[l].ctrl;
   }
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   p.accepted_len = accepted_len;
@@ -367,6 +409,7 @@ int kda_materialize(const int32_t *state_slots, int32_t num_seqs,
   if (num_seqs < 0 || num_seqs > kMaxGridY) return KDA_EINVAL;
   if (num_seqs == 0) return KDA_OK;
   if (!state_slots) return KDA_EINVAL;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::VerifyParams p = verify_params(pool, ring, state_slots, num_seqs, err);
@@ -384,6 +427,7 @@ int kda_ring_reset(const int32_t *slots, int32_t n, const kda_state_pool *pool,
   if (n < 0) return KDA_EINVAL;
   if (n == 0) return KDA_OK;
   if (!slots) return KDA_EINVAL;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::CommitParams p = {nullptr, slots, ring->ctrl, err, n, pool->num_heads,
@@ -399,6 +443,7 @@ int kda_gather_states(const kda_state_pool *pool, const int32_t *slots,
   if (n == 0) return KDA_OK;
   if (!slots || !out) return KDA_EINVAL;
   if (!aligned16(out)) return KDA_EALIGN;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::SlotCopyParams p = {};
@@ -420,6 +465,7 @@ int kda_copy_slots(kda_state_pool *pool, const int32_t *src, const int32_t *dst,
   if (n < 0 || n > kMaxGridY) return KDA_EINVAL;
   if (n == 0) return KDA_OK;
   if (!src || !dst) return KDA_EINVAL;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::SlotCopyParams p = {};
@@ -444,6 +490,7 @@ int kda_verify_snapshot(const kda_tokens *tok, int32_t max_T,
   if (tok->num_seqs == 0) return KDA_OK;
   if (!state_slots || !snapshots) return KDA_EINVAL;
   if (!aligned16(snapshots)) return KDA_EALIGN;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::SnapshotParams p = {};
@@ -478,6 +525,7 @@ int kda_commit_snapshot(const int32_t *accepted_len, const int32_t *state_slots,
   if (num_seqs == 0) return KDA_OK;
   if (!accepted_len || !state_slots || !snapshots) return KDA_EINVAL;
   if (!aligned16(snapshots)) return KDA_EALIGN;
+  if (device_unsafe()) return KDA_EDEVICE;
   unsigned *err = device_error_word();
   if (!err) return KDA_ECUDA;
   kda::SnapshotParams p = {};
@@ -505,6 +553,11 @@ int kda_get_device_error(int32_t *host_bits, kda_stream_t stream) {
   if (cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(zero)) != cudaSuccess)
     return KDA_ECUDA;
   *host_bits = (int32_t)bits;
+  if (bits & KDA_DERR_UNSAFE) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64)
+      g_unsafe_devices.fetch_or(1ull << dev);
+  }
   return bits ? KDA_EDEVICE : KDA_OK;
 }
 

@@ -64,6 +64,7 @@ struct VerifyParams {
   int B, N, H, P, depth, max_T;
   int mode;             // 0 = verify, 1 = materialize (no tokens)
   int prefetch_stride;  // CTAs of the first wave (0: no L2 prefetch)
+  int spin_limit;       // polls of a bounded wait before it gives up
 };
 
 struct CommitParams {
@@ -120,6 +121,7 @@ struct PrefillParams {
   unsigned int *err;
   int B, N, H, P, max_ckpt, ckpt_every, max_chunks;
   int raw;  // inputs are projections: k unnormalised, alpha and beta logits
+  int spin_limit;  // polls of a bounded wait before it gives up
 };
 
 // Workspace geometry of the chunked prefill (shared with the size query):
@@ -186,6 +188,21 @@ __device__ __forceinline__ ChunkLoc locate_chunk(const PrefillParams &p, int g,
   return c;
 }
 
+// Polls of a bounded wait on the tensor cores or the copy engine before it
+// gives up (KDA_DERR_TIMEOUT): the library's default, or the value a test set
+// through kda_set_wait_limit.  The second, drain-before-exit wait of a kernel
+// always uses kDrainWaitPolls.
+constexpr int kDefaultWaitPolls = 1 << 22;
+constexpr int kDrainWaitPolls = 1 << 26;
+int wait_limit_polls();
+
+// The argument checks of kda_prefill_chunked that do not concern the
+// workspace (pool, tokens, chunk, checkpoints, slot table); KDA_OK or the
+// status that call would return.
+int prefill_check_args(const kda_tokens *tok, kda_state_pool *pool,
+                       const int32_t *state_slots, const int32_t *ckpt_slots,
+                       int32_t max_ckpt, int32_t ckpt_every, int32_t chunk);
+
 // Verify launch geometry: dynamic shared memory for (D, ring depth, max_T),
 // and the longest speculative segment the kernel supports (ring depth limit).
 size_t verify_smem_bytes(int D, int depth, int max_T, kda_dtype dt);
@@ -194,6 +211,10 @@ int verify_max_spec_tokens();
 // Launchers: return cudaError_t of the launch.
 cudaError_t launch_verify(const VerifyParams &p, kda_dtype dt, int D,
                           cudaStream_t s);
+// The pipelined verify kernel (d = 128, bf16, ring depth <= 8, <= 8 tokens
+// per row): whether it serves these parameters, and its launcher.
+bool verify_pipe_applies(const VerifyParams &p, kda_dtype dt, int D);
+cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s);
 cudaError_t launch_commit(const CommitParams &p, cudaStream_t s);
 cudaError_t launch_commit_layers(const CommitLayersParams &p, cudaStream_t s);
 cudaError_t launch_ring_reset(const CommitParams &p, cudaStream_t s);

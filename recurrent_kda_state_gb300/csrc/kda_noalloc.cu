@@ -52,7 +52,12 @@ extern "C" int kda_prefill_chunked_noalloc(const kda_tokens *tok,
   if (need == 0 || (tc && need > KDA_NOALLOC_SCRATCH_BYTES))
     return kda_prefill_chunked(tok, pool, state_slots, ckpt_slots, max_ckpt,
                                ckpt_every, chunk, start_pos, nullptr, 0, stream);
-  if (need > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ENOSPC;
+  if (need > KDA_NOALLOC_SCRATCH_BYTES) {
+    // a malformed call reports what kda_prefill_chunked would, not the size
+    const int st = kda::prefill_check_args(tok, pool, state_slots, ckpt_slots, max_ckpt,
+                                           ckpt_every, chunk);
+    return st != KDA_OK ? st : KDA_ENOSPC;
+  }
   unsigned char *ws = scratch_address();
   if (!ws) return KDA_ECUDA;
   return kda_prefill_chunked(tok, pool, state_slots, ckpt_slots, max_ckpt,

@@ -50,7 +50,6 @@ namespace kda {
 namespace {
 
 constexpr int kD = 128, kC = 64, kNC = 32, kThreads = 256;
-constexpr int kSpin = 1 << 22;  // polls of a tensor-core completion barrier
 
 // Byte offsets from a 1024-byte aligned base.
 struct Lay {
@@ -290,8 +289,8 @@ __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t off) {
 
 // Every thread waits for the barrier's phase (bounded); they agree whether
 // it completed.  On success the phase advances.
-__device__ __forceinline__ bool tc_wait(uint64_t *mbar, uint32_t &phase, int tid) {
-  const bool ok = umma::mbar_wait(mbar, phase, kSpin);
+__device__ __forceinline__ bool tc_wait(uint64_t *mbar, uint32_t &phase, int limit) {
+  const bool ok = umma::mbar_wait(mbar, phase, limit);
   const bool all = __syncthreads_and(ok) != 0;
   if (all) phase ^= 1u;
   umma::fence_after_sync();
@@ -421,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     stage_owed = true;
   };
   stage(0);
-  bool ok = true;
+  bool ok = true, mma_owed = false;  // an MMA round in flight
   for (int q = 0; q < nch; ++q) {
     const int s_loc = max(0, q * kC - r0);
     const int e_loc = min(L, (q + 1) * kC - r0);
@@ -431,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (channel pair cp, token quarter tq) takes channels 2cp, 2cp+1 of rows
     // 16tq .. 16tq+15: cumulative log-decay (padded rows: alpha = 1), then the
     // scaled operand tiles; S~ from the state rows this thread owns.
-    if (!(ok = tc_wait(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), sphase, tid))) break;
+    if (!(ok = tc_wait(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), sphase, p.spin_limit))) break;
     stage_owed = false;
     if (tid < kC) {
       const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + Lay::BST)[tid * 8 + (h & 7)];
@@ -587,7 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(mbar);
     }
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
+    mma_owed = false;
     {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> tile
       float g[32];
       {
@@ -655,7 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(mbar);
     }
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
+    mma_owed = false;
     if (q + 1 < nch) stage(q + 1);  // the R2 B tile and X are free now
     float up[16];
     if (c < 64) {  // W~ row t -> rows 0..63 of the R3 A tile; U' kept
@@ -686,7 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(mbar);
     }
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
+    mma_owed = false;
     if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
       const int t = c;
       float ws[16], ws2[16];
@@ -715,7 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::commit(mbar);
     }
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    mma_owed = true;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
+    mma_owed = false;
     {
       float acc[16], acc2[16];
       umma::tmem_ld16(tl + kAcc4 + 16 * hf, acc);
@@ -762,7 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       set_error(p.err, KDA_DERR_TIMEOUT);
       // one more bounded chance for the tensor cores before TMEM is freed
-      umma::mbar_wait(mbar, phase, 1 << 26);
+      if (mma_owed && !umma::mbar_wait(mbar, phase, kDrainWaitPolls))
+        set_error(p.err, KDA_DERR_UNSAFE);
     }
   } else {
     float *dst = p.pool + ((size_t)slot * H + h) * kD * kD;
@@ -771,7 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // no copy into shared memory outlives the CTA
   if (stage_owed && tid == 0)
-    umma::mbar_wait(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), sphase, 1 << 26);
+    if (!umma::mbar_wait(reinterpret_cast<uint64_t *>(sm + Lay::SBAR), sphase, kDrainWaitPolls))
+      set_error(p.err, KDA_DERR_UNSAFE);
   umma::fence_before_sync();
   __syncthreads();
   if (tid < 32) umma::tmem_dealloc(tmem, 512);
@@ -907,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = it / H, h = it - (it / H) * H;
     const ChunkLoc cl = locate_chunk(p, g, kC);
     const int n = cl.n, m = n >> 1;
-    if (!(ok = tc_wait(sbar_p, sphase, tid))) break;
+    if (!(ok = tc_wait(sbar_p, sphase, p.spin_limit))) break;
     stage_owed = false;
     // ---- E1 (as in the fused kernel; V^T over all 128 value columns)
     if (tid < kC) {
@@ -1025,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(mbar);
     }
     mma_owed = true;
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
     {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> tile
       float gv[32];
@@ -1106,7 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(mbar);
     }
     mma_owed = true;
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
     // R2 has read its operands: the next item's rows can land in the staging
     // areas while this item's epilogue and export run
@@ -1158,8 +1167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok && tid == 0) {
     set_error(p.err, KDA_DERR_TIMEOUT);
     // one more bounded chance for what is still in flight
-    if (mma_owed) umma::mbar_wait(mbar, phase, 1 << 26);
-    if (stage_owed) umma::mbar_wait(sbar_p, sphase, 1 << 26);
+    if ((mma_owed) && !umma::mbar_wait(mbar, phase, kDrainWaitPolls))
+      set_error(p.err, KDA_DERR_UNSAFE);
+    if ((stage_owed) && !umma::mbar_wait(sbar_p, sphase, kDrainWaitPolls))
+      set_error(p.err, KDA_DERR_UNSAFE);
   }
   if (tid == 0) umma::bulk_wait_read();  // shared memory stays until read
   umma::fence_before_sync();
@@ -1257,7 +1268,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     const float *up = reinterpret_cast<const float *>(sm + LayS::SMALL +
                                                       (q & 1) * LayS::SMALL_BYTES);
     const float *vec = up + 64 * kNC;
-    if (!(ok = tc_wait(g1bar, ph1, tid))) break;
+    if (!(ok = tc_wait(g1bar, ph1, p.spin_limit))) break;
     owe1 = false;
     if (tid == 32 && q + 2 < nch) {  // two chunks ahead: into L2 (not the MMA warp)
       const uint8_t *e = entry(q + 2);
@@ -1285,7 +1296,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       umma::commit(mbar);
     }
     mma_owed = true;
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
     if (q + 1 < nch) issue_g1(q + 1);  // [W~; Q~] is free; the other parity too
     if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
@@ -1304,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       }
       put16_mn(sm, LayS::UT, t, 16 * hf, ws);
     }
-    if (!(ok = tc_wait(g2bar, ph2, tid))) break;
+    if (!(ok = tc_wait(g2bar, ph2, p.spin_limit))) break;
     owe2 = false;
     tiles_ready();
     // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
@@ -1326,7 +1337,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       umma::commit(mbar);
     }
     mma_owed = true;
-    if (!(ok = tc_wait(mbar, phase, tid))) break;
+    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
     if (q + 1 < nch) issue_g2(q + 1);  // K^ and [T; M] are free
     {
@@ -1373,7 +1384,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   if (!ok) {
     if (tid == 0) {
       set_error(p.err, KDA_DERR_TIMEOUT);
-      if (mma_owed) umma::mbar_wait(mbar, phase, 1 << 26);
+      if ((mma_owed) && !umma::mbar_wait(mbar, phase, kDrainWaitPolls))
+        set_error(p.err, KDA_DERR_UNSAFE);
     }
   } else {
     float *dst = p.pool + ((size_t)slot * H + h) * kD * kD;
@@ -1382,8 +1394,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   }
   // no copy into shared memory outlives the CTA
   if (tid == 0) {
-    if (owe1) umma::mbar_wait(g1bar, ph1, 1 << 26);
-    if (owe2) umma::mbar_wait(g2bar, ph2, 1 << 26);
+    if ((owe1) && !umma::mbar_wait(g1bar, ph1, kDrainWaitPolls))
+      set_error(p.err, KDA_DERR_UNSAFE);
+    if ((owe2) && !umma::mbar_wait(g2bar, ph2, kDrainWaitPolls))
+      set_error(p.err, KDA_DERR_UNSAFE);
   }
   umma::fence_before_sync();
   __syncthreads();

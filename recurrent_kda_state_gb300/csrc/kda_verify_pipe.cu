@@ -1,0 +1,959 @@
+// Verify + lazily fused ReplaySSM commit + ordinary decode as a persistent,
+// warp-specialised pipeline: d_k = d_v = 128, bf16 inputs, ring depth <= 8,
+// at most 8 tokens per row.  ("ReplaySSM shrinks rollback state" and "Small
+// tensor copies leave the hot path", vLLM Kimi K3 optimisation page.)
+//
+// Each (sequence, head) unit computes exactly what verify_kernel computes --
+// replay the accepted ring entries with kda_step, store the state once, then
+// the drafted tokens' outputs from the committed state in chunk form, or the
+// ordinary rows' tokens applied and committed -- and its state is read from
+// HBM once and written at most once.  What changes is how the units flow
+// through an SM: one CTA per SM walks the units u = blockIdx.x + n * gridDim.x
+// with three roles working on different units at once:
+//
+//   producer (1 warp): the units' slot, segment, ring word and beta values
+//       for 32 units at a time (one unit per lane); then per unit its 64 KiB
+//       state with four bulk copies into one of two state stages (two units
+//       ahead of the consumers), its tokens (k, alpha, v, q rows) and pending
+//       ring entries (k, alpha, v) with per-lane 16-byte async copies into
+//       one of three token stages, each copy as soon as its stage is free,
+//       and an L2 hint for the next unit's state;
+//   prep (3 warps): as soon as a unit's token stage lands, for drafts: the decay
+//       products gamma_t, K~ = gamma k, Q~ = gamma q, K^ = k / gamma, the
+//       T x T pair products A = K^ K~^T, B = K^ Q~^T on the tensor cores, the
+//       small triangular inverse M = (I + diag(beta) A)^-1 diag(beta) and
+//       N = B M, then Q^ = Q~ - N K~ (as bf16 hi/lo MMA fragments) and
+//       W = N v; the drafted inputs appended to the unit's ring and its
+//       control word set;
+//   consumers (8 warps): the state from its stage into registers (the stage
+//       is released at once), the replay as soon as the token stage lands
+//       (while the prep still works on it), the state store, and once the
+//       prep is done the drafts' outputs o_t = (S^T Q^)_t + W_t with bf16
+//       hi/lo tensor-core MMAs taken straight from the registers that hold S.
+//
+// so that while the consumers work on one unit the next units' bytes are in
+// flight: the kernel keeps HBM busy instead of alternating load and compute
+// phases.  Every wait is bounded and per warp; a wait that runs out sets
+// KDA_DERR_TIMEOUT, every role stops taking units, and the producer waits
+// (bounded) for its copies in flight before the CTA exits.
+//
+// The consumers' thread mapping and kda_step are those of verify_kernel, so
+// replayed states are bit-identical to ordinary decode in either kernel.
+//
+// Chunk form of the drafts.  With x_t = (S^T K~_t)_j and y_t = (S^T Q~_t)_j
+// for value column j, the corrections delta = M (v_j - x) and the outputs
+// o_t = y_t + sum_{s<=t} B_ts delta_s unroll the recurrence over the drafted
+// tokens; substituting delta, o = S^T (Q~ - N K~) + N v_j with N = B M, so
+// the consumers need one product S^T Q^ per unit and no solve.
+//
+// MMA mapping (mma.sync m16n8k16, bf16 in, fp32 accumulate).  Warp w owns the
+// value columns 16w .. 16w+15; lane (g = lane/4, r = lane%4) holds columns
+// j0 = 16w + 2g, j0 + 1 and key rows c = 16f + 4r + {0..3} of k-tile f.
+// Reading A row g as column j0, row g + 8 as column j0 + 1, and the k index
+// 2r + {0,1} as c = 16f + 4r + {0,1}, 2r + 8 + {0,1} as c = 16f + 4r + {2,3},
+// the four state pairs of k-tile f are exactly the A fragment of that tile;
+// B column n = drafted row t needs X[t][16f + 4r .. +3], which the prep warps
+// store in fragment order.  D row g / g+8, column 2r + {0,1} is then
+// (S^T X)_{j0 / j0+1, t = 2r + {0,1}}.  The pair products use K^ as A (rows
+// s = 0..7, rows 8..15 zero) in the same k order, so D row s, column t is
+// K^_s . X_t.
+#include <mutex>
+
+#include "kda_internal.cuh"
+#include "kda_step.cuh"
+#include "kda_umma.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int PD = 128;                 // head dim
+constexpr int PT = 8;                   // drafted rows per MMA tile (T <= 8)
+constexpr int kDepthMax = 8;            // ring entries a stage holds
+constexpr int kConsumerWarps = 8;       // 2 * PD threads: the state owners
+constexpr int kProducerWarp = 8;
+constexpr int kPrepWarp0 = 9, kPrepWarps = 3, kPrepThreads = 32 * kPrepWarps;
+constexpr int kPipeThreads = 32 * (kConsumerWarps + 1 + kPrepWarps);
+constexpr int kPrepBar = 1;             // named barrier of the prep warps
+constexpr int kTStages = 3;             // token stages
+constexpr int kSStages = 2;             // state stages
+constexpr int kMetaBatch = 32;          // units whose words one lane each reads at once
+constexpr int kMetaRing = 2 * kMetaBatch;
+
+typedef __nv_bfloat16 bf16;
+typedef Rec<PD, bf16> R;
+
+// Per-unit facts the producer hands to the other roles.
+struct UnitMeta {
+  int slot, tok0, T, spec, acc, skip, pad0, pad1;
+};
+// The producer's copy of a unit's words: the meta and the beta values it
+// places (ring entries 0..7, then drafted tokens 0..7), raw input bits.
+struct MetaEnt {
+  UnitMeta m;
+  unsigned short b[16];
+};
+static_assert(sizeof(MetaEnt) == 64, "meta ring entries are 64 bytes");
+
+// Shared-memory carve-up, byte offsets from a 1024-aligned base.
+struct PipeLayout {
+  // state stage: state [PD][PD] fp32 (the pool's layout: row j = value
+  // column), meta (slot and whether the state was loaded)
+  static constexpr int kSsState = 0;
+  static constexpr int kSsMeta = PD * PD * 4;
+  static constexpr int kSStage = (kSsMeta + (int)sizeof(UnitMeta) + 127) & ~127;
+  // token stage:
+  //   rec   the drafted / ordinary tokens (Rec layout, input dtype)
+  //   rv    pending ring entries' v [8][PD] (input dtype), rb their beta [8]
+  //   rk    pending ring entries' k, alpha [2][8][PD] (input dtype)
+  //   frag  three regions of 8 k-tiles x 32 lanes x {hi01, hi23, lo01, lo23}:
+  //         the MMA fragments of K~, Q~ (then Q^), K^ (then W, fp32 [PT][PD])
+  //   am bm pair matrices A, B [PT][PT] fp32; flag (explicit pair products);
+  //   n     N = B M [PT][PT] fp32; meta (complete).  Once the pair
+  //         products are taken, the K~ fragments' region holds the small
+  //         matrices that give M.
+  static constexpr int kTsRec = 0;
+  static constexpr int kTsRv = kTsRec + PT * R::kBytes;
+  static constexpr int kTsRb = kTsRv + kDepthMax * PD * 2;
+  static constexpr int kTsRk = kTsRb + 16;
+  static constexpr int kTsFrag = kTsRk + 2 * kDepthMax * PD * 2;
+  static constexpr int kTsAm = kTsFrag + 3 * 8 * 32 * 16;
+  static constexpr int kTsBm = kTsAm + PT * PT * 4;
+  static constexpr int kTsFlag = kTsBm + PT * PT * 4;
+  static constexpr int kTsN = kTsFlag + 16;
+  static constexpr int kTsMeta = kTsN + PT * PT * 4;
+  static constexpr int kTStage = (kTsMeta + (int)sizeof(UnitMeta) + 127) & ~127;
+  // regions
+  static constexpr int kSStages0 = 0;
+  static constexpr int kTStages0 = kSStages0 + kSStages * kSStage;
+  // the producer's ring of unit words, kMetaRing entries of MetaEnt
+  static constexpr int kMetas = kTStages0 + kTStages * kTStage;
+  // barriers: sfull[2] sempty[2] tfull[3] pfull[3] tempty[3]
+  static constexpr int kBars = kMetas + kMetaRing * 64;
+  static constexpr int kNumBars = 2 * kSStages + 3 * kTStages;
+  static constexpr int kAbort = kBars + kNumBars * 8;
+  static constexpr int kTotal = kAbort + 16 + 1024;  // + alignment slack
+};
+static_assert(PipeLayout::kTotal <= 227 * 1024, "verify pipeline shared memory");
+static_assert(R::kBytes % 16 == 0, "records must keep 16-byte alignment");
+static_assert(PipeLayout::kTsRk % 16 == 0 && PipeLayout::kTsFrag % 16 == 0,
+              "token stage parts must keep 16-byte alignment");
+
+struct Bars {
+  uint64_t *sfull, *sempty, *tfull, *pfull, *tempty;
+  __device__ explicit Bars(unsigned char *smb) {
+    uint64_t *b = reinterpret_cast<uint64_t *>(smb + PipeLayout::kBars);
+    sfull = b;
+    sempty = b + kSStages;
+    tfull = b + 2 * kSStages;
+    pfull = tfull + kTStages;
+    tempty = pfull + kTStages;
+  }
+};
+
+// ------------------------------------------------------------ mbarriers
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               :: "r"(umma::smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+      :: "r"(umma::smem_u32(bar)), "r"(bytes) : "memory");
+}
+// 16 bytes global -> shared without registers; this thread's copies so far
+// arrive on an mbarrier (counted in its expected arrivals) once they land.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+               :: "r"(umma::smem_u32(bar)) : "memory");
+}
+// Use k of a barrier that completes once per use: every lane of the warp
+// waits for use k (parity k & 1), and the warp agrees on the outcome, so a
+// warp never splits over a shuffle or an MMA.  Bounded; on running out the
+// warp sets the CTA's abort flag and the error bit and returns false.
+__device__ __forceinline__ bool pipe_wait(uint64_t *bar, int use, int limit,
+                                          volatile int *abort_flag, unsigned *err) {
+  const bool ok = __all_sync(kFull, umma::mbar_wait(bar, (uint32_t)(use & 1), limit));
+  if (!ok && (threadIdx.x & 31) == 0) {
+    *abort_flag = 1;
+    set_error(err, KDA_DERR_TIMEOUT);
+  }
+  return ok;
+}
+// Whether the CTA is stopping, agreed by the warp.
+__device__ __forceinline__ bool stopping(volatile int *abort_flag) {
+  return __any_sync(kFull, *abort_flag != 0);
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ int named_and(int id, int n, int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(v), "r"(id), "r"(n) : "memory");
+  return r;
+}
+__device__ __forceinline__ int named_or(int id, int n, int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(v), "r"(id), "r"(n) : "memory");
+  return r;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                         uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// a state pair (c, c+1) -> bf16x2 hi = rn(x), lo = rn(x - hi), c in the low half
+__device__ __forceinline__ void split_pair(f2 x, uint32_t &hi, uint32_t &lo) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+  umma::split_bf16x2(a, b, hi, lo);
+}
+
+// --------------------------------------------------------------- producer
+// The words of units b0 .. b0 + 31 of this CTA (n = b0 + lane), one unit per
+// lane, into the meta ring (entry n % kMetaRing), which only the producer
+// reads.  Round one: slot, segment and row kind -- all a state copy needs.
+__device__ void fetch_batch_a(const VerifyParams &p, unsigned char *smb, int b0, int cnt,
+                              int lane) {
+  typedef PipeLayout L;
+  const int n = b0 + lane;
+  if (n < cnt) {
+    MetaEnt e = {};
+    UnitMeta &m = e.m;
+    const int H = p.H, u = blockIdx.x + n * gridDim.x, i = u / H;
+    int c0 = 0, c1 = 0;
+    m.slot = p.state_slots[i];
+    if (p.mode == 0) {
+      c0 = p.cu_seqlens[i];
+      c1 = p.cu_seqlens[i + 1];
+      m.spec = p.is_spec ? (p.is_spec[i] != 0) : 1;
+    }
+    int bad = 0;
+    if (m.slot < 0 || m.slot >= p.P) bad = KDA_DERR_SLOT;
+    if (p.mode == 0 && !bad) {
+      if (c0 < 0 || c1 < c0 || c1 > p.N) {
+        bad = KDA_DERR_SEGMENT;
+      } else {
+        m.tok0 = c0;
+        m.T = c1 - c0;
+        if (m.T > p.max_T || (m.spec && m.T > p.depth)) bad = KDA_DERR_DEPTH;
+      }
+    }
+    if (bad) {
+      set_error(p.err, (unsigned)bad);
+      m.skip = 1;
+      m.T = 0;
+    }
+    reinterpret_cast<MetaEnt *>(smb + L::kMetas)[n % kMetaRing] = e;
+  }
+  __syncwarp();
+}
+
+// Round two: the ring word and the beta values the unit's stages need.
+__device__ void fetch_batch_b(const VerifyParams &p, unsigned char *smb, int b0, int cnt,
+                              int lane) {
+  typedef PipeLayout L;
+  const int n = b0 + lane;
+  if (n < cnt) {
+    MetaEnt &e = reinterpret_cast<MetaEnt *>(smb + L::kMetas)[n % kMetaRing];
+    UnitMeta &m = e.m;
+    if (!m.skip) {
+      const int H = p.H, u = blockIdx.x + n * gridDim.x, h = u - (u / H) * H;
+      const size_t unit = (size_t)m.slot * H + h;
+      const int2 c = *reinterpret_cast<const int2 *>(p.ctrl + unit * 2);
+      const bool ok = c.x >= 0 && c.x <= p.depth && c.y >= 0 && c.y <= c.x;
+      const unsigned short *rb = reinterpret_cast<const unsigned short *>(p.rb) + unit * p.depth;
+      const unsigned short *tb = reinterpret_cast<const unsigned short *>(p.beta);
+      unsigned short bv[16];
+#pragma unroll
+      for (int q = 0; q < kDepthMax; ++q) bv[q] = q < p.depth ? rb[q] : 0;
+#pragma unroll
+      for (int q = 0; q < PT; ++q)
+        bv[kDepthMax + q] = q < m.T ? tb[(size_t)(m.tok0 + q) * H + h] : 0;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) e.b[q] = bv[q];
+      if (!ok) {
+        set_error(p.err, KDA_DERR_RING);
+        m.skip = 1;
+        m.T = 0;
+      } else {
+        m.acc = c.y;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void fetch_batch(const VerifyParams &p, unsigned char *smb, int b0,
+                                            int cnt, int lane) {
+  fetch_batch_a(p, smb, b0, cnt, lane);
+  fetch_batch_b(p, smb, b0, cnt, lane);
+}
+
+__device__ __forceinline__ const MetaEnt &meta_of(unsigned char *smb, int n) {
+  return reinterpret_cast<const MetaEnt *>(smb + PipeLayout::kMetas)[n % kMetaRing];
+}
+
+// L2 hint for unit n's state (lane 0).
+__device__ __forceinline__ void prefetch_state(const VerifyParams &p, unsigned char *smb,
+                                               int n, int lane) {
+  const MetaEnt &e = meta_of(smb, n);
+  if (lane == 0 && !e.m.skip) {
+    const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
+    umma::prefetch_l2(p.pool + ((size_t)e.m.slot * p.H + h) * PD * PD, PD * PD * 4);
+  }
+}
+
+// Unit n's state into state stage n % 2: four 16 KiB bulk copies completing
+// on the stage's barrier, after the meta (lane 0's arrival).
+__device__ void issue_state(const VerifyParams &p, unsigned char *smb, const Bars &bars,
+                            int n, int lane) {
+  typedef PipeLayout L;
+  const int s = n % kSStages;
+  unsigned char *ss = smb + L::kSStages0 + s * L::kSStage;
+  const UnitMeta m = meta_of(smb, n).m;
+  if (lane == 0) {
+    *reinterpret_cast<UnitMeta *>(ss + L::kSsMeta) = m;
+    if (m.skip) mbar_arrive(&bars.sfull[s]);
+    else mbar_arrive_tx(&bars.sfull[s], PD * PD * 4);
+  }
+  __syncwarp();
+  if (!m.skip && lane < 4) {  // four 16 KiB pieces, one per lane
+    const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
+    const size_t unit = (size_t)m.slot * p.H + h;
+    constexpr uint32_t kPiece = PD * PD;  // bytes
+    umma::bulk_g2s(umma::smem_u32(ss + L::kSsState) + lane * kPiece,
+                   reinterpret_cast<const unsigned char *>(p.pool + unit * PD * PD) +
+                       lane * kPiece,
+                   kPiece, umma::smem_u32(&bars.sfull[s]));
+  }
+}
+
+// Unit n's tokens and pending ring entries into token stage n % 3: 16-byte
+// async copies spread over the lanes (each lane's copies arrive on the
+// stage's barrier when they land); the beta values and the meta by plain
+// stores, lane 0 arriving after them.
+__device__ void issue_tokens(const VerifyParams &p, unsigned char *smb, const Bars &bars,
+                             int n, int lane) {
+  typedef PipeLayout L;
+  const int k = n % kTStages;
+  unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
+  const MetaEnt &e = meta_of(smb, n);
+  const UnitMeta m = e.m;
+  if (!m.skip) {
+    const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
+    const size_t unit = (size_t)m.slot * p.H + h;
+    const uint32_t base = umma::smem_u32(ts);
+    // tokens: 64 chunks each (k, alpha, v, q rows of 16 chunks)
+    for (int c = lane; c < m.T * 64; c += 32) {
+      const int t = c >> 6, which = (c >> 4) & 3, c16 = c & 15;
+      const bf16 *src = reinterpret_cast<const bf16 *>(
+          which == 0 ? p.k : which == 1 ? p.alpha : which == 2 ? p.v : p.q);
+      const int off = which == 0 ? R::kK : which == 1 ? R::kA : which == 2 ? R::kV : R::kQ;
+      cp_async16(base + L::kTsRec + (t * R::kStride + off + c16 * 8) * 2,
+                 src + ((size_t)(m.tok0 + t) * p.H + h) * PD + c16 * 8);
+    }
+    // pending ring entries: k, alpha and v
+    for (int c = lane; c < m.acc * 48; c += 32) {
+      const int which = c / (16 * m.acc), r = c - which * 16 * m.acc;
+      const int q = r >> 4, c16 = r & 15;
+      const bf16 *src = reinterpret_cast<const bf16 *>(
+          which == 0 ? p.rk : which == 1 ? p.ra : p.rv);
+      const uint32_t dst = which == 2 ? L::kTsRv + q * PD * 2
+                                      : L::kTsRk + (which * kDepthMax + q) * PD * 2;
+      cp_async16(base + dst + c16 * 16, src + (unit * p.depth + q) * PD + c16 * 8);
+    }
+    if (lane < m.acc) reinterpret_cast<unsigned short *>(ts + L::kTsRb)[lane] = e.b[lane];
+    if (lane >= 8 && lane < 8 + m.T)
+      reinterpret_cast<unsigned short *>(ts + L::kTsRec)[(lane - 8) * R::kStride + R::kB] =
+          e.b[lane];
+  }
+  if (lane == 0) *reinterpret_cast<UnitMeta *>(ts + L::kTsMeta) = m;
+  cp_async_arrive(&bars.tfull[k]);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars.tfull[k]);
+}
+
+// Whether use k of a barrier has completed, without waiting; agreed by the
+// warp (every lane tests, so every lane that goes on has acquired it).
+__device__ __forceinline__ bool use_done(uint64_t *bar, int use) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(umma::smem_u32(bar)), "r"((uint32_t)(use & 1)) : "memory");
+  return __all_sync(kFull, done != 0);
+}
+
+// The producer issues each copy as soon as its stage is free, the state
+// copies and the token copies independently of each other: unit n's state
+// once the consumers have taken unit n - 2's state into registers, unit n's
+// tokens once they have finished unit n - 3.  Polling is bounded: `limit`
+// rounds with nothing to issue end the CTA's work with KDA_DERR_TIMEOUT.
+__device__ void producer(const VerifyParams &p, unsigned char *smb, int lane, int limit) {
+  typedef PipeLayout L;
+  const Bars bars(smb);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
+  const int units = p.B * p.H, G = gridDim.x, u0 = blockIdx.x;
+  const int cnt = u0 < units ? (units - u0 + G - 1) / G : 0;
+  int s_last[kSStages], t_last[kTStages];  // last use issued of each stage
+  for (int i = 0; i < kSStages; ++i) s_last[i] = -1;
+  for (int i = 0; i < kTStages; ++i) t_last[i] = -1;
+  // the first unit's slot and at once its state; then the rest of the first
+  // batches' words (units 0 and 1 were hinted into L2 before the wait)
+  int ns = 0, nt = 0, fetched = 0;
+  fetch_batch_a(p, smb, 0, cnt, lane);
+  if (cnt > 0) {
+    issue_state(p, smb, bars, 0, lane);
+    s_last[0] = 0;
+    ns = 1;
+  }
+  fetch_batch_b(p, smb, 0, cnt, lane);
+  fetched = cnt < kMetaBatch ? cnt : kMetaBatch;
+  int idle = 0;
+  while (ns < cnt || nt < cnt) {
+    if (stopping(abort_flag)) break;
+    bool did = false;
+    if (nt < cnt && nt < fetched && (nt < kTStages ||
+                                     use_done(&bars.tempty[nt % kTStages], nt / kTStages - 1))) {
+      issue_tokens(p, smb, bars, nt, lane);
+      t_last[nt % kTStages] = nt / kTStages;
+      ++nt;
+      did = true;
+    }
+    if (ns < cnt && ns < fetched && (ns < kSStages ||
+                                     use_done(&bars.sempty[ns % kSStages], ns / kSStages - 1))) {
+      issue_state(p, smb, bars, ns, lane);
+      s_last[ns % kSStages] = ns / kSStages;
+      if (ns + 1 < fetched) prefetch_state(p, smb, ns + 1, lane);
+      ++ns;
+      did = true;
+    }
+    // the next batch of words, once both streams are past the older half of
+    // the meta ring
+    if (fetched < cnt && (ns < nt ? ns : nt) >= fetched - kMetaBatch) {
+      fetch_batch(p, smb, fetched, cnt, lane);
+      fetched = fetched + kMetaBatch < cnt ? fetched + kMetaBatch : cnt;
+      did = true;
+    }
+    if (did) {
+      idle = 0;
+    } else if (++idle > limit) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        set_error(p.err, KDA_DERR_TIMEOUT);
+      }
+      break;
+    } else {
+      __nanosleep(64);
+    }
+  }
+  // copies still in flight land before the CTA may exit (normally the
+  // consumers have already waited for them)
+  if (lane == 0) {
+    for (int i = 0; i < kSStages; ++i)
+      if (s_last[i] >= 0 &&
+          !umma::mbar_wait(&bars.sfull[i], (uint32_t)(s_last[i] & 1), kDrainWaitPolls))
+        set_error(p.err, KDA_DERR_UNSAFE);
+    for (int i = 0; i < kTStages; ++i)
+      if (t_last[i] >= 0 &&
+          !umma::mbar_wait(&bars.tfull[i], (uint32_t)(t_last[i] & 1), kDrainWaitPolls))
+        set_error(p.err, KDA_DERR_UNSAFE);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------- prep
+__device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limit) {
+  typedef PipeLayout L;
+  const Bars bars(smb);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
+  const int units = p.B * p.H, G = gridDim.x, lane = pt & 31;
+  const int cnt = (int)blockIdx.x < units ? (units - (int)blockIdx.x + G - 1) / G : 0;
+  for (int n = 0; n < cnt; ++n) {
+    const int k = n % kTStages;
+    const int u = blockIdx.x + n * G, h = u - (u / p.H) * p.H;
+    // both prep warps take the same decision before any named barrier
+    bool go = !stopping(abort_flag);
+    if (go) go = pipe_wait(&bars.tfull[k], n / kTStages, limit, abort_flag, p.err);
+    if (!named_and(kPrepBar, kPrepThreads, go)) break;
+    unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
+    const UnitMeta m = *reinterpret_cast<const UnitMeta *>(ts + L::kTsMeta);
+    const bool drafts = !m.skip && m.spec && m.T > 0;
+    if (drafts) {
+      const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
+      unsigned char *fragb = ts + L::kTsFrag;
+      float *am = reinterpret_cast<float *>(ts + L::kTsAm);
+      float *bmat = reinterpret_cast<float *>(ts + L::kTsBm);
+      float *nm = reinterpret_cast<float *>(ts + L::kTsN);
+      const int T = m.T;
+      // thread: value / key channels c, c + 1 (c = 2 pt), every drafted row:
+      // gamma_t = prod_{r<=t} alpha_r, K~ = gamma k, Q~ = gamma q (zero past
+      // T), K^ = k / gamma; fragments of the three (the thread fills half of
+      // each 16-byte fragment entry)
+      const int c = 2 * pt, f = c >> 4, fq = (c >> 2) & 3, half = (c >> 1) & 1;
+      auto put = [&](int region, int t, float x, float y) {
+        uint32_t hi, lo;
+        umma::split_bf16x2(x, y, hi, lo);
+        uint32_t *e = reinterpret_cast<uint32_t *>(fragb + region * 4096 +
+                                                   ((f * 32) + 4 * t + fq) * 16);
+        e[half] = hi;
+        e[2 + half] = lo;
+      };
+      auto ld2 = [&](const bf16 *q) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(q));
+      };
+      int unsafe = 0;
+      float2 kt[PT], qt[PT];
+      const bool chan = pt < PD / 2;  // threads of a channel pair; the rest append the ring
+      if (chan) {
+        // every load first (the stores below could alias them for the
+        // compiler), then gamma, K~, Q~, K^ and their fragments
+        float2 av[PT], kv[PT], qv[PT];
+#pragma unroll
+        for (int t = 0; t < PT; ++t) {
+          const bf16 *rr = rec + t * R::kStride;
+          const bool in = t < T;
+          av[t] = in ? ld2(rr + R::kA + c) : make_float2(1.f, 1.f);
+          kv[t] = in ? ld2(rr + R::kK + c) : make_float2(0.f, 0.f);
+          qv[t] = in ? ld2(rr + R::kQ + c) : make_float2(0.f, 0.f);
+        }
+        float2 g = make_float2(1.f, 1.f);
+#pragma unroll
+        for (int t = 0; t < PT; ++t) {
+          g.x *= av[t].x;
+          g.y *= av[t].y;
+          kt[t] = make_float2(g.x * kv[t].x, g.y * kv[t].y);
+          qt[t] = make_float2(g.x * qv[t].x, g.y * qv[t].y);
+          float2 kh = make_float2(0.f, 0.f);
+          if (t < T) {
+            kh = make_float2(__fdividef(kv[t].x, g.x), __fdividef(kv[t].y, g.y));
+            unsafe |= !(fminf(g.x, g.y) >= 0x1p-60f && fmaxf(g.x, g.y) <= 0x1p60f);
+          }
+          put(0, t, kt[t].x, kt[t].y);
+          put(1, t, qt[t].x, qt[t].y);
+          put(2, t, kh.x, kh.y);
+        }
+      }
+      unsafe = named_or(kPrepBar, kPrepThreads, unsafe);
+      if (!unsafe) {
+        // the pair products on the tensor cores, one prep warp each:
+        // D row s, column t = K^_s . K~_t (warp 0: A) or K^_s . Q~_t (B)
+        const uint4 *frag = reinterpret_cast<const uint4 *>(fragb);
+        const int w = pt >> 5;
+        if (w < 2) {
+        float dp[4] = {0.f, 0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f};
+        float dr[4] = {0.f, 0.f, 0.f, 0.f};
+        uint4 fa[PD / 16], fb[PD / 16];
+#pragma unroll
+        for (int ff = 0; ff < PD / 16; ++ff) {
+          fa[ff] = frag[(2 * 8 + ff) * 32 + lane];  // K^ rows s
+          fb[ff] = frag[(w * 8 + ff) * 32 + lane];  // K~ or Q~
+        }
+#pragma unroll
+        for (int ff = 0; ff < PD / 16; ++ff) {
+          mma16816(dp, fa[ff].x, 0u, fa[ff].y, 0u, fb[ff].x, fb[ff].y);
+          mma16816(dq, fa[ff].z, 0u, fa[ff].w, 0u, fb[ff].x, fb[ff].y);
+          mma16816(dr, fa[ff].x, 0u, fa[ff].y, 0u, fb[ff].z, fb[ff].w);
+        }
+        float *dst = w == 0 ? am : bmat;
+        const int sI = lane >> 2, t0p = 2 * (lane & 3);
+        dst[t0p * PT + sI] = dp[0] + (dq[0] + dr[0]);
+        dst[(t0p + 1) * PT + sI] = dp[1] + (dq[1] + dr[1]);
+        }
+      } else {
+        // gamma left [2^-60, 2^60] somewhere (K^ may overflow): the pair
+        // matrices with explicit decay products instead, A_ts = sum_c k_tc
+        // k_sc prod_{s<w<=t} alpha_wc (s < t) and B_ts with q_t (s <= t);
+        // 4 lanes per pair, a quarter of the channels each
+        const int nb = T * (T + 1) / 2, npairs = T * T, rg = pt & 3;
+        for (int base = 0; base < npairs * 4; base += kPrepThreads) {
+          const int pair = (base + pt) >> 2;
+          float acc = 0.f;
+          int t = 0, sI = 0;
+          const bool valid = pair < npairs, isB = pair < nb;
+          if (valid) {
+            int r = isB ? pair : pair - nb;
+            if (isB) {
+              while (r >= t + 1) { r -= t + 1; ++t; }
+            } else {
+              t = 1;
+              while (r >= t) { r -= t; ++t; }
+            }
+            sI = r;
+            for (int cc = rg; cc < PD; cc += 4) {
+              float pr = 1.f;
+              for (int w = sI + 1; w <= t; ++w)
+                pr *= __bfloat162float(rec[w * R::kStride + R::kA + cc]);
+              const float x = __bfloat162float(rec[t * R::kStride + (isB ? R::kQ : R::kK) + cc]);
+              acc = fmaf(x * __bfloat162float(rec[sI * R::kStride + R::kK + cc]), pr, acc);
+            }
+          }
+          acc += __shfl_xor_sync(kFull, acc, 1);
+          acc += __shfl_xor_sync(kFull, acc, 2);
+          if (valid && rg == 0) {
+            if (isB) bmat[t * PT + sI] = acc;
+            else am[t * PT + sI] = acc;
+          }
+        }
+      }
+      named_sync(kPrepBar, kPrepThreads);
+      // M = (I + L)^-1 diag(beta) with L = diag(beta) A strictly lower (the
+      // drafts' corrections are delta = M (v - S^T K~)), and N = B M, so that
+      // o = S^T Q~ + N (v - S^T K~).  L is nilpotent (L^8 = 0), so
+      // (I + L)^-1 = (I - L)(I + L^2)(I + L^4) exactly: five rounds of 8 x 8
+      // products, thread pt < 64 taking entry (pt / 8, pt % 8) of each.
+      {
+        float *sl = reinterpret_cast<float *>(fragb);  // K~ fragments are spent
+        float *sl2 = sl + PT * PT, *sl4 = sl2 + PT * PT, *sx = sl4 + PT * PT,
+              *smm = sx + PT * PT;
+        const int ti = pt >> 3, ui = pt & 7;
+        const bool ent = pt < PT * PT;
+        auto beta_of = [&](int t) {
+          return t < T ? __bfloat162float(rec[t * R::kStride + R::kB]) : 0.f;
+        };
+        if (ent) sl[pt] = (ui < ti && ti < T) ? beta_of(ti) * am[ti * PT + ui] : 0.f;
+        named_sync(kPrepBar, kPrepThreads);
+        auto row_col = [&](const float *a, const float *b) {  // (a b)[ti][ui]
+          float x[PT], y[PT], acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < PT; ++q) { x[q] = a[ti * PT + q]; y[q] = b[q * PT + ui]; }
+#pragma unroll
+          for (int q = 0; q < PT; ++q) acc = fmaf(x[q], y[q], acc);
+          return acc;
+        };
+        if (ent) sl2[pt] = row_col(sl, sl);
+        named_sync(kPrepBar, kPrepThreads);
+        if (ent) {
+          const float l = sl[pt], l2 = sl2[pt];
+          const float x = (ti == ui ? 1.f : 0.f) - l + l2 - row_col(sl, sl2);  // (I - L)(I + L^2)
+          const float l4 = row_col(sl2, sl2);
+          sx[pt] = x;
+          sl4[pt] = l4;
+        }
+        named_sync(kPrepBar, kPrepThreads);
+        if (ent) smm[pt] = (sx[pt] + row_col(sx, sl4)) * beta_of(ui);  // X (I + L^4) diag(beta)
+        named_sync(kPrepBar, kPrepThreads);
+        if (ent) {
+          // N = B M with B masked to s <= t < T
+          float x[PT], y[PT], acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < PT; ++q) {
+            x[q] = (q <= ti && ti < T) ? bmat[ti * PT + q] : 0.f;
+            y[q] = smm[q * PT + ui];
+          }
+#pragma unroll
+          for (int q = 0; q < PT; ++q) acc = fmaf(x[q], y[q], acc);
+          nm[pt] = acc;
+        }
+      }
+      named_sync(kPrepBar, kPrepThreads);
+      // Q^ = Q~ - N K~ (fragments, over Q~'s) and W = N v (fp32, over K^'s):
+      // o_t = (S^T Q^)_t + W_t
+      float *wv = reinterpret_cast<float *>(fragb + 2 * 4096);
+      if (chan) {
+        // loads first: v of every drafted row, N's lower triangle
+        float2 vv[PT];
+        float nn[PT * (PT + 1) / 2];
+#pragma unroll
+        for (int u = 0; u < PT; ++u)
+          vv[u] = u < T ? ld2(rec + u * R::kStride + R::kV + c) : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int t = 0, i = 0; t < PT; ++t)
+#pragma unroll
+          for (int u = 0; u <= t; ++u, ++i) nn[i] = nm[t * PT + u];
+#pragma unroll
+        for (int t = 0, i = 0; t < PT; ++t) {
+          float2 qh = qt[t], wt = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u <= t; ++u, ++i) {
+            qh.x = fmaf(-nn[i], kt[u].x, qh.x);
+            qh.y = fmaf(-nn[i], kt[u].y, qh.y);
+            wt.x = fmaf(nn[i], vv[u].x, wt.x);
+            wt.y = fmaf(nn[i], vv[u].y, wt.y);
+          }
+          if (t >= T) qh = wt = make_float2(0.f, 0.f);
+          put(1, t, qh.x, qh.y);
+          *reinterpret_cast<float2 *>(wv + t * PD + c) = wt;
+        }
+      }
+    }
+    mbar_arrive(&bars.pfull[k]);
+    if (!m.skip) {
+      const size_t unit = (size_t)m.slot * p.H + h;
+      if (drafts && pt >= PD / 2) {
+        // ring append by the third prep warp, after the stage's products are
+        // handed over: entries 0..T-1 <- the drafted inputs (k, alpha, v,
+        // beta); this unit's pending entries were copied out with the stage
+        const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
+        const int at = pt - PD / 2, nat = kPrepThreads - PD / 2;
+        bf16 *wk = reinterpret_cast<bf16 *>(p.rk) + unit * p.depth * PD;
+        bf16 *wa = reinterpret_cast<bf16 *>(p.ra) + unit * p.depth * PD;
+        bf16 *wvr = reinterpret_cast<bf16 *>(p.rv) + unit * p.depth * PD;
+        constexpr int CH = PD / 8;  // 16-byte chunks per vector
+        for (int idx = at; idx < m.T * 3 * CH; idx += nat) {
+          const int t = idx / (3 * CH), r = idx - t * 3 * CH;
+          const int which = r / CH, ch = r - which * CH;
+          const int off = which == 0 ? R::kK : which == 1 ? R::kA : R::kV;
+          bf16 *dst = (which == 0 ? wk : which == 1 ? wa : wvr) + (size_t)t * PD + ch * 8;
+          *reinterpret_cast<uint4 *>(dst) =
+              *reinterpret_cast<const uint4 *>(rec + t * R::kStride + off + ch * 8);
+        }
+        if (at < m.T)
+          reinterpret_cast<bf16 *>(p.rb)[unit * p.depth + at] = rec[at * R::kStride + R::kB];
+      }
+      if (pt == 0) {
+        int32_t *c = p.ctrl + unit * 2;
+        c[0] = drafts ? m.T : 0;
+        c[1] = 0;
+      }
+    }
+    // this warp is done with the stage
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.tempty[k]);
+  }
+}
+
+// -------------------------------------------------------------- consumers
+__device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int limit) {
+  typedef PipeLayout L;
+  constexpr int F = PD / 16;
+  const Bars bars(smb);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
+  const int units = p.B * p.H, G = gridDim.x, H = p.H;
+  const int lane = tid & 31, rg = tid & 3, j0 = 2 * (tid >> 2);
+  const int cnt = (int)blockIdx.x < units ? (units - (int)blockIdx.x + G - 1) / G : 0;
+  for (int n = 0; n < cnt; ++n) {
+    const int s = n % kSStages, k = n % kTStages;
+    const int u = blockIdx.x + n * G, h = u - (u / H) * H;
+    if (stopping(abort_flag)) break;
+    if (!pipe_wait(&bars.sfull[s], n / kSStages, limit, abort_flag, p.err)) break;
+    f2 S[2][2 * F];
+    {
+      const unsigned char *ss = smb + L::kSStages0 + s * L::kSStage;
+      if (!reinterpret_cast<const UnitMeta *>(ss + L::kSsMeta)->skip) {
+        const ulonglong2 *c0 =
+            reinterpret_cast<const ulonglong2 *>(ss + L::kSsState + (size_t)j0 * PD * 4);
+        const ulonglong2 *c1 = c0 + PD / 4;
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+          const ulonglong2 x = c0[rg + 4 * f];
+          const ulonglong2 y = c1[rg + 4 * f];
+          S[0][2 * f] = x.x; S[0][2 * f + 1] = x.y;
+          S[1][2 * f] = y.x; S[1][2 * f + 1] = y.y;
+        }
+      }
+    }
+    // the state stage is free again (its bytes are in registers)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.sempty[s]);
+    // the unit's tokens and ring entries (the prep may still be working on
+    // the drafts' fragments)
+    if (!pipe_wait(&bars.tfull[k], n / kTStages, limit, abort_flag, p.err)) break;
+    unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
+    const UnitMeta m = *reinterpret_cast<const UnitMeta *>(ts + L::kTsMeta);
+    const size_t unit = (size_t)m.slot * H + h;
+    const bool drafts = !m.skip && m.spec && m.T > 0;
+    const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
+    auto store_state = [&]() {
+      ulonglong2 *c0 = reinterpret_cast<ulonglong2 *>(p.pool + unit * PD * PD + (size_t)j0 * PD);
+      ulonglong2 *c1 = c0 + PD / 4;
+#pragma unroll
+      for (int f = 0; f < F; ++f) {
+        c0[rg + 4 * f] = make_ulonglong2(S[0][2 * f], S[0][2 * f + 1]);
+        c1[rg + 4 * f] = make_ulonglong2(S[1][2 * f], S[1][2 * f + 1]);
+      }
+    };
+    if (!m.skip) {
+      // lazy commit: replay the accepted ring entries
+      const bf16 *rk = reinterpret_cast<const bf16 *>(ts + L::kTsRk);
+      const bf16 *ra = rk + kDepthMax * PD;
+      const bf16 *rv = reinterpret_cast<const bf16 *>(ts + L::kTsRv);
+      const bf16 *rb = reinterpret_cast<const bf16 *>(ts + L::kTsRb);
+      float o0 = 0.f, o1 = 0.f;
+      for (int t = 0; t < m.acc; ++t)
+        kda_step_ptrs<PD, false, bf16>(S, rk + t * PD, ra + t * PD, nullptr, rv + t * PD,
+                                       rb + t, rg, j0, o0, o1);
+      if (!m.spec) {
+        // ordinary decode (or materialize): apply and commit
+        for (int t = 0; t < m.T; ++t) {
+          kda_step<PD, true, bf16>(S, rec + t * R::kStride, rg, j0, o0, o1);
+          if (rg == 0)
+            *reinterpret_cast<float2 *>(p.o + ((size_t)(m.tok0 + t) * H + h) * PD + j0) =
+                make_float2(o0, o1);
+        }
+        if (m.acc > 0 || m.T > 0) store_state();
+      }
+    }
+    if (!m.skip && m.spec && m.acc > 0) store_state();  // the committed state
+    if (!pipe_wait(&bars.pfull[k], n / kTStages, limit, abort_flag, p.err)) break;
+    if (drafts) {
+      // drafts: o_t = (S^T Q^)_t + W_t, S^T Q^ from the registers on the
+      // tensor cores, hi*hi + lo*hi + hi*lo
+      const uint4 *frag = reinterpret_cast<const uint4 *>(ts + L::kTsFrag) + 8 * 32;
+      uint4 b[F];
+#pragma unroll
+      for (int f = 0; f < F; ++f) b[f] = frag[f * 32 + lane];
+      float dz[4] = {0.f, 0.f, 0.f, 0.f}, ez[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int f = 0; f < F; ++f) {
+        uint32_t ah[4], al[4];
+        split_pair(S[0][2 * f], ah[0], al[0]);      // row g,   k 2r..2r+1
+        split_pair(S[1][2 * f], ah[1], al[1]);      // row g+8, k 2r..2r+1
+        split_pair(S[0][2 * f + 1], ah[2], al[2]);  // row g,   k 2r+8..
+        split_pair(S[1][2 * f + 1], ah[3], al[3]);  // row g+8, k 2r+8..
+        mma16816(dz, ah[0], ah[1], ah[2], ah[3], b[f].x, b[f].y);
+        mma16816(ez, al[0], al[1], al[2], al[3], b[f].x, b[f].y);
+        mma16816(ez, ah[0], ah[1], ah[2], ah[3], b[f].z, b[f].w);
+      }
+      // D row g / g + 8 = column j0 / j0 + 1, columns 2r, 2r + 1 = rows t
+      const float *wv = reinterpret_cast<const float *>(ts + L::kTsFrag + 2 * 4096);
+      const int t0 = 2 * rg;
+      const float2 w0 = *reinterpret_cast<const float2 *>(wv + t0 * PD + j0);
+      const float2 w1 = *reinterpret_cast<const float2 *>(wv + (t0 + 1) * PD + j0);
+      if (t0 < m.T)
+        *reinterpret_cast<float2 *>(p.o + ((size_t)(m.tok0 + t0) * H + h) * PD + j0) =
+            make_float2(dz[0] + ez[0] + w0.x, dz[2] + ez[2] + w0.y);
+      if (t0 + 1 < m.T)
+        *reinterpret_cast<float2 *>(p.o + ((size_t)(m.tok0 + t0 + 1) * H + h) * PD + j0) =
+            make_float2(dz[1] + ez[1] + w1.x, dz[3] + ez[3] + w1.y);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.tempty[k]);
+  }
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 1) verify_pipe_kernel(const VerifyParams p) {
+  typedef PipeLayout L;
+  extern __shared__ float4 smem4[];
+  unsigned char *smb = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int units = p.B * p.H;
+  if (tid == 0) {
+    const Bars b(smb);
+    for (int i = 0; i < kSStages; ++i) {
+      umma::mbar_init(&b.sfull[i], 1);
+      umma::mbar_init(&b.sempty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kTStages; ++i) {
+      umma::mbar_init(&b.tfull[i], 32 + 1);  // async arrivals of the lanes + lane 0
+      umma::mbar_init(&b.pfull[i], kPrepThreads);
+      umma::mbar_init(&b.tempty[i], kConsumerWarps + kPrepWarps);
+    }
+    *reinterpret_cast<volatile int *>(smb + L::kAbort) = 0;
+  }
+  // Launched as a programmatic dependent of the previous kernel: until
+  // griddepcontrol.wait returns, only L2 prefetch hints for this CTA's first
+  // two units (state, ring word, ring beta, token rows), at the addresses the
+  // slot table and segment offsets give when read (relaxed reads that the
+  // previous kernel may still be writing: a stale value wastes a hint, and
+  // L2 is where that kernel's writes become visible, so nothing stale is
+  // used).
+  if (warp == kProducerWarp) {
+    // lanes 0, 1: the first two units' words and states; lanes 2, 3: their
+    // token rows (k, alpha, v, q of each drafted position)
+    const int n = lane & 1, u = blockIdx.x + n * gridDim.x;
+    if (lane < 4 && u < units) {
+      const int i = u / p.H, h = u - (u / p.H) * p.H;
+      if (lane < 2) {
+        int s0;
+        asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];"
+                     : "=r"(s0) : "l"(p.state_slots + i) : "memory");
+        if (s0 >= 0 && s0 < p.P) {
+          const size_t un = (size_t)s0 * p.H + h;
+          umma::prefetch_l2(p.pool + un * PD * PD, PD * PD * 4);
+          asm volatile("prefetch.global.L2 [%0];" :: "l"(p.ctrl + un * 2));
+          asm volatile("prefetch.global.L2 [%0];"
+                       :: "l"(reinterpret_cast<const bf16 *>(p.rb) + un * p.depth));
+        }
+      } else if (p.mode == 0) {
+        int c0, c1;
+        asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];"
+                     : "=r"(c0) : "l"(p.cu_seqlens + i) : "memory");
+        asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];"
+                     : "=r"(c1) : "l"(p.cu_seqlens + i + 1) : "memory");
+        if (c0 >= 0 && c1 >= c0 && c1 - c0 <= PT && c1 <= p.N) {
+          for (int t = c0; t < c1; ++t) {
+            const size_t row = ((size_t)t * p.H + h) * PD;
+            umma::prefetch_l2(reinterpret_cast<const bf16 *>(p.k) + row, PD * 2);
+            umma::prefetch_l2(reinterpret_cast<const bf16 *>(p.alpha) + row, PD * 2);
+            umma::prefetch_l2(reinterpret_cast<const bf16 *>(p.v) + row, PD * 2);
+            umma::prefetch_l2(reinterpret_cast<const bf16 *>(p.q) + row, PD * 2);
+            asm volatile("prefetch.global.L2 [%0];"
+                         :: "l"(reinterpret_cast<const bf16 *>(p.beta) + (size_t)t * p.H + h));
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int limit = p.spin_limit;
+  if (warp == kProducerWarp) producer(p, smb, lane, limit);
+  else if (warp >= kPrepWarp0) prep(p, smb, tid - 32 * kPrepWarp0, limit);
+  else consumer(p, smb, tid, limit);
+  __syncthreads();
+}
+
+}  // namespace
+
+bool verify_pipe_applies(const VerifyParams &p, kda_dtype dt, int D) {
+  return D == PD && dt == KDA_BF16 && p.depth <= kDepthMax && p.max_T <= PT;
+}
+
+cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
+  static std::mutex mu;
+  static int sms_of[64] = {};
+  static bool ready[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const size_t smem = PipeLayout::kTotal;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(verify_pipe_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      ready[dev] = true;
+    }
+    sms = sms_of[dev];
+  }
+  const int units = p.B * p.H;
+  if (units == 0 || sms < 1) return units == 0 ? cudaSuccess : cudaErrorInvalidDevice;
+  // the fewest CTAs that keep the most units per CTA at ceil(units / SMs):
+  // every CTA then walks the same number of units (give or take one)
+  const int per = (units + sms - 1) / sms;
+  const int grid = (units + per - 1) / per;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPipeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_pipe_kernel, p);
+}
+
+}  // namespace kda

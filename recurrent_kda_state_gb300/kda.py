@@ -17,7 +17,7 @@ KDA_OK, KDA_EINVAL, KDA_EDTYPE, KDA_ESHAPE, KDA_EALIGN = 0, -1, -2, -3, -4
 KDA_EPROTO, KDA_ECUDA, KDA_EDEVICE, KDA_ENOSPC = -5, -6, -7, -8
 KDA_DERR_SLOT, KDA_DERR_ACCEPT, KDA_DERR_DEPTH = 1, 2, 4
 KDA_DERR_SEGMENT, KDA_DERR_RING, KDA_DERR_RANGE = 8, 16, 32
-KDA_DERR_TIMEOUT = 64
+KDA_DERR_TIMEOUT, KDA_DERR_UNSAFE = 64, 128
 KDA_F32, KDA_BF16 = 0, 1
 
 _P = ctypes.c_void_p
@@ -46,7 +46,7 @@ EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_raw", "kda_prefill_chunke
            "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
            "kda_gather_states", "kda_copy_slots", "kda_verify_snapshot",
            "kda_commit_snapshot", "kda_forward_mixed", "kda_get_device_error",
-           "kda_status_string", "kda_version")
+           "kda_set_wait_limit", "kda_status_string", "kda_version")
 
 _lib = None
 
@@ -81,6 +81,7 @@ def lib():
                                         _P, _P, ctypes.c_size_t, _I32, rp, _P, _P, _P]
         L.kda_commit_snapshot.argtypes = [_P, _P, _I32, pp, _P, _I32, _P]
         L.kda_get_device_error.argtypes = [ctypes.POINTER(_I32), _P]
+        L.kda_set_wait_limit.argtypes = [_I32]
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_version.restype = ctypes.c_int
@@ -322,3 +323,9 @@ def kda_get_device_error(stream=None):
     if st not in (KDA_OK, KDA_EDEVICE):
         raise KdaError(st, "kda_get_device_error")
     return int(bits.value)
+
+
+def kda_set_wait_limit(polls):
+    """Testing hook: bounded device waits give up after `polls` polls
+    (KDA_DERR_TIMEOUT); a negative value restores the default."""
+    _check(lib().kda_set_wait_limit(int(polls)), "kda_set_wait_limit")
