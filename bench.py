@@ -14,10 +14,12 @@ public API calls, with a timing event pair around its NL verify launches
 (the verify launch duration is that block's time / NL).
 
 Extra keys: `roofline` (verify kernel vs HBM), `cpu_baseline` (the fp64
-oracle on the host cores, bounded sample), `e2e` (same metric with every
-step's inputs copied from pinned host memory and its outputs copied back
-inside the timed region, the copies of neighbouring steps overlapping the
-compute on their own streams), `prefill` (chunked prefill with in-pass checkpoints,
+oracle on the host cores, bounded sample), `e2e` (same metric through the
+public calls issued eagerly every step -- kda_verify per layer and
+kda_commit_layers through the binding -- with every step's inputs copied from
+pinned host memory and its outputs copied back inside the timed region, the
+copies of neighbouring steps overlapping the compute on their own streams),
+`e2e_graph` (the same loop replaying CUDA graphs captured from those calls), `prefill` (chunked prefill with in-pass checkpoints,
 1 x 8192 tokens, chunk 64, checkpoint every 1024, own timed region: the
 two-pass path through the workspace, and the single pass beside it),
 `clocks` (nvidia-smi samples during the timed region),
@@ -82,6 +84,20 @@ def unit_bytes(a_prev, d=D, t=T):
     ring_tok = 3 * d * 2 + 2
     return (d * d * 4 + d * d * 4 * (a_prev > 0) + t * (4 * d * 2 + 2)
             + t * d * 4 + t * ring_tok + a_prev * ring_tok + 8)
+
+
+def load_tensor_peak():
+    """Measured dense bf16 tensor peak (burst) in TFLOP/s, and its source."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                pk = json.load(f)
+            if pk.get("bf16_tflops"):
+                return float(pk["bf16_tflops"]), "measured"
+        except Exception:
+            pass
+    return 1900.0, "fallback"
 
 
 def load_peaks():
@@ -380,8 +396,30 @@ def run_prefill(torch, K, dev):
     alg_bytes = (L * H * (4 * D * 2 + 2) + L * H * D * 4
                  + (2 + L // E) * H * D * D * 4)
     flops = 11.6e6 * (L // C) * H
+    # every tensor-core product of a non-input operand is taken as three bf16
+    # products (hi*hi, lo*hi, hi*lo): the MMAs issue about 3x the chunk form
+    issued = 3.0 * flops
+    hbm_peak, hbm_kind = load_peaks()
+    tc_peak, tc_kind = load_tensor_peak()
+    prof = prefill_tensor_profile()
+    achieved_gbs = alg_bytes / (ms * 1e-3) / 1e9
+    roofline = {
+        "bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+        "frac": achieved_gbs / hbm_peak, "peak_source": hbm_kind,
+        "traffic": prof.get("dram_bytes_per_call") if prof else None,
+        "alg_bytes": alg_bytes,
+        "tensor": {"chunk_tflops": flops / (ms * 1e-3) / 1e12,
+                   "issued_tflops": issued / (ms * 1e-3) / 1e12,
+                   "peak_tflops": tc_peak, "peak_source": tc_kind,
+                   "frac_chunk": flops / (ms * 1e-3) / 1e12 / tc_peak,
+                   "frac_issued": issued / (ms * 1e-3) / 1e12 / tc_peak,
+                   "pipe_active_pct": prof.get("sm__pipe_tensor_cycles_active_pct")
+                   if prof else None,
+                   "chunk_flops": flops, "issued_flops": issued},
+    }
     return {
         "workload": w.name, "tokens_per_s": L / (ms * 1e-3), "ms": ms,
+        "roofline": roofline,
         "launches_per_call": 3, "reps": reps, "algorithmic_bytes": alg_bytes,
         "achieved_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "chunk_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
@@ -389,17 +427,9 @@ def run_prefill(torch, K, dev):
         "single_pass_ms": ms_single,
         "single_pass_tokens_per_s": L / (ms_single * 1e-3),
         "raw_inputs_fused_prep_ms": ms_raw,
-        "raw_inputs_note": "kda_prefill_chunked_raw (two passes): raw keys, decay "
-                           "and beta logits, prep fused into the kernels; a "
-                           "separate prep pass would move %d bytes" % prep_bytes,
-        "note": "two tcgen05 passes through the workspace: every (chunk, head) "
-                "computes its state-independent operands at once (tile images, "
-                "U', decay vectors), then one CTA per (32-column value slice, "
-                "head, sequence) walks the chunks (R3, R4, state, outputs, "
-                "checkpoints); bf16 hi/lo operands (three kind::f16 MMAs per "
-                "product), fp32 state in registers.  single_pass: the fused "
-                "kernel used when no workspace is given",
-        "tensor_pipe": prefill_tensor_profile(),
+        "raw_prep_pass_bytes_avoided": prep_bytes,
+        "tensor_pipe": prof,
+        "note": "two tcgen05 passes through the workspace; single_pass: no workspace",
     }
 
 
@@ -1007,6 +1037,39 @@ def run_kda(args, rank, world, local_rank):
     e2e_launch_us = float(np.mean([events[s][0].elapsed_time(events[s][1]) / NL
                                    for s in range(args.warmup, total_steps)])) * 1e3
 
+    # The same end-to-end loop through the public calls themselves: every step
+    # issues kda_verify for each layer and kda_commit_layers eagerly through
+    # the binding (argument marshalling, host validation and the launch on
+    # every call), with the same pipelined host copies.
+    ev_in, ev_cmp, ev_out = {}, {}, {}
+    barrier()
+    torch.cuda.synchronize()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    aw0 = time.time()
+    a0.record(h2d_s)
+    issue_h2d(first)
+    for s in range(first, total_steps):
+        if s + 1 < total_steps:
+            issue_h2d(s + 1)
+        stream.wait_event(ev_in[s])
+        if s - G >= first:
+            stream.wait_event(ev_out[s - G])
+        for l in range(NL):
+            K.kda_verify(batches[s % G][l], T, pools[l], slots, rings[l], stream=stream)
+        K.kda_commit_layers(acc[s % A], slots, pools[0], rings, stream=stream)
+        ev_cmp[s] = torch.cuda.Event()
+        ev_cmp[s].record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(ev_cmp[s])
+            host_out.copy_(outs[s % G], non_blocking=True)
+            ev_out[s] = torch.cuda.Event()
+            ev_out[s].record(d2h_s)
+    a1.record(d2h_s)
+    torch.cuda.synchronize()
+    aw1 = time.time()
+    ms_api = max_over_ranks(a0.elapsed_time(a1), dist, dev)
+
     prefill = run_prefill(torch, K, dev)
     mixed = run_mixed(torch, K, dev)
     direct = run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np,
@@ -1057,10 +1120,16 @@ def run_kda(args, rank, world, local_rank):
                                       "%d back-to-back verify launches, / %d" % (NL, NL),
                      "alg_bytes_per_launch": float(np.mean(abytes))},
         "cpu_baseline": cpu,
-        "e2e": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
+        "e2e": {"value": job_rate(tokens_rank, world, ms_api), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": ms_e2e / args.steps,
-                "verify_launch_us_during_copies": e2e_launch_us},
+                "ms_per_step": ms_api / args.steps,
+                "host_wall_ms_per_step": (aw1 - aw0) * 1e3 / args.steps,
+                "calls": "eager kda_verify x %d + kda_commit_layers per step "
+                         "through the binding, host copies in the timed region" % NL},
+        "e2e_graph": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
+                      "ms_per_step": ms_e2e / args.steps,
+                      "verify_launch_us_during_copies": e2e_launch_us,
+                      "calls": "the same steps replayed as CUDA graphs captured from the calls"},
         "gpu_launches": (NL + 1) * args.steps,
         "clocks": clocks.summary(w0, w1),
         "device_error_bits": bits,

@@ -282,6 +282,9 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
  * With side_stream non-NULL (and not `stream`) the prefill part runs on
  * side_stream, forked from `stream` and joined back by events, beside the
  * verify part on `stream`; the call returns with `stream` ordered after both.
+ * The two events are made once per host thread and device and reused by
+ * every call (a stream capture of the call records their waits as graph
+ * edges, as with any event).
  */
 int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefill_tokens,
                       kda_state_pool *pool, const int32_t *state_slots,

@@ -40,6 +40,26 @@ bool device_unsafe() {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// The fork and join events of kda_forward_mixed on the current device, made
+// once per host thread and device and reused by every call (a wait enqueued
+// on an event takes the event's state at that moment, so re-recording it for
+// the next call is safe).  nullptr if they could not be made.
+cudaEvent_t *fork_events() {
+  thread_local cudaEvent_t ev[64][2] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ev[dev][0]) {
+    if (cudaEventCreateWithFlags(&ev[dev][0], cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    if (cudaEventCreateWithFlags(&ev[dev][1], cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(ev[dev][0]);
+      ev[dev][0] = nullptr;
+      return nullptr;
+    }
+  }
+  return ev[dev];
+}
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ECUDA; }
 
@@ -318,16 +338,12 @@ int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefil
                     tv.num_seqs > 0;
   cudaStream_t main_s = reinterpret_cast<cudaStream_t>(stream);
   cudaStream_t side_s = reinterpret_cast<cudaStream_t>(side_stream);
-  cudaEvent_t ev[2] = {nullptr, nullptr};
+  cudaEvent_t *ev = nullptr;
   if (fork) {
-    if (cudaEventCreateWithFlags(&ev[0], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ev[1], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventRecord(ev[0], main_s) != cudaSuccess ||
-        cudaStreamWaitEvent(side_s, ev[0], 0) != cudaSuccess) {
-      for (cudaEvent_t e : ev)
-        if (e) cudaEventDestroy(e);
+    ev = fork_events();
+    if (!ev || cudaEventRecord(ev[0], main_s) != cudaSuccess ||
+        cudaStreamWaitEvent(side_s, ev[0], 0) != cudaSuccess)
       return KDA_ECUDA;
-    }
   }
   bool join = false;
   if (num_prefill > 0) {
@@ -346,8 +362,6 @@ int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefil
     // the caller's stream waits for whatever the side stream took (the join)
     if (join && cudaStreamWaitEvent(main_s, ev[1], 0) != cudaSuccess && st == KDA_OK)
       st = KDA_ECUDA;
-    cudaEventDestroy(ev[0]);
-    cudaEventDestroy(ev[1]);
   }
   return st;
 }
