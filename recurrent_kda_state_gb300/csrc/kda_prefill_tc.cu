@@ -793,16 +793,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // inside the sequential chunk chain, and repeats it in each value slice.
 // With a workspace that work runs once per (chunk, head), for all chunks at
 // once, and the chain keeps R3, R4 and the state update:
-//   pass 1, prefill_tc_chunk_kernel: one CTA per (chunk, head): E1, R1, the
-//     inverse and R2 as above with R2 over all 128 value columns, then the
-//     chunk's workspace entry: the [W~; Q~], K^^T and [T; M] tiles as the
-//     shared-memory images the MMAs read (bf16 hi/lo, 128B-swizzled, 1024-byte
-//     aligned, so a bulk copy restores the swizzle), U' as fp32 in four
-//     32-column slices, and e^{g_m}, e^{g_C}, e^{g_C - g_m};
+//   pass 1, prefill_tc_chunk_kernel: two persistent CTAs per SM walk the
+//     (chunk, head) items: E1, R1, the inverse and R2 as above with R2 over
+//     all 128 value columns, and the chunk's workspace entry: the [W~; Q~],
+//     K^^T and [T; M] tiles as the shared-memory images the MMAs read (bf16
+//     hi/lo, 128B-swizzled, 1024-byte aligned, so a bulk copy restores the
+//     swizzle), U' as fp32 in four 32-column slices, and e^{g_m}, e^{g_C},
+//     e^{g_C - g_m}.  Each part of the entry is stored from registers as soon
+//     as it is computed, so a CTA keeps only the operands of its own MMAs in
+//     shared memory (about 100 KB) and two items share an SM: one's CUDA-core
+//     phases run while the other waits on its MMAs or its loads;
 //   pass 2, prefill_tc_pass_kernel: one CTA per (value slice, head, sequence)
 //     walks the chunks: S~ tile, R3, U = U' - W S, R4, outputs, state,
 //     checkpoints, while the bulk-copy engine brings the next chunk's entry in
-//     as soon as each of its buffers is free.
+//     as soon as each of its buffers is free.  It is a programmatic dependent
+//     of pass 1, so its launch and initial state load overlap pass 1's last
+//     items.
 
 struct Entry {                                 // byte offsets in an entry
   static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
@@ -814,29 +820,46 @@ struct Entry {                                 // byte offsets in an entry
 };
 static_assert(Entry::END <= kTcEntryBytes && kTcEntryBytes % 1024 == 0, "entry");
 
-struct LayP {                                  // pass 1
-  static constexpr uint32_t GA_HI = 0, GA_LO = 32768;       // [K~; Q~] -> [W~; Q~]
-  static constexpr uint32_t GB_HI = 65536, GB_LO = 81920;   // K^ (R1 B; exported)
-  static constexpr uint32_t TM_HI = 98304, TM_LO = 114688;  // [T; M] (exported)
-  static constexpr uint32_t VT = 131072;       // V, MN-major (TMA, 128B swizzle)
-  static constexpr uint32_t AF = 147456, XF = AF + 64 * 68 * 4;  // after R1
-  static constexpr uint32_t MISC = XF + 64 * 68 * 4;
+struct LayP {                                  // pass 1 (two CTAs per SM)
+  // [K~; Q~] hi | lo: R1's A; its K~ rows are R2's MN-major B.  128 rows, two
+  // 64-channel atoms of 16 KB per split (rows 64..127 of an atom: Q~).
+  static constexpr uint32_t GA_HI = 0, GA_LO = 32768;
+  static constexpr uint32_t GB_HI = 65536, GB_LO = 81920;   // K^ (R1's B), 64 rows
+  // E1 writes the Q~ rows and K^ to the entry from registers, so once R1 has
+  // read them their space is free:
+  //   V: two 64-channel atoms (TMA, MN-major) in the Q~ hi rows, 16 KB apart;
+  //   the inverse's scratch, then T hi (rows 0..63 of R2's A; the A
+  //   descriptor's rows 64..127 read whatever follows and land in accumulator
+  //   rows nobody reads) in the Q~ lo rows of atom 0;
+  //   the inverse's fp32 A and X over the Q~ lo rows of atom 1 and K^, then
+  //   T lo over the start of A.
+  static constexpr uint32_t V0 = 8192;
+  static constexpr uint32_t PT = 40960, T_HI = 40960, T_LO = 57344;
+  // Once R2 has read its operands nothing of the item is left in shared
+  // memory: the next item's raw q, k, alpha rows land over [K~; Q~] (and
+  // its beta box in MISC) while this item's epilogue runs.  E1 reads them
+  // into registers before its first barrier and writes tiles only after it.
+  static constexpr uint32_t STG_Q = 0, STG_K = 16384, STG_A = 32768;
+  static constexpr uint32_t AF = 57344, XF = AF + 64 * 68 * 4;
+  static constexpr uint32_t MISC = 98304;
   static constexpr uint32_t BET = MISC, GM = BET + 256, GC = GM + 512;
   static constexpr uint32_t EGC = GC + 512, ECM = EGC + 512, EGM = ECM + 512;
-  static constexpr uint32_t PT = EGM + 512, TOT4 = PT + 3072, BST = TOT4 + 2048;
-  static constexpr uint32_t MBAR = BST + 1024, SBAR = MBAR + 8, TSLOT = SBAR + 8;
-  static constexpr uint32_t STG_A = (TSLOT + 8 + 1023) & ~1023u;
-  static constexpr uint32_t END = STG_A + 16384;
+  static constexpr uint32_t TOT4 = EGM + 512, NSCR = TOT4 + 2048, BST = NSCR + 768;
+  static constexpr uint32_t MBAR = BST + 1024, VBAR = MBAR + 8, SBAR = VBAR + 8;
+  static constexpr uint32_t TSLOT = SBAR + 8;
+  static constexpr uint32_t END = TSLOT + 8;
   static constexpr size_t kBytes = END + 1024;
-  // raw q, k rows of the next item in the A and X arrays (free from the end of
-  // R2), alpha in its own area, V straight into VT; all consumed (or, for V,
-  // read by R2) before anything is written over them
-  static constexpr uint32_t STG_Q = AF, STG_K = AF + 16384;
 };
-static_assert(LayP::GB_HI + 65536 == LayP::VT && LayP::VT % 1024 == 0,
-              "K^ and [T; M] contiguous (one export); V tile aligned");
-static_assert(LayP::STG_K + 16384 <= LayP::MISC, "q, k staging in A and X");
-static_assert(LayP::kBytes <= 232448, "pass-1 shared memory");
+static_assert(LayP::V0 % 1024 == 0 && LayP::V0 + 16384 + 8192 <= LayP::GA_LO,
+              "V atoms inside the Q~ hi rows");
+static_assert(LayP::PT + 3 * 1024 <= LayP::T_HI + 8192 && LayP::T_HI + 8192 <= LayP::GA_LO + 16384,
+              "scratch and T hi inside the Q~ lo rows of atom 0");
+static_assert(LayP::AF == LayP::GA_LO + 16384 + 8192 && LayP::XF + 64 * 68 * 4 <= LayP::MISC,
+              "A and X over the Q~ lo rows of atom 1 and K^");
+static_assert(LayP::T_LO + 8192 <= LayP::XF, "T lo over A only");
+static_assert(LayP::STG_A + 16384 <= LayP::GB_HI && LayP::BST % 128 == 0, "staging");
+static_assert(2 * (LayP::kBytes + 1024) <= 233472, "two CTAs per SM");
+
 
 struct LayS {                                  // pass 2
   static constexpr uint32_t GA = 0;            // [W~; Q~] hi, lo
@@ -855,8 +878,36 @@ struct LayS {                                  // pass 2
 static_assert(LayS::SB % 1024 == 0 && LayS::UT % 1024 == 0, "pass-2 tiles");
 static_assert(LayS::kBytes <= 232448, "pass-2 shared memory");
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (a no-op without the launch
+// attribute); let the next grid on the stream start its prologue.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Hint: bring the box of `tm` at (x, head, tok) into L2; nothing lands in
+// shared memory.
+__device__ __forceinline__ void tma_prefetch3(const CUtensorMap *tm, int x, int head, int tok) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               :: "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(head), "r"(tok)
+               : "memory");
+}
+
+// Eight fp32 values -> one 16-byte chunk of a hi and of a lo tile image in
+// global memory.
+__device__ __forceinline__ void put8_global(uint8_t *hi, uint8_t *lo, const float *x) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) umma::split_bf16x2(x[2 * i], x[2 * i + 1], h[i], l[i]);
+  *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4 *>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 template <bool RAW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     prefill_tc_chunk_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
   extern __shared__ float4 smem4[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -872,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *Af = reinterpret_cast<float *>(sm + LayP::AF);
   float *Xf = reinterpret_cast<float *>(sm + LayP::XF);
   uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + LayP::MBAR);
+  uint64_t *vbar_p = reinterpret_cast<uint64_t *>(sm + LayP::VBAR);
   uint64_t *sbar_p = reinterpret_cast<uint64_t *>(sm + LayP::SBAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + LayP::TSLOT);
 
@@ -883,9 +935,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it = blockIdx.x;
   if (it >= total) return;
 
-  if (tid < 32) umma::tmem_alloc(tslot, 512);
+  if (tid < 32) umma::tmem_alloc(tslot, 256);
   if (tid == 0) {
     umma::mbar_init(mbar, 1);
+    umma::mbar_init(vbar_p, 1);
     umma::mbar_init(sbar_p, 1);
   }
   umma::fence_before_sync();
@@ -893,32 +946,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *tslot;
   const uint32_t tl = tmem + ((uint32_t)(tid & 96) << 16);
-  uint32_t phase = 0, sphase = 0;
+  uint32_t phase = 0, vphase = 0, sphase = 0;
+  // every CTA of this grid is resident from the start (two per SM, one
+  // wave), so pass 2 may be scheduled now: its CTAs take SMs as this grid's
+  // CTAs exit, and wait for its completion before reading the entries
+  grid_dep_launch();
   const uint64_t dGA = umma::sdesc_sw128(sb);
-  // TMA loads of item j's raw rows into the staging areas
+  uint8_t *const ent0 = p.ws + prefill_tc_entries_offset(p.B);
+  // TMA loads of item j's raw q, k, alpha rows and beta box into staging
   auto stage = [&](int j) {
     if (tid == 0) {
       const int gj = j / H, hj = j - (j / H) * H;
-      const int t0 = locate_chunk(p, gj, kC).tok0;
-      const uint32_t sbar = sb + LayP::SBAR;
-      mbar_expect_tx(sbar, 4 * 64 * 2 * kD + 64 * 16);
-      tma_load3(sb + LayP::STG_Q, &maps.q, 0, hj, t0, sbar);
-      tma_load3(sb + LayP::STG_K, &maps.k, 0, hj, t0, sbar);
-      tma_load3(sb + LayP::STG_A, &maps.a, 0, hj, t0, sbar);
-      tma_load3(sb + LayP::VT, &maps.v, 0, hj, t0, sbar);  // two 64-channel atoms
-      tma_load3(sb + LayP::VT + 8192, &maps.v, 64, hj, t0, sbar);
-      tma_load2(sb + LayP::BST, &maps.b, hj & ~7, t0, sbar);
+      const int tj = locate_chunk(p, gj, kC).tok0;
+      const uint32_t bar = sb + LayP::SBAR;
+      mbar_expect_tx(bar, 3 * 64 * 2 * kD + 64 * 16);
+      tma_load3(sb + LayP::STG_Q, &maps.q, 0, hj, tj, bar);
+      tma_load3(sb + LayP::STG_K, &maps.k, 0, hj, tj, bar);
+      tma_load3(sb + LayP::STG_A, &maps.a, 0, hj, tj, bar);
+      tma_load2(sb + LayP::BST, &maps.b, hj & ~7, tj, bar);
     }
   };
   stage(it);
-  bool ok = true, stage_owed = true, mma_owed = false;  // what is in flight
+  bool ok = true, stage_owed = true, v_owed = false, mma_owed = false;  // in flight
   for (; it < total; it += gridDim.x) {
     const int g = it / H, h = it - (it / H) * H;
     const ChunkLoc cl = locate_chunk(p, g, kC);
-    const int n = cl.n, m = n >> 1;
+    const int n = cl.n, m = n >> 1, t0 = cl.tok0;
+    uint8_t *ent = ent0 + ((size_t)g * H + h) * kTcEntryBytes;
     if (!(ok = tc_wait(sbar_p, sphase, p.spin_limit))) break;
     stage_owed = false;
-    // ---- E1 (as in the fused kernel; V^T over all 128 value columns)
+    if (tid == 0 && it + (int)gridDim.x < total) {  // the next item's rows into L2
+      const int j = it + gridDim.x, gj = j / H, hj = j - (j / H) * H;
+      const int tj = locate_chunk(p, gj, kC).tok0;
+      tma_prefetch3(&maps.q, 0, hj, tj);
+      tma_prefetch3(&maps.k, 0, hj, tj);
+      tma_prefetch3(&maps.a, 0, hj, tj);
+      tma_prefetch3(&maps.v, 0, hj, tj);
+      tma_prefetch3(&maps.v, 64, hj, tj);
+    }
+    // ---- E1: each thread (channel pair cp, token quarter tq) reads its 16
+    // tokens' q, k, alpha words from the staging area
     if (tid < kC) {
       const uint16_t bw = reinterpret_cast<const uint16_t *>(sm + LayP::BST)[tid * 8 + (h & 7)];
       const float bv = __uint_as_float((uint32_t)bw << 16);
@@ -942,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         la1[u] = t < n ? (RAW ? neg_softplus(a1) : __logf(a1)) : 0.f;
       }
     }
-    float *nscr = reinterpret_cast<float *>(sm + LayP::PT);   // key norms (raw inputs)
+    float *nscr = reinterpret_cast<float *>(sm + LayP::NSCR);   // key norms (raw inputs)
     float *nrm = nscr + 128;
     if (RAW) norm_partials(kr, nscr, tid);
 #pragma unroll
@@ -952,8 +1019,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tot4[tq * 128 + c2] = la0[15];
     tot4[tq * 128 + c2 + 1] = la1[15];
-    if (tid == 0) umma::bulk_wait_read();  // the last item's export has read its tiles
-    __syncthreads();  // staging consumed; quarter sums visible; tiles writable
+    __syncthreads();  // quarter sums visible; staging read (tiles writable)
     {
       float add0 = 0.f, add1 = 0.f;
       for (int w = 0; w < tq; ++w) {
@@ -1002,7 +1068,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
         // K~ and Q~ rows of [K~; Q~] and the K^ rows: K-major for R1, and the
         // same bytes serve R2 (K~) and the chunk walk's R4 (K^) as MN-major
-        // operands, so no transposed copy is written
+        // operands, so no transposed copy is written.  The Q~ and K^ rows
+        // also go to the entry now (a warp writes one 128-byte row).
         uint32_t hi, lo;
         uint32_t off = umma::sw128_off16(t, c2, 128);
         umma::split_bf16x2(f0 * k0, f1 * k1, hi, lo);
@@ -1012,10 +1079,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::split_bf16x2(f0 * q0, f1 * q1, hi, lo);
         *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = hi;
         *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = lo;
+        *reinterpret_cast<uint32_t *>(ent + Entry::GA + off) = hi;
+        *reinterpret_cast<uint32_t *>(ent + Entry::GA + 32768 + off) = lo;
         off = umma::sw128_off16(t, c2, 64);
         umma::split_bf16x2(fi0 * k0, fi1 * k1, hi, lo);
         *reinterpret_cast<uint32_t *>(sm + LayP::GB_HI + off) = hi;
         *reinterpret_cast<uint32_t *>(sm + LayP::GB_LO + off) = lo;
+        *reinterpret_cast<uint32_t *>(ent + Entry::KT + off) = hi;
+        *reinterpret_cast<uint32_t *>(ent + Entry::KT + 16384 + off) = lo;
       }
     }
     tiles_ready();
@@ -1036,7 +1107,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_owed = true;
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
-    {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> tile
+    // R1 has read the Q~ rows and K^: V lands in the Q~ hi rows while the
+    // inverse runs
+    if (tid == 0) {
+      const uint32_t vb = sb + LayP::VBAR;
+      mbar_expect_tx(vb, 2 * 64 * 128);
+      tma_load3(sb + LayP::V0, &maps.v, 0, h, t0, vb);
+      tma_load3(sb + LayP::V0 + 16384, &maps.v, 64, h, t0, vb);
+    }
+    v_owed = true;
+    {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> entry
       float gv[32];
       {
         float g0[16], g1[16];
@@ -1069,14 +1149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = s + e <= t ? gv[8 * ch + e] : 0.f;
-          put8(sm, LayP::TM_HI + umma::sw128_off16(64 + t, s, 128),
-               LayP::TM_LO + umma::sw128_off16(64 + t, s, 128), x);
+          const uint32_t off = umma::sw128_off16(64 + t, s, 128);
+          put8_global(ent + Entry::KT + 32768 + off, ent + Entry::KT + 49152 + off, x);
         }
       }
     }
     __syncthreads();
     unit_lower_inverse(Af, Xf, reinterpret_cast<float *>(sm + LayP::PT), tid);
-    {  // T = X diag(beta) -> rows 0..63 of the [T; M] tile
+    {  // T = X diag(beta) -> rows 0..63 of R2's A tile and of the entry's [T; M]
       const int t = tid >> 2, s0 = (tid & 3) * 16;
       float x[16];
 #pragma unroll
@@ -1084,32 +1164,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = s0 + e;
         x[e] = s <= t ? Xf[fo(t, s)] * bet[s] : 0.f;
       }
-      put8(sm, LayP::TM_HI + umma::sw128_off16(t, s0, 128),
-           LayP::TM_LO + umma::sw128_off16(t, s0, 128), x);
-      put8(sm, LayP::TM_HI + umma::sw128_off16(t, s0 + 8, 128),
-           LayP::TM_LO + umma::sw128_off16(t, s0 + 8, 128), x + 8);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t off = umma::sw128_off16(t, s0 + 8 * hh, 128);
+        put8(sm, LayP::T_HI + off, LayP::T_LO + off, x + 8 * hh);
+        put8_global(ent + Entry::KT + 32768 + off, ent + Entry::KT + 49152 + off, x + 8 * hh);
+      }
     }
     tiles_ready();
+    if (!(ok = tc_wait(vbar_p, vphase, p.spin_limit))) break;
+    v_owed = false;
 
-    // ---- R2: [T; M] K~ -> rows 0..63: W~ (cols 0..127);  [T; M] V -> U'
-    // (cols 128..255).  K~ (rows 0..63 of [K~; Q~], 64-key atoms 16 KB apart)
-    // and V (two 64-channel atoms) are MN-major B operands.
+    // ---- R2: T K~ -> W~ (accumulator columns 0..127);  T V -> U' (128..255).
+    // K~ (rows 0..63 of [K~; Q~], 64-key atoms 16 KB apart) and V (two
+    // 64-channel atoms 16 KB apart) are MN-major B operands.
     if (tid == 0) {
       const uint32_t id = umma::idesc_bf16_bmn(128, 128);
       const uint64_t dKh = umma::sdesc_sw128_mn(sb + LayP::GA_HI, 16384);
       const uint64_t dKl = umma::sdesc_sw128_mn(sb + LayP::GA_LO, 16384);
-      const uint64_t dV = umma::sdesc_sw128_mn(sb + LayP::VT, 8192);
+      const uint64_t dV = umma::sdesc_sw128_mn(sb + LayP::V0, 16384);
       for (int ps = 0; ps < 3; ++ps) {
-        const uint32_t a = ps == 1 ? LayP::TM_LO : LayP::TM_HI;
+        const uint32_t a = ps == 1 ? LayP::T_LO : LayP::T_HI;
         const uint64_t b = ps == 2 ? dKl : dKh;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc2, dadd(dGA, a + kk * 32), dadd(b, kk * 2048), id,
+          umma::mma_bf16(tmem, dadd(dGA, a + kk * 32), dadd(b, kk * 2048), id,
                          (uint32_t)(ps | kk));
       }
       for (int ps = 0; ps < 2; ++ps) {  // V is an exact bf16 input: two passes
-        const uint32_t a = ps ? LayP::TM_LO : LayP::TM_HI;
+        const uint32_t a = ps ? LayP::T_LO : LayP::T_HI;
         for (int kk = 0; kk < 4; ++kk)
-          umma::mma_bf16(tmem + kAcc2 + 128, dadd(dGA, a + kk * 32), dadd(dV, kk * 2048), id,
+          umma::mma_bf16(tmem + 128, dadd(dGA, a + kk * 32), dadd(dV, kk * 2048), id,
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
@@ -1117,51 +1201,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_owed = true;
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
-    // R2 has read its operands: the next item's rows can land in the staging
-    // areas while this item's epilogue and export run
+    // R2 has read every tile: the next item's rows land during the epilogue
     if (it + (int)gridDim.x < total) {
       stage(it + gridDim.x);
       stage_owed = true;
     }
-    uint8_t *ent = p.ws + prefill_tc_entries_offset(p.B) + ((size_t)g * H + h) * kTcEntryBytes;
-    if (c < 64) {  // W~ row t -> rows 0..63 of the [W~; Q~] tile; U' row t -> entry
+    if (c < 64) {  // W~ row t -> rows 0..63 of the entry's [W~; Q~]; U' row t -> entry
       const int t = c;
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
         float w[16];
         const int k0 = 64 * hf + 16 * blk;
-        umma::tmem_ld16(tl + kAcc2 + k0, w);
-        put8(sm, LayP::GA_HI + umma::sw128_off16(t, k0, 128),
-             LayP::GA_LO + umma::sw128_off16(t, k0, 128), w);
-        put8(sm, LayP::GA_HI + umma::sw128_off16(t, k0 + 8, 128),
-             LayP::GA_LO + umma::sw128_off16(t, k0 + 8, 128), w + 8);
+        umma::tmem_ld16(tl + k0, w);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t off = umma::sw128_off16(t, k0 + 8 * hh, 128);
+          put8_global(ent + Entry::GA + off, ent + Entry::GA + 32768 + off, w + 8 * hh);
+        }
       }
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
         float u[16];
         const int j0 = 64 * hf + 16 * blk;
-        umma::tmem_ld16(tl + kAcc2 + 128 + j0, u);
+        umma::tmem_ld16(tl + 128 + j0, u);
         float4 *row = reinterpret_cast<float4 *>(ent + Entry::UP) + ((j0 >> 5) * 64 + t) * 8;
 #pragma unroll
         for (int e = 0; e < 4; ++e)  // chunk (j mod 32) / 4 at position (chunk + t) mod 8
           row[((((j0 & 31) >> 2) + e) + t) & 7] =
               make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
       }
-    }
-    tiles_ready();
-    if (tid == 0) {  // the tile images, by the bulk-copy engine
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        umma::bulk_s2g(ent + Entry::GA + 16384 * k, sb + LayP::GA_HI + 16384 * k, 16384);
-        umma::bulk_s2g(ent + Entry::KT + 16384 * k, sb + LayP::GB_HI + 16384 * k, 16384);
-      }
-      umma::bulk_commit();
-    }
-    if (tid < 128) {
+    } else {
+      const int j = (c - 64) + 64 * hf;  // 0..127 over the threads of lanes 64..127
       float *vec = reinterpret_cast<float *>(ent + Entry::VEC);
-      vec[tid] = egmv[tid];
-      vec[128 + tid] = egc[tid];
-      vec[256 + tid] = ecm[tid];
+      vec[j] = egmv[j];
+      vec[128 + j] = egc[j];
+      vec[256 + j] = ecm[j];
     }
   }
   if (!ok && tid == 0) {
@@ -1169,13 +1243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one more bounded chance for what is still in flight
     if ((mma_owed) && !umma::mbar_wait(mbar, phase, kDrainWaitPolls))
       set_error(p.err, KDA_DERR_UNSAFE);
+    if ((v_owed) && !umma::mbar_wait(vbar_p, vphase, kDrainWaitPolls))
+      set_error(p.err, KDA_DERR_UNSAFE);
     if ((stage_owed) && !umma::mbar_wait(sbar_p, sphase, kDrainWaitPolls))
       set_error(p.err, KDA_DERR_UNSAFE);
   }
-  if (tid == 0) umma::bulk_wait_read();  // shared memory stays until read
   umma::fence_before_sync();
   __syncthreads();
-  if (tid < 32) umma::tmem_dealloc(tmem, 512);
+  if (tid < 32) umma::tmem_dealloc(tmem, 256);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const PrefillParams p) {
@@ -1191,18 +1266,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
   const int tid = threadIdx.x, sl = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
   const int H = p.H, col0 = sl * kNC;
   const int c = tid & 127, hf = tid >> 7;
+  // Launched as a programmatic dependent of pass 1: until grid_dep_wait()
+  // returns, only what was written before pass 1 started (the chunk table,
+  // the segment arrays, the pool) is read.  Every CTA waits before it exits,
+  // so this grid completes after pass 1 whatever path it takes.
   const int cu0 = p.cu_seqlens[i], cu1 = p.cu_seqlens[i + 1];
   const int L = cu1 - cu0;
   const int p0 = p.start_pos ? p.start_pos[i] : 0;
-  if (cu0 < 0 || L < 0 || cu1 > p.N || p0 < 0 || L == 0) return;  // flagged by the table
+  if (cu0 < 0 || L < 0 || cu1 > p.N || p0 < 0 || L == 0) {  // flagged by the table
+    grid_dep_wait();
+    return;
+  }
   const int slot = p.state_slots[i];
   if (slot < 0 || slot >= p.P) {
     if (tid == 0 && sl == 0) set_error(p.err, KDA_DERR_SLOT);
+    grid_dep_wait();
     return;
   }
   const int *table = reinterpret_cast<const int *>(p.ws);
   const int g0 = table[i], nch = table[i + 1] - table[i];
-  if (nch <= 0) return;
+  if (nch <= 0) {
+    grid_dep_wait();
+    return;
+  }
 
   if (tid < 32) umma::tmem_alloc(tslot, 128);
   if (tid == 0) {
@@ -1249,9 +1335,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     }
     owe2 = true;
   };
-  issue_g1(0);
-  issue_g2(0);
-
   float S[16];
   {
     const float *src = p.pool + ((size_t)slot * H + h) * kD * kD;
@@ -1259,6 +1342,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     for (int jj = 0; jj < 16; ++jj)
       S[jj] = src[(size_t)(col0 + 16 * hf + jj) * kD + c];
   }
+  grid_dep_wait();  // pass 1's entries are complete and visible
+  issue_g1(0);
+  issue_g2(0);
   const int r0 = p0 % kC;
   bool ok = true;
   for (int q = 0; q < nch; ++q) {
@@ -1488,6 +1574,10 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   auto kp1 = p.raw ? prefill_tc_chunk_kernel<true> : prefill_tc_chunk_kernel<false>;
   e = cudaFuncSetAttribute(kp1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayP::kBytes);
+  // all of the unified L1 / shared-memory array as shared memory: room for
+  // two CTAs per SM
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kp1, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(prefill_tc_pass_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LayS::kBytes);
@@ -1496,14 +1586,25 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s) {
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // one CTA per SM walks the (chunk, head) items (the last ones exit at once)
+  // two CTAs per SM walk the (chunk, head) items (the last ones exit at once)
   const long long items = (long long)p.max_chunks * p.H;
-  const int grid1 = (int)(items < sms ? items : sms);
+  const int grid1 = (int)(items < 2LL * sms ? items : 2LL * sms);
   kp1<<<grid1, kThreads, LayP::kBytes, s>>>(p, maps);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_tc_pass_kernel<<<dim3(kD / kNC, p.H, p.B), kThreads, LayS::kBytes, s>>>(p);
-  return cudaGetLastError();
+  // pass 2 as a programmatic dependent of pass 1 (its prologue overlaps
+  // pass 1's last items)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kD / kNC, p.H, p.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = LayS::kBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_pass_kernel, p);
 }
 
 }  // namespace kda
