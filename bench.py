@@ -699,6 +699,58 @@ def serving_verify_bytes(steps, h=H):
     return total
 
 
+def run_verify_raw(torch, K, dev, NL, slots, acc, A, G=4, steps=64, warmup=4):
+    """The spec-decode step on projection-space inputs: kda_verify_raw (key
+    L2 norm, alpha = exp(-softplus(z)), beta = sigmoid(b) fused into the
+    verify kernel) on each of NL layers, then kda_commit_layers, with the
+    main line's slots and accepted lengths.  Own pools and rings, own timed
+    region, one CUDA event pair around each step's NL verify launches."""
+    rng = np.random.default_rng(ki.SPEC.seed + 7)
+    pools = [K.StatePool.zeros(P, H, D, device=dev) for _ in range(NL)]
+    rings = [K.ReplayRing(P, H, D, DEPTH, torch.bfloat16, device=dev) for _ in range(NL)]
+    cu = torch.tensor(np.arange(0, (B + 1) * T, T, dtype=np.int32), device=dev)
+    batches = []
+    for _ in range(G):
+        tok = ki.gen_raw_tokens(rng, [T] * B, H, D)
+        t = {n: torch.from_numpy(tok[n]).to(device=dev, dtype=torch.bfloat16)
+             for n in ("q", "k", "v", "alpha", "beta")}
+        batches.append(K.TokenBatch(t["q"], t["k"], t["v"], t["alpha"], t["beta"], cu))
+    stream = torch.cuda.Stream(device=dev)
+    graphs, events = [], []
+    with torch.cuda.stream(stream):
+        for s in range(warmup + steps):
+            g = torch.cuda.CUDAGraph()
+            ev = [torch.cuda.Event(enable_timing=True, external=True)
+                  for _ in range(2)] if s >= warmup else None
+            g.capture_begin()
+            if ev:
+                ev[0].record(stream)
+            for l in range(NL):
+                K.kda_verify(batches[s % G], T, pools[l], slots, rings[l], stream=stream,
+                             raw=True)
+            if ev:
+                ev[1].record(stream)
+            K.kda_commit_layers(acc[s % A], slots, pools[0], rings, stream=stream)
+            g.capture_end()
+            graphs.append(g)
+            events.append(ev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(warmup + steps):
+            graphs[s].replay()
+    torch.cuda.synchronize()
+    bits = K.kda_get_device_error()
+    us = float(np.mean([events[s][0].elapsed_time(events[s][1]) * 1e3 / NL
+                        for s in range(warmup, warmup + steps)]))
+    del graphs, rings, pools
+    torch.cuda.empty_cache()
+    return {"verify_launch_us": us, "tokens_per_s": B * T / (us * 1e-6),
+            "device_error_bits": bits,
+            "note": "kda_verify_raw x NL + kda_commit_layers per step, CUDA graphs, "
+                    "event pair around the NL verify launches; raw keys, decay and "
+                    "beta logits prepared in the kernel"}
+
+
 def run_serving(torch, K, dev, NL, G=4):
     """Serving-shaped load on NL KDA layers (own pools and rings per layer):
     16 sequences prefilled in passes of at most 16384 tokens (chunk 64, a
@@ -1074,6 +1126,7 @@ def run_kda(args, rank, world, local_rank):
     mixed = run_mixed(torch, K, dev)
     direct = run_snapshot_ablation(torch, K, dev, NL, slots, batches, acc, acc_np,
                                    G, A)
+    raw_verify = run_verify_raw(torch, K, dev, NL, slots, acc, A)
     serving = run_serving(torch, K, dev, NL)
     tiny = run_tiny(torch, K, dev)
     cache = state_cache_bytes()
@@ -1138,6 +1191,7 @@ def run_kda(args, rank, world, local_rank):
         "serving": serving,
         "tiny": tiny,
         "ablation_direct_snapshots": direct,
+        "verify_raw_inputs": raw_verify,
     }
     print(json.dumps(line), flush=True)
 

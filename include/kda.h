@@ -263,6 +263,29 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
                const int32_t *is_spec, kda_stream_t stream);
 
 /*
+ * kda_verify_raw -- kda_verify on projection-space inputs, the input prep
+ * fused into the verify kernel (the fused-kernel direction of "Small tensor
+ * copies leave the hot path"; the pages do not define the prep, so it
+ * follows the formulas the synthetic workloads are drawn with, as
+ * kda_prefill_chunked_raw does):
+ *   k     : raw keys, L2-normalised over d_k per (token, head);
+ *   alpha : decay logits z, alpha = exp(-softplus(z)) = 1 / (1 + e^z);
+ *   beta  : logits b, beta = sigmoid(b);
+ *   q, v  : used as given.
+ * Precision: each token's prepared k, alpha and beta are computed once, in
+ * IEEE fp32, when its row is loaded, and rounded to bf16 (round to nearest);
+ * the drafts, ordinary decode and the ring entries all use those bf16 values,
+ * so a replayed state equals the decoded one bit for bit and the ring holds
+ * prepared inputs (a later kda_verify or kda_materialize replays it as usual).
+ * Shapes: bf16 tokens, d_k = d_v = 128, ring depth <= 8, max_T <= 8; any
+ * other shape returns KDA_ESHAPE before anything is launched.  Everything
+ * else -- arguments, ownership, ordering, errors -- is kda_verify's.
+ */
+int kda_verify_raw(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
+                   const int32_t *state_slots, kda_replay_ring *ring,
+                   const int32_t *is_spec, kda_stream_t stream);
+
+/*
  * kda_forward_mixed -- one KDA layer over a packed batch that holds prefill
  * segments beside speculative and ordinary decode segments, read in place
  * with outputs written in place ("Small tensor copies leave the hot path":

@@ -240,13 +240,17 @@ int prefill_impl(const kda_tokens *tok, kda_state_pool *pool, const int32_t *sta
 
 int verify_impl(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
                 const int32_t *state_slots, kda_replay_ring *ring, const int32_t *is_spec,
-                kda_stream_t stream, bool cu_aligned) {
+                kda_stream_t stream, bool cu_aligned, bool raw = false) {
   int st = check_pool(pool);
   if (st) return st;
   if ((st = check_tokens(tok, pool, cu_aligned))) return st;
   if ((st = check_ring(ring, tok->dtype, true))) return st;
   if (max_T < 0) return KDA_EINVAL;
   if (!is_spec && max_T > ring->depth) return KDA_EPROTO;
+  // the prep is fused into the pipelined kernel only
+  if (raw && !(tok->dtype == KDA_BF16 && tok->d_k == 128 && tok->d_v == 128 &&
+               ring->depth <= 8 && max_T <= 8))
+    return KDA_ESHAPE;
   if (kda::verify_smem_bytes(tok->d_k, ring->depth, max_T, tok->dtype) > kMaxSmem)
     return KDA_EINVAL;
   if (tok->num_seqs == 0) return KDA_OK;
@@ -266,6 +270,7 @@ int verify_impl(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
   p.N = tok->num_tokens;
   p.max_T = max_T;
   p.mode = 0;
+  p.raw = raw ? 1 : 0;
   return cuda_status(kda::launch_verify(p, tok->dtype, tok->d_k,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -305,6 +310,12 @@ int kda_verify(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
                const int32_t *state_slots, kda_replay_ring *ring,
                const int32_t *is_spec, kda_stream_t stream) {
   return verify_impl(tok, max_T, pool, state_slots, ring, is_spec, stream, true);
+}
+
+int kda_verify_raw(const kda_tokens *tok, int32_t max_T, kda_state_pool *pool,
+                   const int32_t *state_slots, kda_replay_ring *ring,
+                   const int32_t *is_spec, kda_stream_t stream) {
+  return verify_impl(tok, max_T, pool, state_slots, ring, is_spec, stream, true, true);
 }
 
 int kda_forward_mixed(const kda_tokens *tok, int32_t num_prefill, int32_t prefill_tokens,

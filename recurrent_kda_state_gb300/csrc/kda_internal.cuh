@@ -65,6 +65,7 @@ struct VerifyParams {
   int mode;             // 0 = verify, 1 = materialize (no tokens)
   int prefetch_stride;  // CTAs of the first wave (0: no L2 prefetch)
   int spin_limit;       // polls of a bounded wait before it gives up
+  int raw;              // tokens are projections: prep applied in-kernel
 };
 
 struct CommitParams {

@@ -846,8 +846,8 @@ struct LayP {                                  // pass 1 (two CTAs per SM)
   static constexpr uint32_t EGC = GC + 512, ECM = EGC + 512, EGM = ECM + 512;
   static constexpr uint32_t TOT4 = EGM + 512, NSCR = TOT4 + 2048, BST = NSCR + 768;
   static constexpr uint32_t MBAR = BST + 1024, VBAR = MBAR + 8, SBAR = VBAR + 8;
-  static constexpr uint32_t TSLOT = SBAR + 8;
-  static constexpr uint32_t END = TSLOT + 8;
+  static constexpr uint32_t TSLOT = SBAR + 8, ITEM = TSLOT + 8;  // staged item: tok0, n
+  static constexpr uint32_t END = ITEM + 8;
   static constexpr size_t kBytes = END + 1024;
 };
 static_assert(LayP::V0 % 1024 == 0 && LayP::V0 + 16384 + 8192 <= LayP::GA_LO,
@@ -957,7 +957,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto stage = [&](int j) {
     if (tid == 0) {
       const int gj = j / H, hj = j - (j / H) * H;
-      const int tj = locate_chunk(p, gj, kC).tok0;
+      const ChunkLoc cj = locate_chunk(p, gj, kC);
+      const int tj = cj.tok0;
+      // the item's rows for every thread, read after the staging barrier
+      *reinterpret_cast<int2 *>(sm + LayP::ITEM) = make_int2(tj, cj.n);
       const uint32_t bar = sb + LayP::SBAR;
       mbar_expect_tx(bar, 3 * 64 * 2 * kD + 64 * 16);
       tma_load3(sb + LayP::STG_Q, &maps.q, 0, hj, tj, bar);
@@ -970,11 +973,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool ok = true, stage_owed = true, v_owed = false, mma_owed = false;  // in flight
   for (; it < total; it += gridDim.x) {
     const int g = it / H, h = it - (it / H) * H;
-    const ChunkLoc cl = locate_chunk(p, g, kC);
-    const int n = cl.n, m = n >> 1, t0 = cl.tok0;
     uint8_t *ent = ent0 + ((size_t)g * H + h) * kTcEntryBytes;
     if (!(ok = tc_wait(sbar_p, sphase, p.spin_limit))) break;
     stage_owed = false;
+    const int2 item = *reinterpret_cast<const int2 *>(sm + LayP::ITEM);
+    const int t0 = item.x, n = item.y, m = n >> 1;
     if (tid == 0 && it + (int)gridDim.x < total) {  // the next item's rows into L2
       const int j = it + gridDim.x, gj = j / H, hj = j - (j / H) * H;
       const int tj = locate_chunk(p, gj, kC).tok0;
@@ -1068,8 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float q1 = __uint_as_float(qr[u] & 0xffff0000u);
         // K~ and Q~ rows of [K~; Q~] and the K^ rows: K-major for R1, and the
         // same bytes serve R2 (K~) and the chunk walk's R4 (K^) as MN-major
-        // operands, so no transposed copy is written.  The Q~ and K^ rows
-        // also go to the entry now (a warp writes one 128-byte row).
+        // operands, so no transposed copy is written
         uint32_t hi, lo;
         uint32_t off = umma::sw128_off16(t, c2, 128);
         umma::split_bf16x2(f0 * k0, f1 * k1, hi, lo);
@@ -1079,20 +1081,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         umma::split_bf16x2(f0 * q0, f1 * q1, hi, lo);
         *reinterpret_cast<uint32_t *>(sm + LayP::GA_HI + off) = hi;
         *reinterpret_cast<uint32_t *>(sm + LayP::GA_LO + off) = lo;
-        *reinterpret_cast<uint32_t *>(ent + Entry::GA + off) = hi;
-        *reinterpret_cast<uint32_t *>(ent + Entry::GA + 32768 + off) = lo;
         off = umma::sw128_off16(t, c2, 64);
         umma::split_bf16x2(fi0 * k0, fi1 * k1, hi, lo);
         *reinterpret_cast<uint32_t *>(sm + LayP::GB_HI + off) = hi;
         *reinterpret_cast<uint32_t *>(sm + LayP::GB_LO + off) = lo;
-        *reinterpret_cast<uint32_t *>(ent + Entry::KT + off) = hi;
-        *reinterpret_cast<uint32_t *>(ent + Entry::KT + 16384 + off) = lo;
       }
     }
     tiles_ready();
 
-    // ---- R1: G = [K~; Q~] K^^T
+    // ---- R1: G = [K~; Q~] K^^T, while the bulk-copy engine writes the Q~
+    // rows (rows 64..127 of each 16 KB atom of both splits) and K^ to the
+    // entry: the entry holds the tiles' shared-memory images
     if (tid == 0) {
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
+        const uint32_t off = piece * 16384 + 8192;
+        umma::bulk_s2g(ent + Entry::GA + off, sb + LayP::GA_HI + off, 8192);
+      }
+      umma::bulk_s2g(ent + Entry::KT, sb + LayP::GB_HI, 32768);
+      umma::bulk_commit();
       const uint32_t id = umma::idesc_bf16(128, 64);
       for (int ps = 0; ps < 3; ++ps) {
         const uint32_t a = ps == 1 ? LayP::GA_LO : LayP::GA_HI;
@@ -1103,6 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
+      umma::bulk_wait_read();  // before the Q~ rows and K^ are written over
     }
     mma_owed = true;
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
@@ -1248,6 +1256,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if ((stage_owed) && !umma::mbar_wait(sbar_p, sphase, kDrainWaitPolls))
       set_error(p.err, KDA_DERR_UNSAFE);
   }
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // entry writes done
   umma::fence_before_sync();
   __syncthreads();
   if (tid < 32) umma::tmem_dealloc(tmem, 256);
@@ -1463,9 +1472,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
         }
       }
     }
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
+    // no barrier here: the next chunk's first wait is one, and its
+    // tiles_ready() orders this chunk's TMEM reads before the next MMAs
   }
   if (!ok) {
     if (tid == 0) {

@@ -74,6 +74,7 @@ constexpr int kProducerWarp = 8;
 constexpr int kPrepWarp0 = 9, kPrepWarps = 3, kPrepThreads = 32 * kPrepWarps;
 constexpr int kPipeThreads = 32 * (kConsumerWarps + 1 + kPrepWarps);
 constexpr int kPrepBar = 1;             // named barrier of the prep warps
+constexpr int kPrepChanBar = 2;         // ... of the two channel-pair prep warps
 constexpr int kTStages = 3;             // token stages
 constexpr int kSStages = 2;             // state stages
 constexpr int kMetaBatch = 32;          // units whose words one lane each reads at once
@@ -478,6 +479,55 @@ __device__ void producer(const VerifyParams &p, unsigned char *smb, int lane, in
 }
 
 // ------------------------------------------------------------------- prep
+// Projection-space tokens (RAW): a unit's rows are prepared in place before
+// anything reads them -- the key L2-normalised over its 128 channels,
+// alpha = 1 / (1 + e^z), beta = sigmoid(b) -- in IEEE fp32 and rounded to
+// bf16 once, so decode, the drafts and the ring entries share those bits.
+// The squared norm is always summed in one order: channel-pair sums
+// fma(k_2p, k_2p, k_2p+1^2), a 32-lane xor tree over pairs 0..31 and one over
+// pairs 32..63, then the two halves added; both routines below keep it, so a
+// token prepared as an ordinary row or as a draft gets the same bits.
+__device__ __forceinline__ float pair_sq(float2 k) { return fmaf(k.x, k.x, k.y * k.y); }
+__device__ __forceinline__ float lane_tree(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+__device__ __forceinline__ float inv_norm(float half0, float half1) {
+  return 1.f / fmaxf(sqrtf(half0 + half1), 1e-12f);
+}
+__device__ __forceinline__ float alpha_of_logit(float z) {
+  return __frcp_rn(1.f + expf(z));
+}
+__device__ __forceinline__ float beta_of_logit(float b) {
+  return __frcp_rn(1.f + expf(-b));
+}
+__device__ __forceinline__ float2 round_pair(float2 x, bf16 *dst) {
+  const __nv_bfloat162 r = __floats2bfloat162_rn(x.x, x.y);
+  *reinterpret_cast<__nv_bfloat162 *>(dst) = r;
+  return __bfloat1622float2(r);
+}
+
+// Rows of a unit with no drafts (ordinary decode): warp w prepares rows
+// w, w + 3, ...; lane l holds channel pairs l and l + 32.
+__device__ __forceinline__ void prep_raw_rows(bf16 *rec, int T, int w, int lane) {
+  for (int t = w; t < T; t += kPrepWarps) {
+    bf16 *r = rec + t * R::kStride;
+    const int c0 = 2 * lane, c1 = 2 * lane + PD / 2;
+    const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(r + R::kK + c0));
+    const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(r + R::kK + c1));
+    const float2 z0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(r + R::kA + c0));
+    const float2 z1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(r + R::kA + c1));
+    const float inv = inv_norm(lane_tree(pair_sq(k0)), lane_tree(pair_sq(k1)));
+    round_pair(make_float2(k0.x * inv, k0.y * inv), r + R::kK + c0);
+    round_pair(make_float2(k1.x * inv, k1.y * inv), r + R::kK + c1);
+    round_pair(make_float2(alpha_of_logit(z0.x), alpha_of_logit(z0.y)), r + R::kA + c0);
+    round_pair(make_float2(alpha_of_logit(z1.x), alpha_of_logit(z1.y)), r + R::kA + c1);
+    if (lane == 0) r[R::kB] = __float2bfloat16_rn(beta_of_logit(__bfloat162float(r[R::kB])));
+  }
+}
+
+template <bool RAW>
 __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limit) {
   typedef PipeLayout L;
   const Bars bars(smb);
@@ -494,6 +544,10 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
     unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
     const UnitMeta m = *reinterpret_cast<const UnitMeta *>(ts + L::kTsMeta);
     const bool drafts = !m.skip && m.spec && m.T > 0;
+    if (RAW && !m.skip && !drafts && m.T > 0) {  // drafts: prepared in the first phase
+      prep_raw_rows(reinterpret_cast<bf16 *>(ts + L::kTsRec), m.T, pt >> 5, lane);
+      named_sync(kPrepBar, kPrepThreads);
+    }
     if (drafts) {
       const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
       unsigned char *fragb = ts + L::kTsFrag;
@@ -532,6 +586,29 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           kv[t] = in ? ld2(rr + R::kK + c) : make_float2(0.f, 0.f);
           qv[t] = in ? ld2(rr + R::kQ + c) : make_float2(0.f, 0.f);
         }
+        if (RAW) {
+          // projection-space rows: the squared key norms (this warp's half of
+          // the channel pairs) to the scratch, then the prepared, rounded k
+          // and alpha of this pair in place and in registers
+          float *nh = am;  // the pair products are written later
+#pragma unroll
+          for (int t = 0; t < PT; ++t) {
+            const float x = lane_tree(pair_sq(kv[t]));
+            if (lane == 0) nh[(pt >> 5) * PT + t] = x;
+          }
+          named_sync(kPrepChanBar, 2 * 32);
+          bf16 *rw = const_cast<bf16 *>(rec);
+#pragma unroll
+          for (int t = 0; t < PT; ++t) {
+            if (t < T) {
+              const float inv = inv_norm(nh[t], nh[PT + t]);
+              kv[t] = round_pair(make_float2(kv[t].x * inv, kv[t].y * inv),
+                                 rw + t * R::kStride + R::kK + c);
+              av[t] = round_pair(make_float2(alpha_of_logit(av[t].x), alpha_of_logit(av[t].y)),
+                                 rw + t * R::kStride + R::kA + c);
+            }
+          }
+        }
         float2 g = make_float2(1.f, 1.f);
 #pragma unroll
         for (int t = 0; t < PT; ++t) {
@@ -548,6 +625,10 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           put(1, t, qt[t].x, qt[t].y);
           put(2, t, kh.x, kh.y);
         }
+      }
+      if (RAW && !chan && pt - PD / 2 < T) {  // the third warp: the rows' beta
+        bf16 *rb = const_cast<bf16 *>(rec) + (pt - PD / 2) * R::kStride + R::kB;
+        *rb = __float2bfloat16_rn(beta_of_logit(__bfloat162float(*rb)));
       }
       unsafe = named_or(kPrepBar, kPrepThreads, unsafe);
       if (!unsafe) {
@@ -729,6 +810,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
 }
 
 // -------------------------------------------------------------- consumers
+template <bool RAW>
 __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int limit) {
   typedef PipeLayout L;
   constexpr int F = PD / 16;
@@ -788,19 +870,22 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
       for (int t = 0; t < m.acc; ++t)
         kda_step_ptrs<PD, false, bf16>(S, rk + t * PD, ra + t * PD, nullptr, rv + t * PD,
                                        rb + t, rg, j0, o0, o1);
-      if (!m.spec) {
-        // ordinary decode (or materialize): apply and commit
-        for (int t = 0; t < m.T; ++t) {
-          kda_step<PD, true, bf16>(S, rec + t * R::kStride, rg, j0, o0, o1);
-          if (rg == 0)
-            *reinterpret_cast<float2 *>(p.o + ((size_t)(m.tok0 + t) * H + h) * PD + j0) =
-                make_float2(o0, o1);
-        }
-        if (m.acc > 0 || m.T > 0) store_state();
-      }
     }
     if (!m.skip && m.spec && m.acc > 0) store_state();  // the committed state
-    if (!pipe_wait(&bars.pfull[k], n / kTStages, limit, abort_flag, p.err)) break;
+    // projection-space rows are read only once the prep warps have prepared them
+    if (RAW && !pipe_wait(&bars.pfull[k], n / kTStages, limit, abort_flag, p.err)) break;
+    if (!m.skip && !m.spec) {
+      // ordinary decode (or materialize): apply and commit
+      float o0 = 0.f, o1 = 0.f;
+      for (int t = 0; t < m.T; ++t) {
+        kda_step<PD, true, bf16>(S, rec + t * R::kStride, rg, j0, o0, o1);
+        if (rg == 0)
+          *reinterpret_cast<float2 *>(p.o + ((size_t)(m.tok0 + t) * H + h) * PD + j0) =
+              make_float2(o0, o1);
+      }
+      if (m.acc > 0 || m.T > 0) store_state();
+    }
+    if (!RAW && !pipe_wait(&bars.pfull[k], n / kTStages, limit, abort_flag, p.err)) break;
     if (drafts) {
       // drafts: o_t = (S^T Q^)_t + W_t, S^T Q^ from the registers on the
       // tensor cores, hi*hi + lo*hi + hi*lo
@@ -837,6 +922,7 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
   }
 }
 
+template <bool RAW>
 __global__ void __launch_bounds__(kPipeThreads, 1) verify_pipe_kernel(const VerifyParams p) {
   typedef PipeLayout L;
   extern __shared__ float4 smem4[];
@@ -906,8 +992,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) verify_pipe_kernel(const Veri
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int limit = p.spin_limit;
   if (warp == kProducerWarp) producer(p, smb, lane, limit);
-  else if (warp >= kPrepWarp0) prep(p, smb, tid - 32 * kPrepWarp0, limit);
-  else consumer(p, smb, tid, limit);
+  else if (warp >= kPrepWarp0) prep<RAW>(p, smb, tid - 32 * kPrepWarp0, limit);
+  else consumer<RAW>(p, smb, tid, limit);
   __syncthreads();
 }
 
@@ -928,8 +1014,11 @@ cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!ready[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(verify_pipe_kernel,
+      cudaError_t e = cudaFuncSetAttribute(verify_pipe_kernel<false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(verify_pipe_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
@@ -953,7 +1042,8 @@ cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, verify_pipe_kernel, p);
+  return cudaLaunchKernelEx(&cfg, p.raw ? verify_pipe_kernel<true> : verify_pipe_kernel<false>,
+                            p);
 }
 
 }  // namespace kda

@@ -42,7 +42,7 @@ class kda_replay_ring(ctypes.Structure):
 
 
 EXPORTS = ("kda_prefill_chunked", "kda_prefill_chunked_raw", "kda_prefill_chunked_noalloc",
-           "kda_prefill_workspace_size", "kda_verify",
+           "kda_prefill_workspace_size", "kda_verify", "kda_verify_raw",
            "kda_commit", "kda_commit_layers", "kda_materialize", "kda_ring_reset",
            "kda_gather_states", "kda_copy_slots", "kda_verify_snapshot",
            "kda_commit_snapshot", "kda_forward_mixed", "kda_get_device_error",
@@ -70,6 +70,7 @@ def lib():
         L.kda_prefill_workspace_size.argtypes = [_I32] * 6 + [ctypes.c_int]
         L.kda_prefill_workspace_size.restype = ctypes.c_size_t
         L.kda_verify.argtypes = [tp, _I32, pp, _P, rp, _P, _P]
+        L.kda_verify_raw.argtypes = [tp, _I32, pp, _P, rp, _P, _P]
         L.kda_commit.argtypes = [_P, _P, _I32, pp, rp, _P]
         L.kda_commit_layers.argtypes = [_P, _P, _I32, pp, rp, _I32, _P]
         L.kda_materialize.argtypes = [_P, _I32, pp, rp, _P]
@@ -218,10 +219,14 @@ def kda_prefill_chunked_noalloc(tok, pool, state_slots, chunk, ckpt_every=0,
         _stream(stream)), "kda_prefill_chunked_noalloc")
 
 
-def kda_verify(tok, max_T, pool, state_slots, ring, is_spec=None, stream=None):
-    _check(lib().kda_verify(ctypes.byref(tok.c), max_T, ctypes.byref(pool.c),
-                            _ptr(state_slots), ctypes.byref(ring.c),
-                            _ptr(is_spec), _stream(stream)), "kda_verify")
+def kda_verify(tok, max_T, pool, state_slots, ring, is_spec=None, stream=None,
+               raw=False):
+    """raw: projection-space keys, decay and beta logits, prep fused
+    (kda_verify_raw)."""
+    fn, name = ((lib().kda_verify_raw, "kda_verify_raw") if raw
+                else (lib().kda_verify, "kda_verify"))
+    _check(fn(ctypes.byref(tok.c), max_T, ctypes.byref(pool.c), _ptr(state_slots),
+              ctypes.byref(ring.c), _ptr(is_spec), _stream(stream)), name)
 
 
 def kda_forward_mixed(tok, num_prefill, prefill_tokens, pool, state_slots, chunk,

@@ -196,3 +196,27 @@ def test_prefill_raw_needs_the_tensor_core_shape(L):
     ws = ctypes.c_void_p(0x80000)
     assert L.kda_prefill_chunked_raw(ctypes.byref(tok), ctypes.byref(pool), s, None, 0, 0,
                                      16, None, ws, 1 << 20, None) == kda.KDA_ESHAPE
+
+
+def test_verify_raw_needs_the_pipelined_shape(L):
+    """The fused-prep verify exists only where the prep is fused: bf16 tokens,
+    d = 128, ring depth <= 8, at most 8 tokens per row; every other shape is
+    refused on the host."""
+    by = ctypes.byref
+    s = ctypes.c_void_p(0x40000)
+    pool16, tok16, ring16 = _pool(), _tokens(), _ring()
+    assert L.kda_verify_raw(by(tok16), 4, by(pool16), s, by(ring16), None,
+                            None) == kda.KDA_ESHAPE                     # d = 16, fp32
+    pool = _pool(P=4, H=2, d=128)
+    tok = _tokens(dtype=kda.KDA_BF16, d=128)
+    deep = _ring(depth=9, dtype=kda.KDA_BF16)
+    assert L.kda_verify_raw(by(tok), 4, by(pool), s, by(deep), None,
+                            None) == kda.KDA_ESHAPE                     # ring depth 9
+    ring = _ring(depth=8, dtype=kda.KDA_BF16)
+    flag = ctypes.c_void_p(0x50000)
+    assert L.kda_verify_raw(by(tok), 9, by(pool), s, by(ring), flag,
+                            None) == kda.KDA_ESHAPE                     # 9 tokens per row
+    f32 = _tokens(dtype=kda.KDA_F32, d=128)
+    r32 = _ring(depth=8, dtype=kda.KDA_F32)
+    assert L.kda_verify_raw(by(f32), 4, by(pool), s, by(r32), None,
+                            None) == kda.KDA_ESHAPE                     # fp32 tokens
