@@ -833,13 +833,17 @@ struct LayP {                                  // pass 1 (two CTAs per SM)
   //   rows nobody reads) in the Q~ lo rows of atom 0;
   //   the inverse's fp32 A and X over the Q~ lo rows of atom 1 and K^, then
   //   T lo over the start of A.
-  static constexpr uint32_t V0 = 8192;
+  // Before V lands, its two slots hold the images of the M rows of the
+  // entry's [T; M] (hi, lo) for their bulk copy.
+  static constexpr uint32_t V0 = 8192, M_HI = 8192, M_LO = 24576;
   static constexpr uint32_t PT = 40960, T_HI = 40960, T_LO = 57344;
   // Once R2 has read its operands nothing of the item is left in shared
-  // memory: the next item's raw q, k, alpha rows land over [K~; Q~] (and
-  // its beta box in MISC) while this item's epilogue runs.  E1 reads them
+  // memory: the next item's raw q, k, alpha rows land in [48 KB, 96 KB) (and
+  // its beta box in MISC) while this item's epilogue writes the W~ and U'
+  // images for their bulk copies in [0, 48 KB).  E1 reads the staged rows
   // into registers before its first barrier and writes tiles only after it.
-  static constexpr uint32_t STG_Q = 0, STG_K = 16384, STG_A = 32768;
+  static constexpr uint32_t STG_Q = 49152, STG_K = 65536, STG_A = 81920;
+  static constexpr uint32_t W_IMG = 0, U_IMG = 32768;  // W~ hi | lo (32 KB), U' half (16 KB)
   static constexpr uint32_t AF = 57344, XF = AF + 64 * 68 * 4;
   static constexpr uint32_t MISC = 98304;
   static constexpr uint32_t BET = MISC, GM = BET + 256, GC = GM + 512;
@@ -857,7 +861,8 @@ static_assert(LayP::PT + 3 * 1024 <= LayP::T_HI + 8192 && LayP::T_HI + 8192 <= L
 static_assert(LayP::AF == LayP::GA_LO + 16384 + 8192 && LayP::XF + 64 * 68 * 4 <= LayP::MISC,
               "A and X over the Q~ lo rows of atom 1 and K^");
 static_assert(LayP::T_LO + 8192 <= LayP::XF, "T lo over A only");
-static_assert(LayP::STG_A + 16384 <= LayP::GB_HI && LayP::BST % 128 == 0, "staging");
+static_assert(LayP::STG_Q >= LayP::U_IMG + 16384 && LayP::STG_A + 16384 <= LayP::MISC &&
+                  LayP::BST % 128 == 0, "staging beside the epilogue images");
 static_assert(2 * (LayP::kBytes + 1024) <= 233472, "two CTAs per SM");
 
 
@@ -1022,6 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     tot4[tq * 128 + c2] = la0[15];
     tot4[tq * 128 + c2 + 1] = la1[15];
+    if (tid == 0) umma::bulk_wait_read();  // the last item's images have been read
     __syncthreads();  // quarter sums visible; staging read (tiles writable)
     {
       float add0 = 0.f, add1 = 0.f;
@@ -1115,16 +1121,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mma_owed = true;
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
-    // R1 has read the Q~ rows and K^: V lands in the Q~ hi rows while the
-    // inverse runs
-    if (tid == 0) {
-      const uint32_t vb = sb + LayP::VBAR;
-      mbar_expect_tx(vb, 2 * 64 * 128);
-      tma_load3(sb + LayP::V0, &maps.v, 0, h, t0, vb);
-      tma_load3(sb + LayP::V0 + 16384, &maps.v, 64, h, t0, vb);
-    }
-    v_owed = true;
-    {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> entry
+    {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> image
       float gv[32];
       {
         float g0[16], g1[16];
@@ -1157,12 +1154,25 @@ __global__ void __launch_bounds__(kThreads, 2)
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = s + e <= t ? gv[8 * ch + e] : 0.f;
-          const uint32_t off = umma::sw128_off16(64 + t, s, 128);
-          put8_global(ent + Entry::KT + 32768 + off, ent + Entry::KT + 49152 + off, x);
+          const uint32_t off = umma::sw128_off16(t, s, 128);  // row 64 + t, less 8 KB
+          put8(sm, LayP::M_HI + off, LayP::M_LO + off, x);
         }
       }
     }
-    __syncthreads();
+    tiles_ready();
+    // R1 has read the Q~ rows and K^: the M images go to the entry, then V
+    // lands in their place (the Q~ hi rows) while the inverse runs
+    if (tid == 0) {
+      umma::bulk_s2g(ent + Entry::KT + 32768 + 8192, sb + LayP::M_HI, 8192);
+      umma::bulk_s2g(ent + Entry::KT + 49152 + 8192, sb + LayP::M_LO, 8192);
+      umma::bulk_commit();
+      umma::bulk_wait_read();
+      const uint32_t vb = sb + LayP::VBAR;
+      mbar_expect_tx(vb, 2 * 64 * 128);
+      tma_load3(sb + LayP::V0, &maps.v, 0, h, t0, vb);
+      tma_load3(sb + LayP::V0 + 16384, &maps.v, 64, h, t0, vb);
+    }
+    v_owed = true;
     unit_lower_inverse(Af, Xf, reinterpret_cast<float *>(sm + LayP::PT), tid);
     {  // T = X diag(beta) -> rows 0..63 of R2's A tile and of the entry's [T; M]
       const int t = tid >> 2, s0 = (tid & 3) * 16;
@@ -1176,7 +1186,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int hh = 0; hh < 2; ++hh) {
         const uint32_t off = umma::sw128_off16(t, s0 + 8 * hh, 128);
         put8(sm, LayP::T_HI + off, LayP::T_LO + off, x + 8 * hh);
-        put8_global(ent + Entry::KT + 32768 + off, ent + Entry::KT + 49152 + off, x + 8 * hh);
       }
     }
     tiles_ready();
@@ -1187,6 +1196,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     // K~ (rows 0..63 of [K~; Q~], 64-key atoms 16 KB apart) and V (two
     // 64-channel atoms 16 KB apart) are MN-major B operands.
     if (tid == 0) {
+      // the T rows of the entry's [T; M] straight from R2's A tile
+      umma::bulk_s2g(ent + Entry::KT + 32768, sb + LayP::T_HI, 8192);
+      umma::bulk_s2g(ent + Entry::KT + 49152, sb + LayP::T_LO, 8192);
+      umma::bulk_commit();
       const uint32_t id = umma::idesc_bf16_bmn(128, 128);
       const uint64_t dKh = umma::sdesc_sw128_mn(sb + LayP::GA_HI, 16384);
       const uint64_t dKl = umma::sdesc_sw128_mn(sb + LayP::GA_LO, 16384);
@@ -1205,6 +1218,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                          (uint32_t)(ps | kk));
       }
       umma::commit(mbar);
+      umma::bulk_wait_read();  // T's images, before anything lands over them
     }
     mma_owed = true;
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
@@ -1214,7 +1228,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       stage(it + gridDim.x);
       stage_owed = true;
     }
-    if (c < 64) {  // W~ row t -> rows 0..63 of the entry's [W~; Q~]; U' row t -> entry
+    // Epilogue: W~ (rows 0..63 of the entry's [W~; Q~]) and U' (the entry's
+    // four 32-column slices, the 16-byte chunks of row t rotated by t) as
+    // shared-memory images written out by the bulk-copy engine, so the
+    // entry is written in whole lines: first W~ and U' slices 0, 1, then
+    // slices 2, 3 in the same 16 KB once the first copies have read it.
+    auto u_rows = [&](int t) {
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        float u[16];
+        const int j0 = 64 * hf + 16 * blk;
+        umma::tmem_ld16(tl + 128 + j0, u);
+        float4 *row = reinterpret_cast<float4 *>(sm + LayP::U_IMG) +
+                      (((j0 >> 5) - 2 * hf) * 64 + t) * 8;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)  // chunk (j mod 32) / 4 at position (chunk + t) mod 8
+          row[((((j0 & 31) >> 2) + e) + t) & 7] =
+              make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+      }
+    };
+    if (c < 64) {
       const int t = c;
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
@@ -1223,27 +1256,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         umma::tmem_ld16(tl + k0, w);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t off = umma::sw128_off16(t, k0 + 8 * hh, 128);
-          put8_global(ent + Entry::GA + off, ent + Entry::GA + 32768 + off, w + 8 * hh);
+          const uint32_t off = umma::sw128_off16(t, k0 + 8 * hh, 64);  // two 8 KB atoms
+          put8(sm, LayP::W_IMG + off, LayP::W_IMG + 16384 + off, w + 8 * hh);
         }
       }
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        float u[16];
-        const int j0 = 64 * hf + 16 * blk;
-        umma::tmem_ld16(tl + 128 + j0, u);
-        float4 *row = reinterpret_cast<float4 *>(ent + Entry::UP) + ((j0 >> 5) * 64 + t) * 8;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)  // chunk (j mod 32) / 4 at position (chunk + t) mod 8
-          row[((((j0 & 31) >> 2) + e) + t) & 7] =
-              make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
-      }
+      if (hf == 0) u_rows(t);
     } else {
       const int j = (c - 64) + 64 * hf;  // 0..127 over the threads of lanes 64..127
       float *vec = reinterpret_cast<float *>(ent + Entry::VEC);
       vec[j] = egmv[j];
       vec[128 + j] = egc[j];
       vec[256 + j] = ecm[j];
+    }
+    tiles_ready();
+    if (tid == 0) {
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece)  // hi atom 0, 1, lo atom 0, 1
+        umma::bulk_s2g(ent + Entry::GA + piece * 16384, sb + LayP::W_IMG + piece * 8192, 8192);
+      umma::bulk_s2g(ent + Entry::UP, sb + LayP::U_IMG, 16384);
+      umma::bulk_commit();
+      umma::bulk_wait_read();
+    }
+    __syncthreads();
+    if (c < 64 && hf == 1) u_rows(c);
+    tiles_ready();
+    if (tid == 0) {
+      umma::bulk_s2g(ent + Entry::UP + 16384, sb + LayP::U_IMG, 16384);
+      umma::bulk_commit();
     }
   }
   if (!ok && tid == 0) {
