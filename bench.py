@@ -415,21 +415,16 @@ def run_prefill(torch, K, dev):
                    "frac_issued": issued / (ms * 1e-3) / 1e12 / tc_peak,
                    "pipe_active_pct": prof.get("sm__pipe_tensor_cycles_active_pct")
                    if prof else None,
-                   "chunk_flops": flops, "issued_flops": issued},
+                   "chunk_flops": flops},
     }
     return {
         "workload": w.name, "tokens_per_s": L / (ms * 1e-3), "ms": ms,
         "roofline": roofline,
-        "launches_per_call": 3, "reps": reps, "algorithmic_bytes": alg_bytes,
-        "achieved_gbs": alg_bytes / (ms * 1e-3) / 1e9,
-        "chunk_flops": flops, "achieved_tflops": flops / (ms * 1e-3) / 1e12,
         "workspace_bytes": ws_bytes,
         "single_pass_ms": ms_single,
-        "single_pass_tokens_per_s": L / (ms_single * 1e-3),
         "raw_inputs_fused_prep_ms": ms_raw,
         "raw_prep_pass_bytes_avoided": prep_bytes,
-        "tensor_pipe": prof,
-        "note": "two tcgen05 passes through the workspace; single_pass: no workspace",
+        "reps": reps,
     }
 
 
@@ -1179,14 +1174,14 @@ def run_kda(args, rank, world, local_rank):
                 "host_wall_ms_per_step": (aw1 - aw0) * 1e3 / args.steps,
                 "calls": "eager kda_verify x %d + kda_commit_layers per step "
                          "through the binding, host copies in the timed region" % NL},
-        "e2e_graph": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
-                      "ms_per_step": ms_e2e / args.steps,
-                      "verify_launch_us_during_copies": e2e_launch_us,
-                      "calls": "the same steps replayed as CUDA graphs captured from the calls"},
         "gpu_launches": (NL + 1) * args.steps,
         "clocks": clocks.summary(w0, w1),
         "device_error_bits": bits,
         "prefill": prefill,
+        "e2e_graph": {"value": job_rate(tokens_rank, world, ms_e2e), "unit": "tokens/s",
+                      "ms_per_step": ms_e2e / args.steps,
+                      "verify_launch_us_during_copies": e2e_launch_us,
+                      "calls": "the same steps replayed as CUDA graphs captured from the calls"},
         "mixed": mixed,
         "serving": serving,
         "tiny": tiny,

@@ -297,6 +297,17 @@ __device__ __forceinline__ bool tc_wait(uint64_t *mbar, uint32_t &phase, int lim
   return all;
 }
 
+// This thread waits for the barrier's phase (bounded) with no block barrier:
+// the caller folds the outcome into the next barrier it crosses
+// (tiles_ready_and / __syncthreads_and), so every thread still agrees before
+// acting on it.  On success the phase advances.
+__device__ __forceinline__ bool own_wait(uint64_t *mbar, uint32_t &phase, int limit) {
+  const bool ok = umma::mbar_wait(mbar, phase, limit);
+  if (ok) phase ^= 1u;
+  umma::fence_after_sync();
+  return ok;
+}
+
 // Publish this thread's shared-memory tile writes to the tensor core and
 // meet the MMA-issuing thread.
 __device__ __forceinline__ void tiles_ready() {
@@ -304,6 +315,14 @@ __device__ __forceinline__ void tiles_ready() {
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
+}
+// tiles_ready() that also agrees on every thread's `ok`.
+__device__ __forceinline__ bool tiles_ready_and(bool ok) {
+  umma::fence_smem_to_async();
+  umma::fence_before_sync();
+  const bool all = __syncthreads_and(ok) != 0;
+  umma::fence_after_sync();
+  return all;
 }
 
 // Tensor maps of the packed inputs viewed as [N][H][D] (3-D, innermost D):
@@ -979,8 +998,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (; it < total; it += gridDim.x) {
     const int g = it / H, h = it - (it / H) * H;
     uint8_t *ent = ent0 + ((size_t)g * H + h) * kTcEntryBytes;
-    if (!(ok = tc_wait(sbar_p, sphase, p.spin_limit))) break;
-    stage_owed = false;
+    // every thread waits for the staged rows itself; the outcome is agreed at
+    // E1's first barrier (nothing before it leaves shared memory)
+    const bool gotS = own_wait(sbar_p, sphase, p.spin_limit);
+    if (gotS) stage_owed = false;  // this thread's phase moved: nothing owed
     const int2 item = *reinterpret_cast<const int2 *>(sm + LayP::ITEM);
     const int t0 = item.x, n = item.y, m = n >> 1;
     if (tid == 0 && it + (int)gridDim.x < total) {  // the next item's rows into L2
@@ -1028,7 +1049,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     tot4[tq * 128 + c2] = la0[15];
     tot4[tq * 128 + c2 + 1] = la1[15];
     if (tid == 0) umma::bulk_wait_read();  // the last item's images have been read
-    __syncthreads();  // quarter sums visible; staging read (tiles writable)
+    // quarter sums visible; staging read (tiles writable)
+    if (!(ok = __syncthreads_and(gotS) != 0)) break;
     {
       float add0 = 0.f, add1 = 0.f;
       for (int w = 0; w < tq; ++w) {
@@ -1119,6 +1141,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       umma::bulk_wait_read();  // before the Q~ rows and K^ are written over
     }
     mma_owed = true;
+    // a barrier here, not a thread's own wait: thread 0 has waited for the
+    // bulk reads of K^ and the Q~ rows, which A and the M images overwrite
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
     {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> image
@@ -1188,9 +1212,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         put8(sm, LayP::T_HI + off, LayP::T_LO + off, x + 8 * hh);
       }
     }
-    tiles_ready();
-    if (!(ok = tc_wait(vbar_p, vphase, p.spin_limit))) break;
-    v_owed = false;
+    const bool gotV = own_wait(vbar_p, vphase, p.spin_limit);
+    if (gotV) v_owed = false;
+    if (!(ok = tiles_ready_and(gotV))) break;
 
     // ---- R2: T K~ -> W~ (accumulator columns 0..127);  T V -> U' (128..255).
     // K~ (rows 0..63 of [K~; Q~], 64-key atoms 16 KB apart) and V (two
@@ -1221,6 +1245,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       umma::bulk_wait_read();  // T's images, before anything lands over them
     }
     mma_owed = true;
+    // a barrier here too: thread 0 has waited for the bulk reads of T, which
+    // the U' image overwrites
     if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
     mma_owed = false;
     // R2 has read every tile: the next item's rows land during the epilogue
@@ -1261,14 +1287,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (hf == 0) u_rows(t);
-    } else {
+    }
+    tiles_ready();
+    if (c >= 64) {
       const int j = (c - 64) + 64 * hf;  // 0..127 over the threads of lanes 64..127
       float *vec = reinterpret_cast<float *>(ent + Entry::VEC);
       vec[j] = egmv[j];
       vec[128 + j] = egc[j];
       vec[256 + j] = ecm[j];
     }
-    tiles_ready();
     if (tid == 0) {
 #pragma unroll
       for (int piece = 0; piece < 4; ++piece)  // hi atom 0, 1, lo atom 0, 1
@@ -1402,8 +1429,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     const float *up = reinterpret_cast<const float *>(sm + LayS::SMALL +
                                                       (q & 1) * LayS::SMALL_BYTES);
     const float *vec = up + 64 * kNC;
-    if (!(ok = tc_wait(g1bar, ph1, p.spin_limit))) break;
-    owe1 = false;
+    const bool got1 = own_wait(g1bar, ph1, p.spin_limit);  // agreed at tiles_ready_and
+    if (got1) owe1 = false;  // this thread's phase moved: nothing owed
     if (tid == 32 && q + 2 < nch) {  // two chunks ahead: into L2 (not the MMA warp)
       const uint8_t *e = entry(q + 2);
       umma::prefetch_l2(e + Entry::GA, 131072);
@@ -1417,7 +1444,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       for (int jj = 0; jj < 16; ++jj) x[jj] = egm * S[jj];
       put16_mn(sm, LayS::SB, c, 16 * hf, x);
     }
-    tiles_ready();
+    if (!(ok = tiles_ready_and(got1))) break;
     // ---- R3: [W~; Q~] S~ -> W S (rows 0..63), Q S (rows 64..127)
     if (tid == 0) {  // A_hi [S~_hi | S~_lo], then A_lo [S~_hi | S~_lo] (N = 64)
       const uint32_t id = umma::idesc_bf16_bmn(128, 2 * kNC);
@@ -1430,9 +1457,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       umma::commit(mbar);
     }
     mma_owed = true;
-    if (!(ok = tc_wait(mbar, phase, p.spin_limit))) break;
-    mma_owed = false;
-    if (q + 1 < nch) issue_g1(q + 1);  // [W~; Q~] is free; the other parity too
+    // each thread sees R3 complete; the outcome is agreed at the next barrier
+    // (nothing below writes global memory before it)
+    const bool got3 = own_wait(mbar, phase, p.spin_limit);
+    if (got3) mma_owed = false;
+    if (tid == 0 && got3 && q + 1 < nch) issue_g1(q + 1);  // [W~; Q~] is free; the other parity too
     if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
       const int t = c;
       float ws[16], ws2[16];
@@ -1449,9 +1478,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
       }
       put16_mn(sm, LayS::UT, t, 16 * hf, ws);
     }
-    if (!(ok = tc_wait(g2bar, ph2, p.spin_limit))) break;
-    owe2 = false;
-    tiles_ready();
+    const bool got2 = own_wait(g2bar, ph2, p.spin_limit);
+    if (got2) owe2 = false;
+    if (!(ok = tiles_ready_and(got2 && got3))) break;
     // ---- R4: K^^T U -> state increment; [T; M] U accumulates M U on Q S
     if (tid == 0) {  // as R3: both A splits against [U_hi | U_lo]; K^^T is the
                      // K^ tile read MN-major (64-key atoms 8 KB apart)
@@ -1511,8 +1540,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
         }
       }
     }
-    // no barrier here: the next chunk's first wait is one, and its
-    // tiles_ready() orders this chunk's TMEM reads before the next MMAs
+    // no barrier here: the next chunk's tiles_ready_and() orders this
+    // chunk's TMEM reads before the next MMAs
   }
   if (!ok) {
     if (tid == 0) {
