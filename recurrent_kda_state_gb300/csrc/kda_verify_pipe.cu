@@ -57,6 +57,8 @@
 // (S^T X)_{j0 / j0+1, t = 2r + {0,1}}.  The pair products use K^ as A (rows
 // s = 0..7, rows 8..15 zero) in the same k order, so D row s, column t is
 // K^_s . X_t.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -97,11 +99,13 @@ static_assert(sizeof(MetaEnt) == 64, "meta ring entries are 64 bytes");
 
 // Shared-memory carve-up, byte offsets from a 1024-aligned base.
 struct PipeLayout {
-  // state stage: state [PD][PD] fp32 (the pool's layout: row j = value
-  // column), meta (slot and whether the state was loaded)
+  // state stage: state [PD][PD] fp32 as four 16 KB boxes of 32 key channels
+  // x 128 value rows (row j = value column, 128 bytes, its 16-byte chunks
+  // swizzled by j % 8: the TMA 128-byte swizzle), then the meta (slot and
+  // whether the state was loaded); stages 1024-byte aligned for the swizzle
   static constexpr int kSsState = 0;
   static constexpr int kSsMeta = PD * PD * 4;
-  static constexpr int kSStage = (kSsMeta + (int)sizeof(UnitMeta) + 127) & ~127;
+  static constexpr int kSStage = (kSsMeta + (int)sizeof(UnitMeta) + 1023) & ~1023;
   // token stage:
   //   rec   the drafted / ordinary tokens (Rec layout, input dtype)
   //   rv    pending ring entries' v [8][PD] (input dtype), rb their beta [8]
@@ -320,8 +324,8 @@ __device__ __forceinline__ void prefetch_state(const VerifyParams &p, unsigned c
 
 // Unit n's state into state stage n % 2: four 16 KiB bulk copies completing
 // on the stage's barrier, after the meta (lane 0's arrival).
-__device__ void issue_state(const VerifyParams &p, unsigned char *smb, const Bars &bars,
-                            int n, int lane) {
+__device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsigned char *smb,
+                            const Bars &bars, int n, int lane) {
   typedef PipeLayout L;
   const int s = n % kSStages;
   unsigned char *ss = smb + L::kSStages0 + s * L::kSStage;
@@ -332,14 +336,16 @@ __device__ void issue_state(const VerifyParams &p, unsigned char *smb, const Bar
     else mbar_arrive_tx(&bars.sfull[s], PD * PD * 4);
   }
   __syncwarp();
-  if (!m.skip && lane < 4) {  // four 16 KiB pieces, one per lane
+  if (!m.skip && lane < 4) {  // four 16 KiB boxes, one per lane
     const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
-    const size_t unit = (size_t)m.slot * p.H + h;
-    constexpr uint32_t kPiece = PD * PD;  // bytes
-    umma::bulk_g2s(umma::smem_u32(ss + L::kSsState) + lane * kPiece,
-                   reinterpret_cast<const unsigned char *>(p.pool + unit * PD * PD) +
-                       lane * kPiece,
-                   kPiece, umma::smem_u32(&bars.sfull[s]));
+    const int row0 = (m.slot * p.H + h) * PD;  // the unit's first value row
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(umma::smem_u32(ss + L::kSsState) + lane * (PD * 32 * 4)),
+           "l"(reinterpret_cast<uint64_t>(smap)), "r"(lane * 32), "r"(row0),
+           "r"(umma::smem_u32(&bars.sfull[s]))
+        : "memory");
   }
 }
 
@@ -405,7 +411,8 @@ __device__ __forceinline__ bool use_done(uint64_t *bar, int use) {
 // once the consumers have taken unit n - 2's state into registers, unit n's
 // tokens once they have finished unit n - 3.  Polling is bounded: `limit`
 // rounds with nothing to issue end the CTA's work with KDA_DERR_TIMEOUT.
-__device__ void producer(const VerifyParams &p, unsigned char *smb, int lane, int limit) {
+__device__ void producer(const VerifyParams &p, const CUtensorMap *smap, unsigned char *smb,
+                         int lane, int limit) {
   typedef PipeLayout L;
   const Bars bars(smb);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
@@ -419,7 +426,7 @@ __device__ void producer(const VerifyParams &p, unsigned char *smb, int lane, in
   int ns = 0, nt = 0, fetched = 0;
   fetch_batch_a(p, smb, 0, cnt, lane);
   if (cnt > 0) {
-    issue_state(p, smb, bars, 0, lane);
+    issue_state(p, smap, smb, bars, 0, lane);
     s_last[0] = 0;
     ns = 1;
   }
@@ -438,7 +445,7 @@ __device__ void producer(const VerifyParams &p, unsigned char *smb, int lane, in
     }
     if (ns < cnt && ns < fetched && (ns < kSStages ||
                                      use_done(&bars.sempty[ns % kSStages], ns / kSStages - 1))) {
-      issue_state(p, smb, bars, ns, lane);
+      issue_state(p, smap, smb, bars, ns, lane);
       s_last[ns % kSStages] = ns / kSStages;
       if (ns + 1 < fetched) prefetch_state(p, smb, ns + 1, lane);
       ++ns;
@@ -828,13 +835,17 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
     {
       const unsigned char *ss = smb + L::kSStages0 + s * L::kSStage;
       if (!reinterpret_cast<const UnitMeta *>(ss + L::kSsMeta)->skip) {
-        const ulonglong2 *c0 =
-            reinterpret_cast<const ulonglong2 *>(ss + L::kSsState + (size_t)j0 * PD * 4);
-        const ulonglong2 *c1 = c0 + PD / 4;
+        // chunk q = rg + 4f (key channels 4q .. 4q + 3) of rows j0, j0 + 1:
+        // box q / 8, position (q % 8) ^ (row % 8) -- the eight rows of a
+        // warp's lanes land in distinct bank groups
+        const unsigned char *st = ss + L::kSsState;
 #pragma unroll
         for (int f = 0; f < F; ++f) {
-          const ulonglong2 x = c0[rg + 4 * f];
-          const ulonglong2 y = c1[rg + 4 * f];
+          const int q = rg + 4 * f, box = (q >> 3) * (PD * 32 * 4), cb = q & 7;
+          const ulonglong2 x = *reinterpret_cast<const ulonglong2 *>(
+              st + box + j0 * 128 + ((cb ^ (j0 & 7)) << 4));
+          const ulonglong2 y = *reinterpret_cast<const ulonglong2 *>(
+              st + box + (j0 + 1) * 128 + ((cb ^ ((j0 + 1) & 7)) << 4));
           S[0][2 * f] = x.x; S[0][2 * f + 1] = x.y;
           S[1][2 * f] = y.x; S[1][2 * f + 1] = y.y;
         }
@@ -923,7 +934,8 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
 }
 
 template <bool RAW>
-__global__ void __launch_bounds__(kPipeThreads, 1) verify_pipe_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kPipeThreads, 1)
+    verify_pipe_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap smap) {
   typedef PipeLayout L;
   extern __shared__ float4 smem4[];
   unsigned char *smb = reinterpret_cast<unsigned char *>(
@@ -991,12 +1003,50 @@ __global__ void __launch_bounds__(kPipeThreads, 1) verify_pipe_kernel(const Veri
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int limit = p.spin_limit;
-  if (warp == kProducerWarp) producer(p, smb, lane, limit);
+  if (warp == kProducerWarp) producer(p, &smap, smb, lane, limit);
   else if (warp >= kPrepWarp0) prep<RAW>(p, smb, tid - 32 * kPrepWarp0, limit);
   else consumer<RAW>(p, smb, tid, limit);
   __syncthreads();
 }
 
+}  // namespace
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The pool as a 2-D fp32 tensor [P * H * PD rows][PD], boxes of 32 key
+// channels x PD value rows (128-byte rows) with the 128-byte swizzle.
+cudaError_t state_map(CUtensorMap *tm, float *pool, int P, int H) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {(cuuint64_t)PD, (cuuint64_t)P * H * PD};
+  const cuuint64_t gstride[1] = {(cuuint64_t)PD * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)PD};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, gdim, gstride, box,
+                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 }  // namespace
 
 bool verify_pipe_applies(const VerifyParams &p, kda_dtype dt, int D) {
@@ -1042,8 +1092,11 @@ cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  CUtensorMap smap;
+  const cudaError_t e = state_map(&smap, p.pool, p.P, p.H);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, p.raw ? verify_pipe_kernel<true> : verify_pipe_kernel<false>,
-                            p);
+                            p, smap);
 }
 
 }  // namespace kda
