@@ -59,6 +59,7 @@
 // K^_s . X_t.
 #include <cuda.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -83,7 +84,22 @@ constexpr int kMetaBatch = 32;          // units whose words one lane each reads
 constexpr int kMetaRing = 2 * kMetaBatch;
 
 typedef __nv_bfloat16 bf16;
-typedef Rec<PD, bf16> R;
+// A token stage's rows: dense [PT][PD] arrays of k, alpha, q and v (row t =
+// token t: the layout one TMA box of PT tokens x PD channels lands in), then
+// beta [PT].  Channel c of token t's field X is at X + t * kStride + c; the
+// beta of token t at kB + t.
+struct R {
+  static constexpr int kStride = PD;
+  static constexpr int kK = 0, kA = PT * PD, kQ = 2 * PT * PD, kV = 3 * PT * PD;
+  static constexpr int kB = 4 * PT * PD;
+  static constexpr int kBytes = (kB + PT) * 2;
+};
+
+// The packed token tensors [N][H][PD] (bf16) as 3-D tensor maps with boxes of
+// PD channels x 1 head x PT tokens (rows past N read as zeros).
+struct TokMaps {
+  CUtensorMap k, a, q, v;
+};
 
 // Per-unit facts the producer hands to the other roles.
 struct UnitMeta {
@@ -107,7 +123,7 @@ struct PipeLayout {
   static constexpr int kSsMeta = PD * PD * 4;
   static constexpr int kSStage = (kSsMeta + (int)sizeof(UnitMeta) + 1023) & ~1023;
   // token stage:
-  //   rec   the drafted / ordinary tokens (Rec layout, input dtype)
+  //   rec   the drafted / ordinary tokens (R layout, input dtype)
   //   rv    pending ring entries' v [8][PD] (input dtype), rb their beta [8]
   //   rk    pending ring entries' k, alpha [2][8][PD] (input dtype)
   //   frag  three regions of 8 k-tiles x 32 lanes x {hi01, hi23, lo01, lo23}:
@@ -117,7 +133,7 @@ struct PipeLayout {
   //         products are taken, the K~ fragments' region holds the small
   //         matrices that give M.
   static constexpr int kTsRec = 0;
-  static constexpr int kTsRv = kTsRec + PT * R::kBytes;
+  static constexpr int kTsRv = kTsRec + R::kBytes;
   static constexpr int kTsRb = kTsRv + kDepthMax * PD * 2;
   static constexpr int kTsRk = kTsRb + 16;
   static constexpr int kTsFrag = kTsRk + 2 * kDepthMax * PD * 2;
@@ -353,8 +369,8 @@ __device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsi
 // async copies spread over the lanes (each lane's copies arrive on the
 // stage's barrier when they land); the beta values and the meta by plain
 // stores, lane 0 arriving after them.
-__device__ void issue_tokens(const VerifyParams &p, unsigned char *smb, const Bars &bars,
-                             int n, int lane) {
+__device__ void issue_tokens(const VerifyParams &p, const TokMaps *tmaps, unsigned char *smb,
+                             const Bars &bars, int n, int lane) {
   typedef PipeLayout L;
   const int k = n % kTStages;
   unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
@@ -364,14 +380,23 @@ __device__ void issue_tokens(const VerifyParams &p, unsigned char *smb, const Ba
     const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
     const size_t unit = (size_t)m.slot * p.H + h;
     const uint32_t base = umma::smem_u32(ts);
-    // tokens: 64 chunks each (k, alpha, v, q rows of 16 chunks)
-    for (int c = lane; c < m.T * 64; c += 32) {
-      const int t = c >> 6, which = (c >> 4) & 3, c16 = c & 15;
-      const bf16 *src = reinterpret_cast<const bf16 *>(
-          which == 0 ? p.k : which == 1 ? p.alpha : which == 2 ? p.v : p.q);
-      const int off = which == 0 ? R::kK : which == 1 ? R::kA : which == 2 ? R::kV : R::kQ;
-      cp_async16(base + L::kTsRec + (t * R::kStride + off + c16 * 8) * 2,
-                 src + ((size_t)(m.tok0 + t) * p.H + h) * PD + c16 * 8);
+    if (m.T > 0 && lane == 0) {
+      // the rows: one TMA box of PT tokens per field (rows past the segment
+      // are other tokens or zeros and are never read), their bytes on the
+      // stage's barrier
+      const uint32_t bar = umma::smem_u32(&bars.tfull[k]);
+      asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
+                   :: "r"(bar), "r"(4 * PT * PD * 2) : "memory");
+      const CUtensorMap *maps[4] = {&tmaps->k, &tmaps->a, &tmaps->q, &tmaps->v};
+      const int offs[4] = {R::kK, R::kA, R::kQ, R::kV};
+#pragma unroll
+      for (int f = 0; f < 4; ++f)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];"
+            :: "r"(base + L::kTsRec + offs[f] * 2), "l"(reinterpret_cast<uint64_t>(maps[f])),
+               "r"(0), "r"(h), "r"(m.tok0), "r"(bar)
+            : "memory");
     }
     // pending ring entries: k, alpha and v
     for (int c = lane; c < m.acc * 48; c += 32) {
@@ -385,8 +410,7 @@ __device__ void issue_tokens(const VerifyParams &p, unsigned char *smb, const Ba
     }
     if (lane < m.acc) reinterpret_cast<unsigned short *>(ts + L::kTsRb)[lane] = e.b[lane];
     if (lane >= 8 && lane < 8 + m.T)
-      reinterpret_cast<unsigned short *>(ts + L::kTsRec)[(lane - 8) * R::kStride + R::kB] =
-          e.b[lane];
+      reinterpret_cast<unsigned short *>(ts + L::kTsRec)[R::kB + (lane - 8)] = e.b[lane];
   }
   if (lane == 0) *reinterpret_cast<UnitMeta *>(ts + L::kTsMeta) = m;
   cp_async_arrive(&bars.tfull[k]);
@@ -411,8 +435,8 @@ __device__ __forceinline__ bool use_done(uint64_t *bar, int use) {
 // once the consumers have taken unit n - 2's state into registers, unit n's
 // tokens once they have finished unit n - 3.  Polling is bounded: `limit`
 // rounds with nothing to issue end the CTA's work with KDA_DERR_TIMEOUT.
-__device__ void producer(const VerifyParams &p, const CUtensorMap *smap, unsigned char *smb,
-                         int lane, int limit) {
+__device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const TokMaps *tmaps,
+                         unsigned char *smb, int lane, int limit) {
   typedef PipeLayout L;
   const Bars bars(smb);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
@@ -438,7 +462,7 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, unsigne
     bool did = false;
     if (nt < cnt && nt < fetched && (nt < kTStages ||
                                      use_done(&bars.tempty[nt % kTStages], nt / kTStages - 1))) {
-      issue_tokens(p, smb, bars, nt, lane);
+      issue_tokens(p, tmaps, smb, bars, nt, lane);
       t_last[nt % kTStages] = nt / kTStages;
       ++nt;
       did = true;
@@ -530,7 +554,8 @@ __device__ __forceinline__ void prep_raw_rows(bf16 *rec, int T, int w, int lane)
     round_pair(make_float2(k1.x * inv, k1.y * inv), r + R::kK + c1);
     round_pair(make_float2(alpha_of_logit(z0.x), alpha_of_logit(z0.y)), r + R::kA + c0);
     round_pair(make_float2(alpha_of_logit(z1.x), alpha_of_logit(z1.y)), r + R::kA + c1);
-    if (lane == 0) r[R::kB] = __float2bfloat16_rn(beta_of_logit(__bfloat162float(r[R::kB])));
+    if (lane == 0)
+      rec[R::kB + t] = __float2bfloat16_rn(beta_of_logit(__bfloat162float(rec[R::kB + t])));
   }
 }
 
@@ -634,7 +659,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
         }
       }
       if (RAW && !chan && pt - PD / 2 < T) {  // the third warp: the rows' beta
-        bf16 *rb = const_cast<bf16 *>(rec) + (pt - PD / 2) * R::kStride + R::kB;
+        bf16 *rb = const_cast<bf16 *>(rec) + R::kB + (pt - PD / 2);
         *rb = __float2bfloat16_rn(beta_of_logit(__bfloat162float(*rb)));
       }
       unsafe = named_or(kPrepBar, kPrepThreads, unsafe);
@@ -712,7 +737,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
         const int ti = pt >> 3, ui = pt & 7;
         const bool ent = pt < PT * PT;
         auto beta_of = [&](int t) {
-          return t < T ? __bfloat162float(rec[t * R::kStride + R::kB]) : 0.f;
+          return t < T ? __bfloat162float(rec[R::kB + t]) : 0.f;
         };
         if (ent) sl[pt] = (ui < ti && ti < T) ? beta_of(ti) * am[ti * PT + ui] : 0.f;
         named_sync(kPrepBar, kPrepThreads);
@@ -802,7 +827,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
               *reinterpret_cast<const uint4 *>(rec + t * R::kStride + off + ch * 8);
         }
         if (at < m.T)
-          reinterpret_cast<bf16 *>(p.rb)[unit * p.depth + at] = rec[at * R::kStride + R::kB];
+          reinterpret_cast<bf16 *>(p.rb)[unit * p.depth + at] = rec[R::kB + at];
       }
       if (pt == 0) {
         int32_t *c = p.ctrl + unit * 2;
@@ -889,7 +914,9 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
       // ordinary decode (or materialize): apply and commit
       float o0 = 0.f, o1 = 0.f;
       for (int t = 0; t < m.T; ++t) {
-        kda_step<PD, true, bf16>(S, rec + t * R::kStride, rg, j0, o0, o1);
+        kda_step_ptrs<PD, true, bf16>(S, rec + R::kK + t * PD, rec + R::kA + t * PD,
+                                      rec + R::kQ + t * PD, rec + R::kV + t * PD,
+                                      rec + R::kB + t, rg, j0, o0, o1);
         if (rg == 0)
           *reinterpret_cast<float2 *>(p.o + ((size_t)(m.tok0 + t) * H + h) * PD + j0) =
               make_float2(o0, o1);
@@ -935,7 +962,8 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
 
 template <bool RAW>
 __global__ void __launch_bounds__(kPipeThreads, 1)
-    verify_pipe_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap smap) {
+    verify_pipe_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap smap,
+                       const __grid_constant__ TokMaps tmaps) {
   typedef PipeLayout L;
   extern __shared__ float4 smem4[];
   unsigned char *smb = reinterpret_cast<unsigned char *>(
@@ -1003,7 +1031,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int limit = p.spin_limit;
-  if (warp == kProducerWarp) producer(p, &smap, smb, lane, limit);
+  if (warp == kProducerWarp) producer(p, &smap, &tmaps, smb, lane, limit);
   else if (warp >= kPrepWarp0) prep<RAW>(p, smb, tid - 32 * kPrepWarp0, limit);
   else consumer<RAW>(p, smb, tid, limit);
   __syncthreads();
@@ -1045,6 +1073,22 @@ cudaError_t state_map(CUtensorMap *tm, float *pool, int P, int H) {
   const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, gdim, gstride, box,
                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Packed bf16 tokens [N][H][PD] as a 3-D tensor map, boxes of PD channels x 1
+// head x PT tokens, zero fill past N.
+cudaError_t token_map(CUtensorMap *tm, const void *base, int N, int H) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[3] = {(cuuint64_t)PD, (cuuint64_t)H, (cuuint64_t)N};
+  const cuuint64_t gstride[2] = {(cuuint64_t)PD * 2, (cuuint64_t)H * PD * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)PD, 1, (cuuint32_t)PT};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                         gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 }  // namespace
@@ -1093,10 +1137,19 @@ cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   CUtensorMap smap;
-  const cudaError_t e = state_map(&smap, p.pool, p.P, p.H);
+  cudaError_t e = state_map(&smap, p.pool, p.P, p.H);
   if (e != cudaSuccess) return e;
+  TokMaps tmaps;
+  memset(&tmaps, 0, sizeof(tmaps));  // materialize: no tokens, never read
+  if (p.mode == 0 && p.N > 0) {
+    e = token_map(&tmaps.k, p.k, p.N, p.H);
+    if (e == cudaSuccess) e = token_map(&tmaps.a, p.alpha, p.N, p.H);
+    if (e == cudaSuccess) e = token_map(&tmaps.q, p.q, p.N, p.H);
+    if (e == cudaSuccess) e = token_map(&tmaps.v, p.v, p.N, p.H);
+    if (e != cudaSuccess) return e;
+  }
   return cudaLaunchKernelEx(&cfg, p.raw ? verify_pipe_kernel<true> : verify_pipe_kernel<false>,
-                            p, smap);
+                            p, smap, tmaps);
 }
 
 }  // namespace kda
