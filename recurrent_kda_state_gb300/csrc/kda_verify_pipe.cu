@@ -99,6 +99,8 @@ struct R {
 // PD channels x 1 head x PT tokens (rows past N read as zeros).
 struct TokMaps {
   CUtensorMap k, a, q, v;
+  CUtensorMap rk, ra, rv;  // the ring payload [P * H][depth][PD], boxes of depth entries
+  int tok_rows, ring_rows;  // box heights: min(PT, N) tokens, depth (<= 8) entries
 };
 
 // Per-unit facts the producer hands to the other roles.
@@ -132,10 +134,12 @@ struct PipeLayout {
   //   n     N = B M [PT][PT] fp32; meta (complete).  Once the pair
   //         products are taken, the K~ fragments' region holds the small
   //         matrices that give M.
+  // (the TMA boxes' destinations -- the four token fields, rv and both
+  // halves of rk -- start on 128-byte boundaries)
   static constexpr int kTsRec = 0;
-  static constexpr int kTsRv = kTsRec + R::kBytes;
+  static constexpr int kTsRv = (kTsRec + R::kBytes + 127) & ~127;
   static constexpr int kTsRb = kTsRv + kDepthMax * PD * 2;
-  static constexpr int kTsRk = kTsRb + 16;
+  static constexpr int kTsRk = (kTsRb + 16 + 127) & ~127;
   static constexpr int kTsFrag = kTsRk + 2 * kDepthMax * PD * 2;
   static constexpr int kTsAm = kTsFrag + 3 * 8 * 32 * 16;
   static constexpr int kTsBm = kTsAm + PT * PT * 4;
@@ -158,6 +162,14 @@ static_assert(PipeLayout::kTotal <= 227 * 1024, "verify pipeline shared memory")
 static_assert(R::kBytes % 16 == 0, "records must keep 16-byte alignment");
 static_assert(PipeLayout::kTsRk % 16 == 0 && PipeLayout::kTsFrag % 16 == 0,
               "token stage parts must keep 16-byte alignment");
+static_assert(PipeLayout::kTStages0 % 128 == 0 && PipeLayout::kTStage % 128 == 0 &&
+                  (PipeLayout::kTsRec + R::kA * 2) % 128 == 0 &&
+                  (PipeLayout::kTsRec + R::kQ * 2) % 128 == 0 &&
+                  (PipeLayout::kTsRec + R::kV * 2) % 128 == 0 &&
+                  PipeLayout::kTsRv % 128 == 0 && PipeLayout::kTsRk % 128 == 0 &&
+                  (PipeLayout::kTsRk + kDepthMax * PD * 2) % 128 == 0 &&
+                  PipeLayout::kSStage % 1024 == 0 && PipeLayout::kTStages0 % 1024 == 0,
+              "TMA destinations: 128-byte boundaries (1024 for the swizzled state)");
 
 struct Bars {
   uint64_t *sfull, *sempty, *tfull, *pfull, *tempty;
@@ -369,51 +381,68 @@ __device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsi
 // async copies spread over the lanes (each lane's copies arrive on the
 // stage's barrier when they land); the beta values and the meta by plain
 // stores, lane 0 arriving after them.
+// One TMA box of the map at (0, y, z) into shared memory, on `bar`.
+__device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap *map, int y, int z,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Unit n's token rows into token stage n % 3 (lane 0): one TMA box of PT
+// tokens per field, their bytes on the stage's barrier.  Rows past the
+// segment are other tokens or zeros and are never read.  Needs only the
+// unit's segment, so the first stages' rows go out before the ring words are
+// read.
+__device__ void issue_rows(const TokMaps *tmaps, unsigned char *smb, const Bars &bars, int n,
+                           int H, int lane) {
+  typedef PipeLayout L;
+  const int k = n % kTStages;
+  const UnitMeta m = meta_of(smb, n).m;
+  if (m.skip || m.T == 0 || lane != 0) return;
+  const int u = blockIdx.x + n * gridDim.x, h = u - (u / H) * H;
+  const uint32_t base = umma::smem_u32(smb + L::kTStages0 + k * L::kTStage);
+  const uint32_t bar = umma::smem_u32(&bars.tfull[k]);
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
+               :: "r"(bar), "r"(4 * tmaps->tok_rows * PD * 2) : "memory");
+  tma_box3(base + L::kTsRec + R::kK * 2, &tmaps->k, h, m.tok0, bar);
+  tma_box3(base + L::kTsRec + R::kA * 2, &tmaps->a, h, m.tok0, bar);
+  tma_box3(base + L::kTsRec + R::kQ * 2, &tmaps->q, h, m.tok0, bar);
+  tma_box3(base + L::kTsRec + R::kV * 2, &tmaps->v, h, m.tok0, bar);
+}
+
+// The rest of unit n's stage: (unless `rows_done`) its token rows, its
+// pending ring entries (k, alpha, v: one TMA box of the ring's depth entries
+// each), the beta values and the meta by plain
+// stores, lane 0 arriving after them.
 __device__ void issue_tokens(const VerifyParams &p, const TokMaps *tmaps, unsigned char *smb,
-                             const Bars &bars, int n, int lane) {
+                             const Bars &bars, int n, int lane, bool rows_done) {
   typedef PipeLayout L;
   const int k = n % kTStages;
   unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
   const MetaEnt &e = meta_of(smb, n);
   const UnitMeta m = e.m;
+  if (!rows_done) issue_rows(tmaps, smb, bars, n, p.H, lane);
   if (!m.skip) {
     const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
-    const size_t unit = (size_t)m.slot * p.H + h;
-    const uint32_t base = umma::smem_u32(ts);
-    if (m.T > 0 && lane == 0) {
-      // the rows: one TMA box of PT tokens per field (rows past the segment
-      // are other tokens or zeros and are never read), their bytes on the
-      // stage's barrier
+    const int unit = m.slot * p.H + h;
+    if (m.acc > 0 && lane == 0) {
+      const uint32_t base = umma::smem_u32(ts);
       const uint32_t bar = umma::smem_u32(&bars.tfull[k]);
       asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
-                   :: "r"(bar), "r"(4 * PT * PD * 2) : "memory");
-      const CUtensorMap *maps[4] = {&tmaps->k, &tmaps->a, &tmaps->q, &tmaps->v};
-      const int offs[4] = {R::kK, R::kA, R::kQ, R::kV};
-#pragma unroll
-      for (int f = 0; f < 4; ++f)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];"
-            :: "r"(base + L::kTsRec + offs[f] * 2), "l"(reinterpret_cast<uint64_t>(maps[f])),
-               "r"(0), "r"(h), "r"(m.tok0), "r"(bar)
-            : "memory");
-    }
-    // pending ring entries: k, alpha and v
-    for (int c = lane; c < m.acc * 48; c += 32) {
-      const int which = c / (16 * m.acc), r = c - which * 16 * m.acc;
-      const int q = r >> 4, c16 = r & 15;
-      const bf16 *src = reinterpret_cast<const bf16 *>(
-          which == 0 ? p.rk : which == 1 ? p.ra : p.rv);
-      const uint32_t dst = which == 2 ? L::kTsRv + q * PD * 2
-                                      : L::kTsRk + (which * kDepthMax + q) * PD * 2;
-      cp_async16(base + dst + c16 * 16, src + (unit * p.depth + q) * PD + c16 * 8);
+                   :: "r"(bar), "r"(3 * tmaps->ring_rows * PD * 2) : "memory");
+      tma_box3(base + L::kTsRk, &tmaps->rk, 0, unit, bar);
+      tma_box3(base + L::kTsRk + kDepthMax * PD * 2, &tmaps->ra, 0, unit, bar);
+      tma_box3(base + L::kTsRv, &tmaps->rv, 0, unit, bar);
     }
     if (lane < m.acc) reinterpret_cast<unsigned short *>(ts + L::kTsRb)[lane] = e.b[lane];
     if (lane >= 8 && lane < 8 + m.T)
       reinterpret_cast<unsigned short *>(ts + L::kTsRec)[R::kB + (lane - 8)] = e.b[lane];
   }
   if (lane == 0) *reinterpret_cast<UnitMeta *>(ts + L::kTsMeta) = m;
-  cp_async_arrive(&bars.tfull[k]);
+  cp_async_arrive(&bars.tfull[k]);  // this lane has no copies of its own in flight
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars.tfull[k]);
 }
@@ -449,10 +478,12 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
   // batches' words (units 0 and 1 were hinted into L2 before the wait)
   int ns = 0, nt = 0, fetched = 0;
   fetch_batch_a(p, smb, 0, cnt, lane);
+  const int early = cnt < kTStages ? cnt : kTStages;  // stages whose rows go out now
   if (cnt > 0) {
     issue_state(p, smap, smb, bars, 0, lane);
     s_last[0] = 0;
     ns = 1;
+    for (int n = 0; n < early; ++n) issue_rows(tmaps, smb, bars, n, p.H, lane);
   }
   fetch_batch_b(p, smb, 0, cnt, lane);
   fetched = cnt < kMetaBatch ? cnt : kMetaBatch;
@@ -462,7 +493,7 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
     bool did = false;
     if (nt < cnt && nt < fetched && (nt < kTStages ||
                                      use_done(&bars.tempty[nt % kTStages], nt / kTStages - 1))) {
-      issue_tokens(p, tmaps, smb, bars, nt, lane);
+      issue_tokens(p, tmaps, smb, bars, nt, lane, nt < early);
       t_last[nt % kTStages] = nt / kTStages;
       ++nt;
       did = true;
@@ -493,6 +524,13 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
     } else {
       __nanosleep(64);
     }
+  }
+  // stages whose rows went out early but whose tokens were not issued (the
+  // CTA stopped first) get the rest of their copies and arrivals, so that
+  // their barriers complete and can be drained
+  for (; nt < early; ++nt) {
+    issue_tokens(p, tmaps, smb, bars, nt, lane, true);
+    t_last[nt % kTStages] = nt / kTStages;
   }
   // copies still in flight land before the CTA may exit (normally the
   // consumers have already waited for them)
@@ -1077,13 +1115,29 @@ cudaError_t state_map(CUtensorMap *tm, float *pool, int P, int H) {
 }
 
 // Packed bf16 tokens [N][H][PD] as a 3-D tensor map, boxes of PD channels x 1
-// head x PT tokens, zero fill past N.
+// head x min(PT, N) tokens, zero fill past N.
 cudaError_t token_map(CUtensorMap *tm, const void *base, int N, int H) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t gdim[3] = {(cuuint64_t)PD, (cuuint64_t)H, (cuuint64_t)N};
   const cuuint64_t gstride[2] = {(cuuint64_t)PD * 2, (cuuint64_t)H * PD * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)PD, 1, (cuuint32_t)PT};
+  const cuuint32_t box[3] = {(cuuint32_t)PD, 1, (cuuint32_t)(N < PT ? N : PT)};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                         gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// A ring payload array [units][depth][PD] (bf16) as a 3-D tensor map, boxes
+// of PD channels x depth entries x 1 unit.
+cudaError_t ring_map(CUtensorMap *tm, const void *base, int depth, int units) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[3] = {(cuuint64_t)PD, (cuuint64_t)depth, (cuuint64_t)units};
+  const cuuint64_t gstride[2] = {(cuuint64_t)PD * 2, (cuuint64_t)depth * PD * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)PD, (cuuint32_t)depth, 1};
   const cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
                          gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1141,6 +1195,12 @@ cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   TokMaps tmaps;
   memset(&tmaps, 0, sizeof(tmaps));  // materialize: no tokens, never read
+  tmaps.ring_rows = p.depth;
+  tmaps.tok_rows = p.N < PT ? p.N : PT;
+  e = ring_map(&tmaps.rk, p.rk, p.depth, p.P * p.H);
+  if (e == cudaSuccess) e = ring_map(&tmaps.ra, p.ra, p.depth, p.P * p.H);
+  if (e == cudaSuccess) e = ring_map(&tmaps.rv, p.rv, p.depth, p.P * p.H);
+  if (e != cudaSuccess) return e;
   if (p.mode == 0 && p.N > 0) {
     e = token_map(&tmaps.k, p.k, p.N, p.H);
     if (e == cudaSuccess) e = token_map(&tmaps.a, p.alpha, p.N, p.H);
