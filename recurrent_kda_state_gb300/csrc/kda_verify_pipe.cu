@@ -75,6 +75,7 @@ constexpr int kDepthMax = 8;            // ring entries a stage holds
 constexpr int kConsumerWarps = 8;       // 2 * PD threads: the state owners
 constexpr int kProducerWarp = 8;
 constexpr int kPrepWarp0 = 9, kPrepWarps = 3, kPrepThreads = 32 * kPrepWarps;
+constexpr int kPrepMath = 64;           // the two channel-pair prep warps; the third appends
 constexpr int kPipeThreads = 32 * (kConsumerWarps + 1 + kPrepWarps);
 constexpr int kPrepBar = 1;             // named barrier of the prep warps
 constexpr int kPrepChanBar = 2;         // ... of the two channel-pair prep warps
@@ -381,6 +382,37 @@ __device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsi
 // async copies spread over the lanes (each lane's copies arrive on the
 // stage's barrier when they land); the beta values and the meta by plain
 // stores, lane 0 arriving after them.
+// L2 hint for a box of the map at (0, y, z); nothing lands in shared memory.
+__device__ __forceinline__ void tma_prefetch_box3(const CUtensorMap *map, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z) : "memory");
+}
+
+// L2 hints for the token rows and pending ring entries of units b0 .. b0 +
+// 31 (one unit per lane), issued as soon as their words are read: the rows'
+// box loads, issued a stage later, then find them in L2 instead of queueing
+// behind the state streams in DRAM.
+__device__ void prefetch_units(const VerifyParams &p, const TokMaps *tmaps, unsigned char *smb,
+                               int b0, int cnt, int lane) {
+  const int n = b0 + lane;
+  if (n >= cnt) return;
+  const UnitMeta m = meta_of(smb, n).m;
+  if (m.skip) return;
+  const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
+  if (m.T > 0) {
+    tma_prefetch_box3(&tmaps->k, h, m.tok0);
+    tma_prefetch_box3(&tmaps->a, h, m.tok0);
+    tma_prefetch_box3(&tmaps->q, h, m.tok0);
+    tma_prefetch_box3(&tmaps->v, h, m.tok0);
+  }
+  if (m.acc > 0) {
+    const int unit = m.slot * p.H + h;
+    tma_prefetch_box3(&tmaps->rk, 0, unit);
+    tma_prefetch_box3(&tmaps->ra, 0, unit);
+    tma_prefetch_box3(&tmaps->rv, 0, unit);
+  }
+}
+
 // One TMA box of the map at (0, y, z) into shared memory, on `bar`.
 __device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap *map, int y, int z,
                                          uint32_t bar) {
@@ -487,6 +519,7 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
   }
   fetch_batch_b(p, smb, 0, cnt, lane);
   fetched = cnt < kMetaBatch ? cnt : kMetaBatch;
+  prefetch_units(p, tmaps, smb, 0, cnt, lane);
   int idle = 0;
   while (ns < cnt || nt < cnt) {
     if (stopping(abort_flag)) break;
@@ -510,6 +543,7 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
     // the meta ring
     if (fetched < cnt && (ns < nt ? ns : nt) >= fetched - kMetaBatch) {
       fetch_batch(p, smb, fetched, cnt, lane);
+      prefetch_units(p, tmaps, smb, fetched, cnt, lane);
       fetched = fetched + kMetaBatch < cnt ? fetched + kMetaBatch : cnt;
       did = true;
     }
@@ -577,10 +611,10 @@ __device__ __forceinline__ float2 round_pair(float2 x, bf16 *dst) {
   return __bfloat1622float2(r);
 }
 
-// Rows of a unit with no drafts (ordinary decode): warp w prepares rows
-// w, w + 3, ...; lane l holds channel pairs l and l + 32.
+// Rows of a unit with no drafts (ordinary decode): prep math warp w
+// prepares rows w, w + 2, ...; lane l holds channel pairs l and l + 32.
 __device__ __forceinline__ void prep_raw_rows(bf16 *rec, int T, int w, int lane) {
-  for (int t = w; t < T; t += kPrepWarps) {
+  for (int t = w; t < T; t += kPrepMath / 32) {
     bf16 *r = rec + t * R::kStride;
     const int c0 = 2 * lane, c1 = 2 * lane + PD / 2;
     const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(r + R::kK + c0));
@@ -597,6 +631,48 @@ __device__ __forceinline__ void prep_raw_rows(bf16 *rec, int T, int w, int lane)
   }
 }
 
+// The third prep warp appends each unit's drafted inputs to the ring once
+// the unit's products are handed over (pfull), outside the other two prep
+// warps' barriers, so they start the next unit at once.
+__device__ void ring_append(const VerifyParams &p, unsigned char *smb, int lane, int limit) {
+  typedef PipeLayout L;
+  const Bars bars(smb);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
+  const int units = p.B * p.H, G = gridDim.x;
+  const int cnt = (int)blockIdx.x < units ? (units - (int)blockIdx.x + G - 1) / G : 0;
+  for (int n = 0; n < cnt; ++n) {
+    const int k = n % kTStages;
+    if (stopping(abort_flag)) break;
+    if (!pipe_wait(&bars.pfull[k], n / kTStages, limit, abort_flag, p.err)) break;
+    unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
+    const UnitMeta m = *reinterpret_cast<const UnitMeta *>(ts + L::kTsMeta);
+    if (!m.skip && m.spec && m.T > 0) {
+      // entries 0..T-1 <- the drafted inputs (k, alpha, v, beta); this
+      // unit's pending entries were copied out with the stage
+      const int u = blockIdx.x + n * G, h = u - (u / p.H) * p.H;
+      const size_t unit = (size_t)m.slot * p.H + h;
+      const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
+      bf16 *wk = reinterpret_cast<bf16 *>(p.rk) + unit * p.depth * PD;
+      bf16 *wa = reinterpret_cast<bf16 *>(p.ra) + unit * p.depth * PD;
+      bf16 *wvr = reinterpret_cast<bf16 *>(p.rv) + unit * p.depth * PD;
+      constexpr int CH = PD / 8;  // 16-byte chunks per vector
+      for (int idx = lane; idx < m.T * 3 * CH; idx += 32) {
+        const int t = idx / (3 * CH), r = idx - t * 3 * CH;
+        const int which = r / CH, ch = r - which * CH;
+        const int off = which == 0 ? R::kK : which == 1 ? R::kA : R::kV;
+        bf16 *dst = (which == 0 ? wk : which == 1 ? wa : wvr) + (size_t)t * PD + ch * 8;
+        *reinterpret_cast<uint4 *>(dst) =
+            *reinterpret_cast<const uint4 *>(rec + t * R::kStride + off + ch * 8);
+      }
+      if (lane < m.T)
+        reinterpret_cast<bf16 *>(p.rb)[unit * p.depth + lane] = rec[R::kB + lane];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.tempty[k]);
+  }
+}
+
+// The drafts' operands, by the two channel-pair prep warps (pt < 64).
 template <bool RAW>
 __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limit) {
   typedef PipeLayout L;
@@ -610,13 +686,13 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
     // both prep warps take the same decision before any named barrier
     bool go = !stopping(abort_flag);
     if (go) go = pipe_wait(&bars.tfull[k], n / kTStages, limit, abort_flag, p.err);
-    if (!named_and(kPrepBar, kPrepThreads, go)) break;
+    if (!named_and(kPrepBar, kPrepMath, go)) break;
     unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
     const UnitMeta m = *reinterpret_cast<const UnitMeta *>(ts + L::kTsMeta);
     const bool drafts = !m.skip && m.spec && m.T > 0;
     if (RAW && !m.skip && !drafts && m.T > 0) {  // drafts: prepared in the first phase
       prep_raw_rows(reinterpret_cast<bf16 *>(ts + L::kTsRec), m.T, pt >> 5, lane);
-      named_sync(kPrepBar, kPrepThreads);
+      named_sync(kPrepBar, kPrepMath);
     }
     if (drafts) {
       const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
@@ -643,7 +719,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
       };
       int unsafe = 0;
       float2 kt[PT], qt[PT];
-      const bool chan = pt < PD / 2;  // threads of a channel pair; the rest append the ring
+      const bool chan = pt < PD / 2;  // every math thread holds a channel pair
       if (chan) {
         // every load first (the stores below could alias them for the
         // compiler), then gamma, K~, Q~, K^ and their fragments
@@ -696,11 +772,11 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           put(2, t, kh.x, kh.y);
         }
       }
-      if (RAW && !chan && pt - PD / 2 < T) {  // the third warp: the rows' beta
-        bf16 *rb = const_cast<bf16 *>(rec) + R::kB + (pt - PD / 2);
+      if (RAW && pt < T) {  // the rows' beta
+        bf16 *rb = const_cast<bf16 *>(rec) + R::kB + pt;
         *rb = __float2bfloat16_rn(beta_of_logit(__bfloat162float(*rb)));
       }
-      unsafe = named_or(kPrepBar, kPrepThreads, unsafe);
+      unsafe = named_or(kPrepBar, kPrepMath, unsafe);
       if (!unsafe) {
         // the pair products on the tensor cores, one prep warp each:
         // D row s, column t = K^_s . K~_t (warp 0: A) or K^_s . Q~_t (B)
@@ -732,7 +808,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
         // k_sc prod_{s<w<=t} alpha_wc (s < t) and B_ts with q_t (s <= t);
         // 4 lanes per pair, a quarter of the channels each
         const int nb = T * (T + 1) / 2, npairs = T * T, rg = pt & 3;
-        for (int base = 0; base < npairs * 4; base += kPrepThreads) {
+        for (int base = 0; base < npairs * 4; base += kPrepMath) {
           const int pair = (base + pt) >> 2;
           float acc = 0.f;
           int t = 0, sI = 0;
@@ -762,7 +838,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           }
         }
       }
-      named_sync(kPrepBar, kPrepThreads);
+      named_sync(kPrepBar, kPrepMath);
       // M = (I + L)^-1 diag(beta) with L = diag(beta) A strictly lower (the
       // drafts' corrections are delta = M (v - S^T K~)), and N = B M, so that
       // o = S^T Q~ + N (v - S^T K~).  L is nilpotent (L^8 = 0), so
@@ -778,7 +854,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           return t < T ? __bfloat162float(rec[R::kB + t]) : 0.f;
         };
         if (ent) sl[pt] = (ui < ti && ti < T) ? beta_of(ti) * am[ti * PT + ui] : 0.f;
-        named_sync(kPrepBar, kPrepThreads);
+        named_sync(kPrepBar, kPrepMath);
         auto row_col = [&](const float *a, const float *b) {  // (a b)[ti][ui]
           float x[PT], y[PT], acc = 0.f;
 #pragma unroll
@@ -788,7 +864,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           return acc;
         };
         if (ent) sl2[pt] = row_col(sl, sl);
-        named_sync(kPrepBar, kPrepThreads);
+        named_sync(kPrepBar, kPrepMath);
         if (ent) {
           const float l = sl[pt], l2 = sl2[pt];
           const float x = (ti == ui ? 1.f : 0.f) - l + l2 - row_col(sl, sl2);  // (I - L)(I + L^2)
@@ -796,9 +872,9 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           sx[pt] = x;
           sl4[pt] = l4;
         }
-        named_sync(kPrepBar, kPrepThreads);
+        named_sync(kPrepBar, kPrepMath);
         if (ent) smm[pt] = (sx[pt] + row_col(sx, sl4)) * beta_of(ui);  // X (I + L^4) diag(beta)
-        named_sync(kPrepBar, kPrepThreads);
+        named_sync(kPrepBar, kPrepMath);
         if (ent) {
           // N = B M with B masked to s <= t < T
           float x[PT], y[PT], acc = 0.f;
@@ -812,7 +888,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           nm[pt] = acc;
         }
       }
-      named_sync(kPrepBar, kPrepThreads);
+      named_sync(kPrepBar, kPrepMath);
       // Q^ = Q~ - N K~ (fragments, over Q~'s) and W = N v (fp32, over K^'s):
       // o_t = (S^T Q^)_t + W_t
       float *wv = reinterpret_cast<float *>(fragb + 2 * 4096);
@@ -844,34 +920,11 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
       }
     }
     mbar_arrive(&bars.pfull[k]);
-    if (!m.skip) {
+    if (!m.skip && pt == 0) {
       const size_t unit = (size_t)m.slot * p.H + h;
-      if (drafts && pt >= PD / 2) {
-        // ring append by the third prep warp, after the stage's products are
-        // handed over: entries 0..T-1 <- the drafted inputs (k, alpha, v,
-        // beta); this unit's pending entries were copied out with the stage
-        const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
-        const int at = pt - PD / 2, nat = kPrepThreads - PD / 2;
-        bf16 *wk = reinterpret_cast<bf16 *>(p.rk) + unit * p.depth * PD;
-        bf16 *wa = reinterpret_cast<bf16 *>(p.ra) + unit * p.depth * PD;
-        bf16 *wvr = reinterpret_cast<bf16 *>(p.rv) + unit * p.depth * PD;
-        constexpr int CH = PD / 8;  // 16-byte chunks per vector
-        for (int idx = at; idx < m.T * 3 * CH; idx += nat) {
-          const int t = idx / (3 * CH), r = idx - t * 3 * CH;
-          const int which = r / CH, ch = r - which * CH;
-          const int off = which == 0 ? R::kK : which == 1 ? R::kA : R::kV;
-          bf16 *dst = (which == 0 ? wk : which == 1 ? wa : wvr) + (size_t)t * PD + ch * 8;
-          *reinterpret_cast<uint4 *>(dst) =
-              *reinterpret_cast<const uint4 *>(rec + t * R::kStride + off + ch * 8);
-        }
-        if (at < m.T)
-          reinterpret_cast<bf16 *>(p.rb)[unit * p.depth + at] = rec[R::kB + at];
-      }
-      if (pt == 0) {
-        int32_t *c = p.ctrl + unit * 2;
-        c[0] = drafts ? m.T : 0;
-        c[1] = 0;
-      }
+      int32_t *c = p.ctrl + unit * 2;
+      c[0] = drafts ? m.T : 0;
+      c[1] = 0;
     }
     // this warp is done with the stage
     __syncwarp();
@@ -1016,7 +1069,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     }
     for (int i = 0; i < kTStages; ++i) {
       umma::mbar_init(&b.tfull[i], 32 + 1);  // async arrivals of the lanes + lane 0
-      umma::mbar_init(&b.pfull[i], kPrepThreads);
+      umma::mbar_init(&b.pfull[i], kPrepMath);
       umma::mbar_init(&b.tempty[i], kConsumerWarps + kPrepWarps);
     }
     *reinterpret_cast<volatile int *>(smb + L::kAbort) = 0;
@@ -1070,6 +1123,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int limit = p.spin_limit;
   if (warp == kProducerWarp) producer(p, &smap, &tmaps, smb, lane, limit);
+  else if (warp >= kPrepWarp0 + kPrepMath / 32) ring_append(p, smb, lane, limit);
   else if (warp >= kPrepWarp0) prep<RAW>(p, smb, tid - 32 * kPrepWarp0, limit);
   else consumer<RAW>(p, smb, tid, limit);
   __syncthreads();
