@@ -382,37 +382,6 @@ __device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsi
 // async copies spread over the lanes (each lane's copies arrive on the
 // stage's barrier when they land); the beta values and the meta by plain
 // stores, lane 0 arriving after them.
-// L2 hint for a box of the map at (0, y, z); nothing lands in shared memory.
-__device__ __forceinline__ void tma_prefetch_box3(const CUtensorMap *map, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z) : "memory");
-}
-
-// L2 hints for the token rows and pending ring entries of units b0 .. b0 +
-// 31 (one unit per lane), issued as soon as their words are read: the rows'
-// box loads, issued a stage later, then find them in L2 instead of queueing
-// behind the state streams in DRAM.
-__device__ void prefetch_units(const VerifyParams &p, const TokMaps *tmaps, unsigned char *smb,
-                               int b0, int cnt, int lane) {
-  const int n = b0 + lane;
-  if (n >= cnt) return;
-  const UnitMeta m = meta_of(smb, n).m;
-  if (m.skip) return;
-  const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
-  if (m.T > 0) {
-    tma_prefetch_box3(&tmaps->k, h, m.tok0);
-    tma_prefetch_box3(&tmaps->a, h, m.tok0);
-    tma_prefetch_box3(&tmaps->q, h, m.tok0);
-    tma_prefetch_box3(&tmaps->v, h, m.tok0);
-  }
-  if (m.acc > 0) {
-    const int unit = m.slot * p.H + h;
-    tma_prefetch_box3(&tmaps->rk, 0, unit);
-    tma_prefetch_box3(&tmaps->ra, 0, unit);
-    tma_prefetch_box3(&tmaps->rv, 0, unit);
-  }
-}
-
 // One TMA box of the map at (0, y, z) into shared memory, on `bar`.
 __device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap *map, int y, int z,
                                          uint32_t bar) {
@@ -519,7 +488,6 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
   }
   fetch_batch_b(p, smb, 0, cnt, lane);
   fetched = cnt < kMetaBatch ? cnt : kMetaBatch;
-  prefetch_units(p, tmaps, smb, 0, cnt, lane);
   int idle = 0;
   while (ns < cnt || nt < cnt) {
     if (stopping(abort_flag)) break;
@@ -543,7 +511,6 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
     // the meta ring
     if (fetched < cnt && (ns < nt ? ns : nt) >= fetched - kMetaBatch) {
       fetch_batch(p, smb, fetched, cnt, lane);
-      prefetch_units(p, tmaps, smb, fetched, cnt, lane);
       fetched = fetched + kMetaBatch < cnt ? fetched + kMetaBatch : cnt;
       did = true;
     }
