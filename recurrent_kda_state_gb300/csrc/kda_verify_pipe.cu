@@ -13,18 +13,21 @@
 //
 //   producer (1 warp): the units' slot, segment, ring word and beta values
 //       for 32 units at a time (one unit per lane); then per unit its 64 KiB
-//       state with four bulk copies into one of two state stages (two units
-//       ahead of the consumers), its tokens (k, alpha, v, q rows) and pending
-//       ring entries (k, alpha, v) with per-lane 16-byte async copies into
-//       one of three token stages, each copy as soon as its stage is free,
-//       and an L2 hint for the next unit's state;
-//   prep (3 warps): as soon as a unit's token stage lands, for drafts: the decay
-//       products gamma_t, K~ = gamma k, Q~ = gamma q, K^ = k / gamma, the
-//       T x T pair products A = K^ K~^T, B = K^ Q~^T on the tensor cores, the
-//       small triangular inverse M = (I + diag(beta) A)^-1 diag(beta) and
-//       N = B M, then Q^ = Q~ - N K~ (as bf16 hi/lo MMA fragments) and
-//       W = N v; the drafted inputs appended to the unit's ring and its
-//       control word set;
+//       state as four 128-byte-swizzled TMA boxes through a tensor map of
+//       the pool into one of two state stages (two units ahead of the
+//       consumers), its token rows as four TMA boxes (k, alpha, q, v: 8
+//       tokens x 128 channels) and its pending ring entries as three TMA
+//       boxes into one of three token stages, each as soon as its stage is
+//       free (the first three stages' rows as soon as the segments are
+//       known), and an L2 hint for the next unit's state;
+//   prep (2 warps): as soon as a unit's token stage lands, for drafts: the
+//       decay products gamma_t, K~ = gamma k, Q~ = gamma q, K^ = k / gamma,
+//       the T x T pair products A = K^ K~^T, B = K^ Q~^T on the tensor cores,
+//       N = B (I + diag(beta) A)^-1 diag(beta) by back substitution, then
+//       Q^ = Q~ - N K~ (as bf16 hi/lo MMA fragments) and W = N v, and the
+//       unit's control word;
+//   ring append (1 warp): after each unit's hand-off, its drafted inputs
+//       into the unit's ring, outside the prep warps' barriers;
 //   consumers (8 warps): the state from its stage into registers (the stage
 //       is released at once), the replay as soon as the token stage lands
 //       (while the prep still works on it), the state store, and once the
@@ -74,7 +77,7 @@ constexpr int PT = 8;                   // drafted rows per MMA tile (T <= 8)
 constexpr int kDepthMax = 8;            // ring entries a stage holds
 constexpr int kConsumerWarps = 8;       // 2 * PD threads: the state owners
 constexpr int kProducerWarp = 8;
-constexpr int kPrepWarp0 = 9, kPrepWarps = 3, kPrepThreads = 32 * kPrepWarps;
+constexpr int kPrepWarp0 = 9, kPrepWarps = 3;
 constexpr int kPrepMath = 64;           // the two channel-pair prep warps; the third appends
 constexpr int kPipeThreads = 32 * (kConsumerWarps + 1 + kPrepWarps);
 constexpr int kPrepBar = 1;             // named barrier of the prep warps
@@ -194,11 +197,8 @@ __device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes) {
       "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
       :: "r"(umma::smem_u32(bar)), "r"(bytes) : "memory");
 }
-// 16 bytes global -> shared without registers; this thread's copies so far
-// arrive on an mbarrier (counted in its expected arrivals) once they land.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
-}
+// This thread's cp.async copies so far (none, in this kernel) arrive on an
+// mbarrier (counted in its expected arrivals) once they land.
 __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
                :: "r"(umma::smem_u32(bar)) : "memory");
@@ -806,54 +806,34 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
         }
       }
       named_sync(kPrepBar, kPrepMath);
-      // M = (I + L)^-1 diag(beta) with L = diag(beta) A strictly lower (the
-      // drafts' corrections are delta = M (v - S^T K~)), and N = B M, so that
-      // o = S^T Q~ + N (v - S^T K~).  L is nilpotent (L^8 = 0), so
-      // (I + L)^-1 = (I - L)(I + L^2)(I + L^4) exactly: five rounds of 8 x 8
-      // products, thread pt < 64 taking entry (pt / 8, pt % 8) of each.
-      {
-        float *sl = reinterpret_cast<float *>(fragb);  // K~ fragments are spent
-        float *sl2 = sl + PT * PT, *sl4 = sl2 + PT * PT, *sx = sl4 + PT * PT,
-              *smm = sx + PT * PT;
-        const int ti = pt >> 3, ui = pt & 7;
-        const bool ent = pt < PT * PT;
-        auto beta_of = [&](int t) {
-          return t < T ? __bfloat162float(rec[R::kB + t]) : 0.f;
-        };
-        if (ent) sl[pt] = (ui < ti && ti < T) ? beta_of(ti) * am[ti * PT + ui] : 0.f;
-        named_sync(kPrepBar, kPrepMath);
-        auto row_col = [&](const float *a, const float *b) {  // (a b)[ti][ui]
-          float x[PT], y[PT], acc = 0.f;
+      // N = B M with M = (I + L)^-1 diag(beta), L = diag(beta) A strictly
+      // lower (the drafts' corrections are delta = M (v - S^T K~), so that
+      // o = S^T Q~ + N (v - S^T K~)).  Row r of Y = B (I + L)^-1 solves
+      // Y (I + L) = B: Y[r][s] = B[r][s] - sum_{t > s} Y[r][t] L[t][s], by
+      // back substitution over the columns s = 7 .. 0, one thread per row and
+      // no barrier inside; then N = Y diag(beta).
+      if (pt < PT) {
+        const int r = pt;
+        // every load first: beta, L's strict lower triangle, B's row r
+        float bt[PT], lv[PT * (PT - 1) / 2], br[PT], y[PT];
 #pragma unroll
-          for (int q = 0; q < PT; ++q) { x[q] = a[ti * PT + q]; y[q] = b[q * PT + ui]; }
-#pragma unroll
-          for (int q = 0; q < PT; ++q) acc = fmaf(x[q], y[q], acc);
-          return acc;
-        };
-        if (ent) sl2[pt] = row_col(sl, sl);
-        named_sync(kPrepBar, kPrepMath);
-        if (ent) {
-          const float l = sl[pt], l2 = sl2[pt];
-          const float x = (ti == ui ? 1.f : 0.f) - l + l2 - row_col(sl, sl2);  // (I - L)(I + L^2)
-          const float l4 = row_col(sl2, sl2);
-          sx[pt] = x;
-          sl4[pt] = l4;
+        for (int q = 0; q < PT; ++q) {
+          bt[q] = q < T ? __bfloat162float(rec[R::kB + q]) : 0.f;
+          br[q] = (q <= r && r < T) ? bmat[r * PT + q] : 0.f;
         }
-        named_sync(kPrepBar, kPrepMath);
-        if (ent) smm[pt] = (sx[pt] + row_col(sx, sl4)) * beta_of(ui);  // X (I + L^4) diag(beta)
-        named_sync(kPrepBar, kPrepMath);
-        if (ent) {
-          // N = B M with B masked to s <= t < T
-          float x[PT], y[PT], acc = 0.f;
 #pragma unroll
-          for (int q = 0; q < PT; ++q) {
-            x[q] = (q <= ti && ti < T) ? bmat[ti * PT + q] : 0.f;
-            y[q] = smm[q * PT + ui];
-          }
+        for (int t = 1, i = 0; t < PT; ++t)
 #pragma unroll
-          for (int q = 0; q < PT; ++q) acc = fmaf(x[q], y[q], acc);
-          nm[pt] = acc;
+          for (int q = 0; q < t; ++q, ++i) lv[i] = t < T ? bt[t] * am[t * PT + q] : 0.f;
+#pragma unroll
+        for (int sc = PT - 1; sc >= 0; --sc) {
+          float acc = br[sc];
+#pragma unroll
+          for (int t = sc + 1; t < PT; ++t) acc = fmaf(-y[t], lv[t * (t - 1) / 2 + sc], acc);
+          y[sc] = acc;
         }
+#pragma unroll
+        for (int q = 0; q < PT; ++q) nm[r * PT + q] = y[q] * bt[q];
       }
       named_sync(kPrepBar, kPrepMath);
       // Q^ = Q~ - N K~ (fragments, over Q~'s) and W = N v (fp32, over K^'s):
