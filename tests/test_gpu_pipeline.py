@@ -178,3 +178,27 @@ def test_pipeline_device_errors_skip_units():
     got = np.concatenate([o[cu[i]:cu[i + 1]] for i in ok])
     assert_outputs(got, o_ref)
     assert_states(from_gpu_states(pool.data[6]), sess.pool[6])
+
+
+@pytest.mark.parametrize("lens,spec", [([3], [1]), ([2, 1], [1, 0]), ([1], [0])],
+                         ids=["one_row_3", "spec2_plus_decode1", "one_decode"])
+def test_pipeline_batch_shorter_than_a_token_box(lens, spec):
+    """Batches of fewer than 8 tokens (the token boxes shrink to the batch):
+    two verify + commit steps against the oracle and the per-unit kernel,
+    with pending ring entries replayed in the second step."""
+    H, P = 8, 5
+    rng = np.random.default_rng(5500 + sum(lens))
+    B = len(lens)
+    slots_np = ki.slot_table(rng, B, P)
+    init = (rng.standard_normal((P, H, 128, 128)) * 0.3).astype(np.float32)
+    sched = []
+    for _ in range(2):
+        tok = ki.round_to(ki.gen_tokens(rng, lens, H, 128), "bf16")
+        acc = np.array([rng.integers(0, n + 1) if s else 0 for n, s in zip(lens, spec)],
+                       dtype=np.int32)
+        sched.append((tok, np.array(spec, np.int32), acc))
+    s8, o8 = _run(slots_np, init, sched, 8, H, P)
+    s9, o9 = _run(slots_np, init, sched, 9, H, P, check_oracle=False)
+    assert torch.equal(s8, s9)
+    for a, b in zip(o8, o9):
+        assert_outputs(a, b)
