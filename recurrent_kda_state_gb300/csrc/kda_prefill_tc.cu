@@ -40,6 +40,7 @@
 // kda_umma.cuh); the TMEM accumulators sit at fixed columns.
 #include <cuda.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -331,6 +332,16 @@ __device__ __forceinline__ bool tiles_ready_and(bool ok) {
 struct InputMaps {
   CUtensorMap q, k, a, v, b;  // b: beta [N][H] as 2-D, boxes of 8 heads x 64 tokens
 };
+static_assert(offsetof(InputMaps, b) == offsetof(InputMaps, q) + 4 * sizeof(CUtensorMap),
+              "the five maps are consecutive");
+
+// Threads 32 .. 36 prefetch the five maps' descriptors, which a copy would
+// otherwise fetch at its first use.
+__device__ __forceinline__ void prefetch_input_maps(const InputMaps &maps, int tid) {
+  if (tid >= 32 && tid < 37)
+    asm volatile("prefetch.tensormap [%0];"
+                 :: "l"(reinterpret_cast<uint64_t>(&maps.q + (tid - 32))) : "memory");
+}
 
 // One TMA load of a 2-D box of `tm` at (x, token) into shared memory,
 // completing its bytes on the mbarrier's transaction count.
@@ -377,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *Xf = reinterpret_cast<float *>(sm + Lay::XF);
   uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + Lay::MBAR);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + Lay::TSLOT);
+  prefetch_input_maps(maps, threadIdx.x);
 
   const int tid = threadIdx.x, sl = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
   const int H = p.H, col0 = sl * kNC;
@@ -958,6 +970,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int total = reinterpret_cast<const int *>(p.ws)[p.B] * H;
   int it = blockIdx.x;
   if (it >= total) return;
+  prefetch_input_maps(maps, tid);
 
   if (tid < 32) umma::tmem_alloc(tslot, 256);
   if (tid == 0) {

@@ -13,13 +13,13 @@
 //
 //   producer (1 warp): the units' slot, segment, ring word and beta values
 //       for 32 units at a time (one unit per lane); then per unit its 64 KiB
-//       state as four 128-byte-swizzled TMA boxes through a tensor map of
-//       the pool into one of two state stages (two units ahead of the
-//       consumers), its token rows as four TMA boxes (k, alpha, q, v: 8
-//       tokens x 128 channels) and its pending ring entries as three TMA
-//       boxes into one of three token stages, each as soon as its stage is
-//       free (the first three stages' rows as soon as the segments are
-//       known), and an L2 hint for the next unit's state;
+//       state as one 128-byte-swizzled TMA box (four 16 KB blocks of 32 key
+//       channels) through a 3-D tensor map of the pool into one of two state
+//       stages (two units ahead of the consumers), its token rows as four
+//       TMA boxes (k, alpha, q, v: 8 tokens x 128 channels) and its pending
+//       ring entries as three TMA boxes into one of three token stages, each
+//       as soon as its stage is free (the first unit's rows as soon as its
+//       segment is known), and an L2 hint for the next unit's state;
 //   prep (2 warps): as soon as a unit's token stage lands, for drafts: the
 //       decay products gamma_t, K~ = gamma k, Q~ = gamma q, K^ = k / gamma,
 //       the T x T pair products A = K^ K~^T, B = K^ Q~^T on the tensor cores,
@@ -62,6 +62,7 @@
 // K^_s . X_t.
 #include <cuda.h>
 
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -106,6 +107,8 @@ struct TokMaps {
   CUtensorMap rk, ra, rv;  // the ring payload [P * H][depth][PD], boxes of depth entries
   int tok_rows, ring_rows;  // box heights: min(PT, N) tokens, depth (<= 8) entries
 };
+static_assert(offsetof(TokMaps, rv) == offsetof(TokMaps, k) + 6 * sizeof(CUtensorMap),
+              "the seven maps are consecutive");
 
 // Per-unit facts the producer hands to the other roles.
 struct UnitMeta {
@@ -121,7 +124,7 @@ static_assert(sizeof(MetaEnt) == 64, "meta ring entries are 64 bytes");
 
 // Shared-memory carve-up, byte offsets from a 1024-aligned base.
 struct PipeLayout {
-  // state stage: state [PD][PD] fp32 as four 16 KB boxes of 32 key channels
+  // state stage: state [PD][PD] fp32 as four 16 KB blocks of 32 key channels
   // x 128 value rows (row j = value column, 128 bytes, its 16-byte chunks
   // swizzled by j % 8: the TMA 128-byte swizzle), then the meta (slot and
   // whether the state was loaded); stages 1024-byte aligned for the swizzle
@@ -296,39 +299,66 @@ __device__ void fetch_batch_a(const VerifyParams &p, unsigned char *smb, int b0,
   __syncwarp();
 }
 
-// Round two: the ring word and the beta values the unit's stages need.
-__device__ void fetch_batch_b(const VerifyParams &p, unsigned char *smb, int b0, int cnt,
-                              int lane) {
+// Round two: the ring word and the beta values the unit's stages need, in
+// two halves, so that the loads can be in flight while the first copies are
+// issued (they would otherwise queue behind those copies' bytes).  The
+// loads, into the lane's registers:
+struct WordsB {
+  int2 c;
+  unsigned short bv[16];
+};
+__device__ __forceinline__ WordsB load_words_b(const VerifyParams &p, unsigned char *smb,
+                                               int b0, int cnt, int lane) {
+  typedef PipeLayout L;
+  WordsB w;
+  w.c = make_int2(0, 0);
+#pragma unroll
+  for (int q = 0; q < 16; ++q) w.bv[q] = 0;
+  const int n = b0 + lane;
+  if (n < cnt) {
+    const UnitMeta m = reinterpret_cast<const MetaEnt *>(smb + L::kMetas)[n % kMetaRing].m;
+    if (!m.skip) {
+      const int H = p.H, u = blockIdx.x + n * gridDim.x, h = u - (u / H) * H;
+      const size_t unit = (size_t)m.slot * H + h;
+      w.c = *reinterpret_cast<const int2 *>(p.ctrl + unit * 2);
+      const unsigned short *rb = reinterpret_cast<const unsigned short *>(p.rb) + unit * p.depth;
+      const unsigned short *tb = reinterpret_cast<const unsigned short *>(p.beta);
+#pragma unroll
+      for (int q = 0; q < kDepthMax; ++q) w.bv[q] = q < p.depth ? rb[q] : 0;
+#pragma unroll
+      for (int q = 0; q < PT; ++q)
+        w.bv[kDepthMax + q] = q < m.T ? tb[(size_t)(m.tok0 + q) * H + h] : 0;
+    }
+  }
+  return w;
+}
+// ... and their checks and placement in the unit's meta ring entry.
+__device__ __forceinline__ void place_words_b(const VerifyParams &p, unsigned char *smb, int b0,
+                                              int cnt, int lane, const WordsB &w) {
   typedef PipeLayout L;
   const int n = b0 + lane;
   if (n < cnt) {
     MetaEnt &e = reinterpret_cast<MetaEnt *>(smb + L::kMetas)[n % kMetaRing];
     UnitMeta &m = e.m;
     if (!m.skip) {
-      const int H = p.H, u = blockIdx.x + n * gridDim.x, h = u - (u / H) * H;
-      const size_t unit = (size_t)m.slot * H + h;
-      const int2 c = *reinterpret_cast<const int2 *>(p.ctrl + unit * 2);
-      const bool ok = c.x >= 0 && c.x <= p.depth && c.y >= 0 && c.y <= c.x;
-      const unsigned short *rb = reinterpret_cast<const unsigned short *>(p.rb) + unit * p.depth;
-      const unsigned short *tb = reinterpret_cast<const unsigned short *>(p.beta);
-      unsigned short bv[16];
+      const bool ok = w.c.x >= 0 && w.c.x <= p.depth && w.c.y >= 0 && w.c.y <= w.c.x;
 #pragma unroll
-      for (int q = 0; q < kDepthMax; ++q) bv[q] = q < p.depth ? rb[q] : 0;
-#pragma unroll
-      for (int q = 0; q < PT; ++q)
-        bv[kDepthMax + q] = q < m.T ? tb[(size_t)(m.tok0 + q) * H + h] : 0;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) e.b[q] = bv[q];
+      for (int q = 0; q < 16; ++q) e.b[q] = w.bv[q];
       if (!ok) {
         set_error(p.err, KDA_DERR_RING);
         m.skip = 1;
         m.T = 0;
       } else {
-        m.acc = c.y;
+        m.acc = w.c.y;
       }
     }
   }
   __syncwarp();
+}
+__device__ __forceinline__ void fetch_batch_b(const VerifyParams &p, unsigned char *smb, int b0,
+                                              int cnt, int lane) {
+  const WordsB w = load_words_b(p, smb, b0, cnt, lane);
+  place_words_b(p, smb, b0, cnt, lane, w);
 }
 
 __device__ __forceinline__ void fetch_batch(const VerifyParams &p, unsigned char *smb, int b0,
@@ -351,8 +381,8 @@ __device__ __forceinline__ void prefetch_state(const VerifyParams &p, unsigned c
   }
 }
 
-// Unit n's state into state stage n % 2: four 16 KiB bulk copies completing
-// on the stage's barrier, after the meta (lane 0's arrival).
+// Unit n's state into state stage n % 2: one 64 KiB tensor copy (lane 0)
+// completing on the stage's barrier, after the meta.
 __device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsigned char *smb,
                             const Bars &bars, int n, int lane) {
   typedef PipeLayout L;
@@ -361,21 +391,21 @@ __device__ void issue_state(const VerifyParams &p, const CUtensorMap *smap, unsi
   const UnitMeta m = meta_of(smb, n).m;
   if (lane == 0) {
     *reinterpret_cast<UnitMeta *>(ss + L::kSsMeta) = m;
-    if (m.skip) mbar_arrive(&bars.sfull[s]);
-    else mbar_arrive_tx(&bars.sfull[s], PD * PD * 4);
+    if (m.skip) {
+      mbar_arrive(&bars.sfull[s]);
+    } else {
+      mbar_arrive_tx(&bars.sfull[s], PD * PD * 4);
+      const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
+      const int row0 = (m.slot * p.H + h) * PD;  // the unit's first value row
+      asm volatile(
+          "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3, %4}], [%5];"
+          :: "r"(umma::smem_u32(ss + L::kSsState)), "l"(reinterpret_cast<uint64_t>(smap)),
+             "r"(0), "r"(row0), "r"(0), "r"(umma::smem_u32(&bars.sfull[s]))
+          : "memory");
+    }
   }
   __syncwarp();
-  if (!m.skip && lane < 4) {  // four 16 KiB boxes, one per lane
-    const int u = blockIdx.x + n * gridDim.x, h = u - (u / p.H) * p.H;
-    const int row0 = (m.slot * p.H + h) * PD;  // the unit's first value row
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];"
-        :: "r"(umma::smem_u32(ss + L::kSsState) + lane * (PD * 32 * 4)),
-           "l"(reinterpret_cast<uint64_t>(smap)), "r"(lane * 32), "r"(row0),
-           "r"(umma::smem_u32(&bars.sfull[s]))
-        : "memory");
-  }
 }
 
 // Unit n's tokens and pending ring entries into token stage n % 3: 16-byte
@@ -395,8 +425,8 @@ __device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap *map, i
 // Unit n's token rows into token stage n % 3 (lane 0): one TMA box of PT
 // tokens per field, their bytes on the stage's barrier.  Rows past the
 // segment are other tokens or zeros and are never read.  Needs only the
-// unit's segment, so the first stages' rows go out before the ring words are
-// read.
+// unit's segment, so the first unit's rows go out before the ring words are
+// placed.
 __device__ void issue_rows(const TokMaps *tmaps, unsigned char *smb, const Bars &bars, int n,
                            int H, int lane) {
   typedef PipeLayout L;
@@ -475,18 +505,23 @@ __device__ void producer(const VerifyParams &p, const CUtensorMap *smap, const T
   int s_last[kSStages], t_last[kTStages];  // last use issued of each stage
   for (int i = 0; i < kSStages; ++i) s_last[i] = -1;
   for (int i = 0; i < kTStages; ++i) t_last[i] = -1;
-  // the first unit's slot and at once its state; then the rest of the first
-  // batches' words (units 0 and 1 were hinted into L2 before the wait)
+  // the first batch's slots; their ring words and beta values requested
+  // before the first unit's state and rows go out, and placed after (units
+  // 0 and 1 were hinted into L2 before the wait)
   int ns = 0, nt = 0, fetched = 0;
   fetch_batch_a(p, smb, 0, cnt, lane);
-  const int early = cnt < kTStages ? cnt : kTStages;  // stages whose rows go out now
+  const WordsB w0 = load_words_b(p, smb, 0, cnt, lane);  // in flight meanwhile
+  // every copy takes the producer a while to issue: the first unit's state
+  // and rows now, its ring entries as soon as its words are placed, and only
+  // then the later units' copies
+  const int early = cnt > 0 ? 1 : 0;  // stages whose rows went out here
   if (cnt > 0) {
     issue_state(p, smap, smb, bars, 0, lane);
     s_last[0] = 0;
     ns = 1;
-    for (int n = 0; n < early; ++n) issue_rows(tmaps, smb, bars, n, p.H, lane);
+    issue_rows(tmaps, smb, bars, 0, p.H, lane);
   }
-  fetch_batch_b(p, smb, 0, cnt, lane);
+  place_words_b(p, smb, 0, cnt, lane, w0);
   fetched = cnt < kMetaBatch ? cnt : kMetaBatch;
   int idle = 0;
   while (ns < cnt || nt < cnt) {
@@ -1022,13 +1057,21 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     *reinterpret_cast<volatile int *>(smb + L::kAbort) = 0;
   }
   // Launched as a programmatic dependent of the previous kernel: until
-  // griddepcontrol.wait returns, only L2 prefetch hints for this CTA's first
+  // griddepcontrol.wait returns, only the tensor-map descriptor prefetches
+  // and L2 prefetch hints for this CTA's first
   // two units (state, ring word, ring beta, token rows), at the addresses the
   // slot table and segment offsets give when read (relaxed reads that the
   // previous kernel may still be writing: a stale value wastes a hint, and
   // L2 is where that kernel's writes become visible, so nothing stale is
   // used).
   if (warp == kProducerWarp) {
+    // lanes 8 .. 15: the tensor maps' descriptors, which a copy otherwise
+    // fetches at its first use, holding up the producer's first copies
+    if (lane >= 8 && lane < 16) {
+      const CUtensorMap *tm = lane == 8 ? &smap : &tmaps.k + (lane - 9);
+      asm volatile("prefetch.tensormap [%0];"
+                   :: "l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+    }
     // lanes 0, 1: the first two units' words and states; lanes 2, 3: their
     // token rows (k, alpha, v, q of each drafted position)
     const int n = lane & 1, u = blockIdx.x + n * gridDim.x;
@@ -1100,16 +1143,20 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// The pool as a 2-D fp32 tensor [P * H * PD rows][PD], boxes of 32 key
-// channels x PD value rows (128-byte rows) with the 128-byte swizzle.
+// The pool [P * H * PD value rows][PD key channels] fp32 as a 3-D tensor:
+// x = key channel within a group of 32 (128 bytes), y = value row (stride
+// PD * 4 bytes), z = group of 32 key channels (stride 128 bytes).  One box of
+// 32 x PD x 4 is a unit's whole state, landing as four 16 KB blocks (one per
+// group, z outermost) of 128-byte rows with the 128-byte swizzle: the same
+// bytes four 2-D boxes of 32 channels x PD rows would give, in one copy.
 cudaError_t state_map(CUtensorMap *tm, float *pool, int P, int H) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {(cuuint64_t)PD, (cuuint64_t)P * H * PD};
-  const cuuint64_t gstride[1] = {(cuuint64_t)PD * 4};
-  const cuuint32_t box[2] = {32, (cuuint32_t)PD};
-  const cuuint32_t estride[2] = {1, 1};
-  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pool, gdim, gstride, box,
+  const cuuint64_t gdim[3] = {32, (cuuint64_t)P * H * PD, PD / 32};
+  const cuuint64_t gstride[2] = {(cuuint64_t)PD * 4, 128};
+  const cuuint32_t box[3] = {32, (cuuint32_t)PD, PD / 32};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pool, gdim, gstride, box,
                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
