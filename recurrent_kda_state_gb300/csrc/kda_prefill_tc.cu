@@ -375,8 +375,7 @@ template <bool RAW>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
   extern __shared__ float4 smem4[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = umma::align1024(smem4);
   const uint32_t sb = umma::smem_u32(sm);
   float *bet = reinterpret_cast<float *>(sm + Lay::BET);
   float *sgm = reinterpret_cast<float *>(sm + Lay::GM);
@@ -946,8 +945,7 @@ template <bool RAW>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_tc_chunk_kernel(const PrefillParams p, const __grid_constant__ InputMaps maps) {
   extern __shared__ float4 smem4[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = umma::align1024(smem4);
   const uint32_t sb = umma::smem_u32(sm);
   float *bet = reinterpret_cast<float *>(sm + LayP::BET);
   float *sgm = reinterpret_cast<float *>(sm + LayP::GM);
@@ -1343,8 +1341,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const PrefillParams p) {
   extern __shared__ float4 smem4[];
-  uint8_t *sm = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sm = umma::align1024(smem4);
   const uint32_t sb = umma::smem_u32(sm);
   uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + LayS::MBAR);
   uint64_t *g1bar = reinterpret_cast<uint64_t *>(sm + LayS::G1);

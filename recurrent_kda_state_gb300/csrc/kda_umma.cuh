@@ -19,6 +19,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte aligned byte of a dynamic shared-memory array, reached
+// by an offset from the array itself rather than through an integer, so the
+// compiler still knows that pointers derived from it address shared memory.
+__device__ __forceinline__ unsigned char *align1024(void *smem) {
+  unsigned char *b = static_cast<unsigned char *>(smem);
+  return b + ((1024u - (smem_u32(b) & 1023u)) & 1023u);
+}
+
 // Shared-memory matrix descriptor: start address, leading byte offset (unused
 // for swizzled K-major tiles), stride byte offset between 8-row groups
 // (1024), descriptor version 1, 128-byte swizzle.

@@ -336,8 +336,7 @@ __global__ void __launch_bounds__(2 * D, 2)
     verify_kernel(const VerifyParams p) {
   constexpr int F = D / 16;
   extern __shared__ float4 smem4[];
-  unsigned char *smb = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  unsigned char *smb = umma::align1024(smem4);
   __shared__ int s_acc;  // accepted count to replay, -1: ring word invalid
   __shared__ uint64_t s_mbar;
   __shared__ uint32_t s_tmem;

@@ -1039,8 +1039,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                        const __grid_constant__ TokMaps tmaps) {
   typedef PipeLayout L;
   extern __shared__ float4 smem4[];
-  unsigned char *smb = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem4) + 1023) & ~(uintptr_t)1023);
+  unsigned char *smb = umma::align1024(smem4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int units = p.B * p.H;
   if (tid == 0) {
