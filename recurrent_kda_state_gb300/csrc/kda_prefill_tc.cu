@@ -1158,16 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mma_owed = false;
     {  // A = strict_tril(diag(beta) G_top) -> fp32;  M = tril(G_bottom) -> image
       float gv[32];
-      {
-        float g0[16], g1[16];
-        umma::tmem_ld16(tl + kAccG + 32 * hf, g0);
-        umma::tmem_ld16(tl + kAccG + 32 * hf + 16, g1);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          gv[e] = g0[e];
-          gv[16 + e] = g1[e];
-        }
-      }
+      umma::tmem_ld32(tl + kAccG + 32 * hf, gv);
       if (c < 64) {
         const int t = c;
         const float bt = bet[t];
@@ -1474,17 +1465,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     if (tid == 0 && got3 && q + 1 < nch) issue_g1(q + 1);  // [W~; Q~] is free; the other parity too
     if (c < 64) {  // U = U' - W S -> U^T tile (row j, k = t)
       const int t = c;
-      float ws[16], ws2[16];
-      umma::tmem_ld16(tl + kA3 + 16 * hf, ws);
-      umma::tmem_ld16(tl + kA3 + kNC + 16 * hf, ws2);
+      float ws[16];
+      umma::tmem_ld16_pair_sum(tl + kA3 + 16 * hf, tl + kA3 + kNC + 16 * hf, ws);
       const float4 *u4 = reinterpret_cast<const float4 *>(up + t * kNC);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {  // rotated chunks: 8 rows hit 8 bank groups
         const float4 uv = u4[(4 * hf + e + t) & 7];
-        ws[4 * e] = uv.x - (ws[4 * e] + ws2[4 * e]);
-        ws[4 * e + 1] = uv.y - (ws[4 * e + 1] + ws2[4 * e + 1]);
-        ws[4 * e + 2] = uv.z - (ws[4 * e + 2] + ws2[4 * e + 2]);
-        ws[4 * e + 3] = uv.w - (ws[4 * e + 3] + ws2[4 * e + 3]);
+        ws[4 * e] = uv.x - ws[4 * e];
+        ws[4 * e + 1] = uv.y - ws[4 * e + 1];
+        ws[4 * e + 2] = uv.z - ws[4 * e + 2];
+        ws[4 * e + 3] = uv.w - ws[4 * e + 3];
       }
       put16_mn(sm, LayS::UT, t, 16 * hf, ws);
     }
@@ -1514,24 +1504,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_pass_kernel(const Pref
     mma_owed = false;
     if (q + 1 < nch) issue_g2(q + 1);  // K^ and [T; M] are free
     {
-      float acc[16], acc2[16];
-      umma::tmem_ld16(tl + kA4 + 16 * hf, acc);
-      umma::tmem_ld16(tl + kA4 + kNC + 16 * hf, acc2);
+      // the increment's two halves, and (warps of rows 64..127) the outputs'
+      // two halves, loaded together with one wait
+      float acc[16], o[16];
+      if (c >= 64)
+        umma::tmem_ld16_pair_sum2(tl + kA4 + 16 * hf, tl + kA4 + kNC + 16 * hf,
+                                  tl + kA3 + 16 * hf, tl + kA3 + kNC + 16 * hf, acc, o);
+      else
+        umma::tmem_ld16_pair_sum(tl + kA4 + 16 * hf, tl + kA4 + kNC + 16 * hf, acc);
       const float a1 = vec[128 + c], a2 = vec[256 + c];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * (acc[jj] + acc2[jj]));
+      for (int jj = 0; jj < 16; ++jj) S[jj] = fmaf(a1, S[jj], a2 * acc[jj]);
       if (c >= 64) {  // outputs of row t = c - 64
-        float o[16], o2[16];
-        umma::tmem_ld16(tl + kA3 + 16 * hf, o);
-        umma::tmem_ld16(tl + kA3 + kNC + 16 * hf, o2);
         const int t = c - 64;
         if (t < n) {
           float4 *dst = reinterpret_cast<float4 *>(
               p.o + ((size_t)(tok0 + t) * H + h) * kD + col0 + 16 * hf);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(o[4 * e] + o2[4 * e], o[4 * e + 1] + o2[4 * e + 1],
-                                 o[4 * e + 2] + o2[4 * e + 2], o[4 * e + 3] + o2[4 * e + 3]);
+            dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
       }
     }
