@@ -20,7 +20,9 @@
 //       ring entries as three TMA boxes into one of three token stages, each
 //       as soon as its stage is free (the first unit's rows as soon as its
 //       segment is known), and an L2 hint for the next unit's state;
-//   prep (2 warps): as soon as a unit's token stage lands, for drafts: the
+//   prep (groups of 2 warps taking units in turn: one group on prepared
+//       inputs, two on projection-space inputs, see PipeRoles): as soon as a
+//       unit's token stage lands, for drafts: the
 //       decay products gamma_t, K~ = gamma k, Q~ = gamma q, K^ = k / gamma,
 //       the T x T pair products A = K^ K~^T, B = K^ Q~^T on the tensor cores,
 //       N = B (I + diag(beta) A)^-1 diag(beta) by back substitution, then
@@ -78,11 +80,25 @@ constexpr int PT = 8;                   // drafted rows per MMA tile (T <= 8)
 constexpr int kDepthMax = 8;            // ring entries a stage holds
 constexpr int kConsumerWarps = 8;       // 2 * PD threads: the state owners
 constexpr int kProducerWarp = 8;
-constexpr int kPrepWarp0 = 9, kPrepWarps = 3;
-constexpr int kPrepMath = 64;           // the two channel-pair prep warps; the third appends
-constexpr int kPipeThreads = 32 * (kConsumerWarps + 1 + kPrepWarps);
-constexpr int kPrepBar = 1;             // named barrier of the prep warps
-constexpr int kPrepChanBar = 2;         // ... of the two channel-pair prep warps
+// Prep groups of two channel-pair warps take units in turn; one more warp
+// appends to the ring.  On prepared inputs one group (twelve warps, three
+// per scheduler, so the consumers keep the registers they use); on
+// projection-space inputs, whose prep also normalises keys and maps the
+// decay and beta logits, two groups prepare two units at once (fourteen
+// warps put four on two schedulers, whose 16 K registers then cap every
+// thread at 128: slower consumers, paid for by the heavier prep's overlap).
+constexpr int kPrepWarp0 = 9;
+constexpr int kPrepMath = 64;           // a group's two channel-pair warps
+template <bool RAW>
+struct PipeRoles {
+  static constexpr int kGroups = RAW ? 2 : 1;
+  static constexpr int kRingWarp = kPrepWarp0 + 2 * kGroups;
+  static constexpr int kPrepWarps = 2 * kGroups + 1;  // with the ring warp
+  static constexpr int kThreads = 32 * (kConsumerWarps + 1 + kPrepWarps);
+};
+// named barriers of group g: kPrepBar + 2 g (its 64 threads), kPrepChanBar + 2 g
+constexpr int kPrepBar = 1;
+constexpr int kPrepChanBar = 2;
 constexpr int kTStages = 3;             // token stages
 constexpr int kSStages = 2;             // state stages
 constexpr int kMetaBatch = 32;          // units whose words one lane each reads at once
@@ -166,6 +182,8 @@ struct PipeLayout {
   static constexpr int kTotal = kAbort + 16 + 1024;  // + alignment slack
 };
 static_assert(PipeLayout::kTotal <= 227 * 1024, "verify pipeline shared memory");
+static_assert(kPrepChanBar + 2 * (PipeRoles<true>::kGroups - 1) <= 15,
+              "the prep groups' named barrier ids (0 is the CTA barrier)");
 static_assert(R::kBytes % 16 == 0, "records must keep 16-byte alignment");
 static_assert(PipeLayout::kTsRk % 16 == 0 && PipeLayout::kTsFrag % 16 == 0,
               "token stage parts must keep 16-byte alignment");
@@ -674,9 +692,16 @@ __device__ void ring_append(const VerifyParams &p, unsigned char *smb, int lane,
   }
 }
 
-// The drafts' operands, by the two channel-pair prep warps (pt < 64).
+// The drafts' operands of units grp, grp + PipeRoles<RAW>::kGroups, ..., by prep group
+// grp's two channel-pair warps (pt < 64).  Every group walks every unit in
+// order: it waits for each unit's token stage and arrives on its release
+// (tempty), working only on its own units.  A parity wait cannot tell a
+// stage barrier's phase from the one two after it; with every group among
+// the releases, no stage is refilled before each group has seen its
+// previous use, so no group's wait is ever two phases behind.
 template <bool RAW>
-__device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limit) {
+__device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int grp, int limit) {
+  const int bar = kPrepBar + 2 * grp, chan_bar = kPrepChanBar + 2 * grp;
   typedef PipeLayout L;
   const Bars bars(smb);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smb + L::kAbort);
@@ -688,13 +713,18 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
     // both prep warps take the same decision before any named barrier
     bool go = !stopping(abort_flag);
     if (go) go = pipe_wait(&bars.tfull[k], n / kTStages, limit, abort_flag, p.err);
-    if (!named_and(kPrepBar, kPrepMath, go)) break;
+    if (!named_and(bar, kPrepMath, go)) break;
+    if (n % PipeRoles<RAW>::kGroups != grp) {  // another group's unit: only its release
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.tempty[k]);
+      continue;
+    }
     unsigned char *ts = smb + L::kTStages0 + k * L::kTStage;
     const UnitMeta m = *reinterpret_cast<const UnitMeta *>(ts + L::kTsMeta);
     const bool drafts = !m.skip && m.spec && m.T > 0;
     if (RAW && !m.skip && !drafts && m.T > 0) {  // drafts: prepared in the first phase
       prep_raw_rows(reinterpret_cast<bf16 *>(ts + L::kTsRec), m.T, pt >> 5, lane);
-      named_sync(kPrepBar, kPrepMath);
+      named_sync(bar, kPrepMath);
     }
     if (drafts) {
       const bf16 *rec = reinterpret_cast<const bf16 *>(ts + L::kTsRec);
@@ -744,7 +774,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
             const float x = lane_tree(pair_sq(kv[t]));
             if (lane == 0) nh[(pt >> 5) * PT + t] = x;
           }
-          named_sync(kPrepChanBar, 2 * 32);
+          named_sync(chan_bar, 2 * 32);
           bf16 *rw = const_cast<bf16 *>(rec);
 #pragma unroll
           for (int t = 0; t < PT; ++t) {
@@ -778,7 +808,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
         bf16 *rb = const_cast<bf16 *>(rec) + R::kB + pt;
         *rb = __float2bfloat16_rn(beta_of_logit(__bfloat162float(*rb)));
       }
-      unsafe = named_or(kPrepBar, kPrepMath, unsafe);
+      unsafe = named_or(bar, kPrepMath, unsafe);
       if (!unsafe) {
         // the pair products on the tensor cores, one prep warp each:
         // D row s, column t = K^_s . K~_t (warp 0: A) or K^_s . Q~_t (B)
@@ -840,7 +870,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
           }
         }
       }
-      named_sync(kPrepBar, kPrepMath);
+      named_sync(bar, kPrepMath);
       // N = B M with M = (I + L)^-1 diag(beta), L = diag(beta) A strictly
       // lower (the drafts' corrections are delta = M (v - S^T K~), so that
       // o = S^T Q~ + N (v - S^T K~)).  Row r of Y = B (I + L)^-1 solves
@@ -870,7 +900,7 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int limi
 #pragma unroll
         for (int q = 0; q < PT; ++q) nm[r * PT + q] = y[q] * bt[q];
       }
-      named_sync(kPrepBar, kPrepMath);
+      named_sync(bar, kPrepMath);
       // Q^ = Q~ - N K~ (fragments, over Q~'s) and W = N v (fp32, over K^'s):
       // o_t = (S^T Q^)_t + W_t
       float *wv = reinterpret_cast<float *>(fragb + 2 * 4096);
@@ -1034,7 +1064,7 @@ __device__ void consumer(const VerifyParams &p, unsigned char *smb, int tid, int
 }
 
 template <bool RAW>
-__global__ void __launch_bounds__(kPipeThreads, 1)
+__global__ void __launch_bounds__(PipeRoles<RAW>::kThreads, 1)
     verify_pipe_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap smap,
                        const __grid_constant__ TokMaps tmaps) {
   typedef PipeLayout L;
@@ -1051,7 +1081,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     for (int i = 0; i < kTStages; ++i) {
       umma::mbar_init(&b.tfull[i], 32 + 1);  // async arrivals of the lanes + lane 0
       umma::mbar_init(&b.pfull[i], kPrepMath);
-      umma::mbar_init(&b.tempty[i], kConsumerWarps + kPrepWarps);
+      // per use: the consumers, every prep warp and the ring warp
+      umma::mbar_init(&b.tempty[i], kConsumerWarps + PipeRoles<RAW>::kPrepWarps);
     }
     *reinterpret_cast<volatile int *>(smb + L::kAbort) = 0;
   }
@@ -1112,8 +1143,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int limit = p.spin_limit;
   if (warp == kProducerWarp) producer(p, &smap, &tmaps, smb, lane, limit);
-  else if (warp >= kPrepWarp0 + kPrepMath / 32) ring_append(p, smb, lane, limit);
-  else if (warp >= kPrepWarp0) prep<RAW>(p, smb, tid - 32 * kPrepWarp0, limit);
+  else if (warp == PipeRoles<RAW>::kRingWarp) ring_append(p, smb, lane, limit);
+  else if (warp >= kPrepWarp0) {
+    const int grp = (warp - kPrepWarp0) >> 1;
+    prep<RAW>(p, smb, tid - 32 * (kPrepWarp0 + 2 * grp), grp, limit);
+  }
   else consumer<RAW>(p, smb, tid, limit);
   __syncthreads();
 }
@@ -1232,7 +1266,7 @@ cudaError_t launch_verify_pipe(const VerifyParams &p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kPipeThreads);
+  cfg.blockDim = dim3(p.raw ? PipeRoles<true>::kThreads : PipeRoles<false>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
