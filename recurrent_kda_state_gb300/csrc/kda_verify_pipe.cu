@@ -755,14 +755,23 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int grp,
       if (chan) {
         // every load first (the stores below could alias them for the
         // compiler), then gamma, K~, Q~, K^ and their fragments
+        // (all PT rows are loaded -- the stage holds them, past T other
+        // tokens or stale bytes -- and the rows past T replaced after, so
+        // no load waits on a branch)
         float2 av[PT], kv[PT], qv[PT];
 #pragma unroll
         for (int t = 0; t < PT; ++t) {
           const bf16 *rr = rec + t * R::kStride;
-          const bool in = t < T;
-          av[t] = in ? ld2(rr + R::kA + c) : make_float2(1.f, 1.f);
-          kv[t] = in ? ld2(rr + R::kK + c) : make_float2(0.f, 0.f);
-          qv[t] = in ? ld2(rr + R::kQ + c) : make_float2(0.f, 0.f);
+          av[t] = ld2(rr + R::kA + c);
+          kv[t] = ld2(rr + R::kK + c);
+          qv[t] = ld2(rr + R::kQ + c);
+        }
+#pragma unroll
+        for (int t = 0; t < PT; ++t) {
+          if (t >= T) {
+            av[t] = make_float2(1.f, 1.f);
+            kv[t] = qv[t] = make_float2(0.f, 0.f);
+          }
         }
         if (RAW) {
           // projection-space rows: the squared key norms (this warp's half of
