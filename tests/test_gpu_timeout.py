@@ -117,3 +117,52 @@ def test_prefill_wait_runs_out_writes_nothing(single_pass):
     for s in (2, 4, 5):
         assert_states(from_gpu_states(pool.data[s]), sess.pool[s])
     assert K.kda_get_device_error() == 0
+
+
+def test_verify_raw_wait_runs_out_writes_nothing():
+    """The projection-space verify (two prep groups on alternate units) with
+    a zero wait limit, on a ring with pending accepted entries: TIMEOUT is
+    set and outputs, states, ring payload and control words are untouched;
+    with the default limit the same call gives the oracle's outputs and
+    states from the inputs the oracle prepared."""
+    from test_gpu_verify_raw import raw_tokens_clear_of_ties
+    rng = np.random.default_rng(6300)
+    B, H, P, T = 12, 16, 24, 8
+    slots_np = ki.slot_table(rng, B, P)
+    slots = i32(slots_np)
+    init = (rng.standard_normal((P, H, 128, 128)) * 0.05).astype(np.float32)
+    pool = K.StatePool(to_gpu_states(init).cuda())
+    ring = K.ReplayRing(P, H, 128, T, torch.bfloat16)
+    sess = oracle.OracleSession(P, H, 128, 128, init=init.astype(np.float64))
+    raw0, prep0 = raw_tokens_clear_of_ties(rng, [T] * B, H)
+    a0 = ki.accepted_uniform(rng, B, T)
+    K.kda_verify(device_batch(raw0, "bf16"), T, pool, slots, ring, raw=True)
+    K.kda_commit(i32(a0), slots, pool, ring)
+    sess.verify(prep0, slots_np)
+    sess.commit(a0, slots_np)
+    torch.cuda.synchronize()
+    assert K.kda_get_device_error() == 0
+
+    raw, prep = raw_tokens_clear_of_ties(rng, [T] * B, H)
+    tb = device_batch(raw, "bf16")
+    snap = {n: getattr(ring, n).clone() for n in ("k", "v", "alpha", "beta", "ctrl")}
+    pool_before = pool.data.clone()
+    tb.o.fill_(float("nan"))
+    K.kda_set_wait_limit(0)
+    K.kda_verify(tb, T, pool, slots, ring, raw=True)
+    bits = K.kda_get_device_error()
+    K.kda_set_wait_limit(-1)
+    assert bits & K.KDA_DERR_TIMEOUT
+    assert not bits & K.KDA_DERR_UNSAFE
+    assert torch.isnan(tb.o).all()
+    assert torch.equal(pool.data, pool_before)
+    for n, t in snap.items():
+        assert torch.equal(getattr(ring, n), t), n
+
+    K.kda_verify(tb, T, pool, slots, ring, raw=True)
+    o_ref = sess.verify(prep, slots_np)
+    assert_outputs(tb.o.cpu().numpy(), o_ref)
+    K.kda_materialize(slots, pool, ring)
+    for s in slots_np:
+        assert_states(from_gpu_states(pool.data[s]), sess.pool[s])
+    assert K.kda_get_device_error() == 0
