@@ -899,12 +899,13 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int grp,
         for (int t = 1, i = 0; t < PT; ++t)
 #pragma unroll
           for (int q = 0; q < t; ++q, ++i) lv[i] = t < T ? bt[t] * am[t * PT + q] : 0.f;
+        // column by column: once Y[r][t] is known it leaves every column
+        // s < t at once, so the dependent chain is one FMA per column
 #pragma unroll
-        for (int sc = PT - 1; sc >= 0; --sc) {
-          float acc = br[sc];
+        for (int t = PT - 1; t >= 0; --t) {
+          y[t] = br[t];
 #pragma unroll
-          for (int t = sc + 1; t < PT; ++t) acc = fmaf(-y[t], lv[t * (t - 1) / 2 + sc], acc);
-          y[sc] = acc;
+          for (int q = 0; q < t; ++q) br[q] = fmaf(-y[t], lv[t * (t - 1) / 2 + q], br[q]);
         }
 #pragma unroll
         for (int q = 0; q < PT; ++q) nm[r * PT + q] = y[q] * bt[q];
@@ -918,8 +919,10 @@ __device__ void prep(const VerifyParams &p, unsigned char *smb, int pt, int grp,
         float2 vv[PT];
         float nn[PT * (PT + 1) / 2];
 #pragma unroll
+        for (int u = 0; u < PT; ++u) vv[u] = ld2(rec + u * R::kStride + R::kV + c);
+#pragma unroll
         for (int u = 0; u < PT; ++u)
-          vv[u] = u < T ? ld2(rec + u * R::kStride + R::kV + c) : make_float2(0.f, 0.f);
+          if (u >= T) vv[u] = make_float2(0.f, 0.f);  // rows past T: other tokens
 #pragma unroll
         for (int t = 0, i = 0; t < PT; ++t)
 #pragma unroll
